@@ -1,0 +1,152 @@
+"""Pins for the oracle's dot products and reductions (CPU only).
+
+Brute force with exact rational arithmetic, closed forms, the hand-worked
+2x64 example, and tie rules.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from golden_io import hexbytes, load, nf4_codebook_fixture
+
+
+def _exact_dot(row, col):
+    return sum(Fraction(float(a)) * Fraction(float(b)) for a, b in zip(row, col))
+
+
+@pytest.mark.parametrize("n,k,m", [(1, 8, 1), (2, 16, 3), (3, 64, 2), (7, 16, 1), (5, 8, 4)])
+def test_dense_brute_force_fractions(n, k, m):
+    rng = np.random.default_rng(100 + n * k + m)
+    w = rng.standard_normal((n, k)).astype(np.float16)
+    x = rng.standard_normal((m, k)).astype(np.float16)
+    y = oracle.gemv_dense(w, x)
+    assert y.shape == (m, n)
+    for mm in range(m):
+        for nn in range(n):
+            ref = _exact_dot(w[nn], x[mm])
+            assert abs(y[mm, nn] - float(ref)) <= 1e-13 * max(1.0, float(sum(
+                abs(Fraction(float(a)) * Fraction(float(b))) for a, b in zip(w[nn], x[mm]))))
+    a = oracle.abs_dot_dense(w, x)
+    assert np.all(a >= np.abs(y) - 1e-12)
+
+
+def test_dense_closed_forms():
+    k = 64
+    w = np.ones((3, k), np.float16)
+    x = (np.arange(k) % 4).astype(np.float16)
+    assert np.array_equal(oracle.gemv_dense(w, x)[0], np.full(3, 96.0))   # 1.5 K
+    # identity: y = x exactly
+    xi = np.random.default_rng(5).standard_normal(16).astype(np.float16)
+    assert np.array_equal(oracle.gemv_dense(np.eye(16, dtype=np.float16), xi)[0], xi.astype(np.float64))
+    # W[n, k] = n (non-square): a transposed operand would give K(K-1)/2 instead of n K
+    n, k = 5, 12
+    w = np.repeat(np.arange(n, dtype=np.float16)[:, None], k, axis=1)
+    y = oracle.gemv_dense(w, np.ones(k, np.float16))[0]
+    assert np.array_equal(y, np.arange(n) * float(k))
+
+
+def test_q4_0_q8_1_h4_hand_example():
+    g = load("q4_0_q8_1_h4.json")
+    w = np.empty((2, 64), np.float32)
+    w[0] = np.tile(np.array([-1.0, 0.5], np.float32), 32)
+    w[1] = 0.5
+    w[1, 0] = 1.0
+    w[1, 32] = 1.0
+    q4, d4 = oracle.quantize_q4_0(w)
+    qs = oracle.pack_q4_0(q4)
+    q8, d8, s8 = oracle.quantize_q8_1(np.ones((1, 64), np.float32))
+    sumi = oracle.q4_0_q8_1_blockdots(qs, q8)
+    assert sumi.dtype == np.int32
+    assert np.array_equal(sumi[0], np.asarray(g["sumi"]))
+    y = oracle.gemv_q4_0_q8_1(qs, d4, q8, d8)
+    assert list(y[0]) == g["y"]                         # exact in binary
+    # ~ the unquantised sum of w (quantisation error only)
+    assert abs(y[0, 1] - w[1].sum()) < 0.01
+
+
+def test_q4_0_q8_1_against_dequantised_fractions():
+    rng = np.random.default_rng(200)
+    n, k, m = 3, 96, 2
+    w = (rng.standard_normal((n, k)) * 0.02).astype(np.float32)
+    x = rng.standard_normal((m, k)).astype(np.float32)
+    q4, d4 = oracle.quantize_q4_0(w)
+    qs = oracle.pack_q4_0(q4)
+    q8, d8, _ = oracle.quantize_q8_1(x)
+    y = oracle.gemv_q4_0_q8_1(qs, d4, q8, d8)
+    sumi = oracle.q4_0_q8_1_blockdots(qs, q8)
+    # independent route: per element, dequantise both operands exactly and sum
+    for mm in range(m):
+        for nn in range(n):
+            acc = Fraction(0)
+            for kk in range(k):
+                b = kk // 32
+                wv = Fraction(float(d4[nn, b])) * (int(q4[nn, kk]) - 8)
+                xv = Fraction(float(d8[mm, b])) * int(q8[mm, kk])
+                acc += wv * xv
+            assert abs(y[mm, nn] - float(acc)) <= 1e-12 * max(1.0, abs(float(acc)))
+            for b in range(k // 32):
+                s = sum((int(q4[nn, kk]) - 8) * int(q8[mm, kk]) for kk in range(32 * b, 32 * b + 32))
+                assert sumi[mm, nn, b] == s
+    ad = oracle.abs_dot_q4_0_q8_1(qs, d4, q8, d8)
+    ref = np.abs(oracle.dequantize_q4_0(qs, d4)) @ np.abs(d8.astype(np.float64).repeat(32, 1) * q8).T
+    assert np.allclose(ad, ref.T, rtol=1e-12)
+
+
+def test_nf4_gemv_against_dequantised_fractions():
+    cb = nf4_codebook_fixture()
+    rng = np.random.default_rng(300)
+    n, k = 4, 128
+    import torch
+    w = torch.from_numpy((rng.standard_normal((n, k)) * 0.02).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    x = torch.from_numpy(rng.standard_normal(k).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    codes, absmax = oracle.quantize_nf4(w, cb)
+    qs = oracle.pack_nf4(codes)
+    y = oracle.gemv_nf4(qs, absmax, cb, x)[0]
+    for nn in range(n):
+        acc = Fraction(0)
+        for kk in range(k):
+            acc += Fraction(float(absmax[nn, kk // 64])) * Fraction(float(cb[codes[nn, kk]])) * Fraction(float(x[kk]))
+        assert abs(y[nn] - float(acc)) <= 1e-13 * max(1.0, abs(float(acc)))
+    ad = oracle.abs_dot_nf4(qs, absmax, cb, x)[0]
+    assert np.allclose(ad, np.abs(oracle.dequantize_nf4(qs, absmax, cb)) @ np.abs(x.astype(np.float64)))
+
+
+def test_nf4_gemv_h5_block_with_unit_x():
+    # the H5 block (levels in order, absmax 1) dotted with ones = 4 * sum(cb)
+    cb = nf4_codebook_fixture()
+    qs = hexbytes(load("nf4_h5.json")["qs_hex"])[None, :]
+    y = oracle.gemv_nf4(qs, np.ones((1, 1), np.float32), cb, np.ones(64, np.float32))
+    assert y[0, 0] == pytest.approx(4 * float(np.sum(cb.astype(np.float64))), abs=1e-12)
+
+
+def test_argmax_h6():
+    for case in load("argmax_h6.json")["cases"]:
+        row = np.asarray(case["row"], dtype=np.float32)
+        assert oracle.argmax_rows(row)[0] == case["argmax"], case["why"]
+
+
+def test_argmax_rows_identical_columns_and_far_ties():
+    rng = np.random.default_rng(7)
+    base = rng.standard_normal(1000).astype(np.float32)
+    base[0] = base[999] = base.max() + 1          # equal maxima at both ends
+    lg = np.tile(base, (32, 1))
+    assert np.all(oracle.argmax_rows(lg) == 0)
+
+
+def test_xor_words_hand_cases():
+    for case in load("xor_words.json")["cases"]:
+        assert int(oracle.xor_words(hexbytes(case["bytes_hex"]))) == int(case["xor"], 16)
+
+
+def test_xor_words_is_order_free_and_self_inverse():
+    rng = np.random.default_rng(8)
+    b = rng.integers(0, 256, 4096, dtype=np.uint8)
+    x = int(oracle.xor_words(b))
+    words = b.view('<u4')
+    acc = 0
+    for wv in words[::-1]:
+        acc ^= int(wv)
+    assert acc == x
+    assert int(oracle.xor_words(np.concatenate([b, b]))) == 0
