@@ -1,0 +1,894 @@
+#!/usr/bin/env python3
+"""Decode-GEMV benchmark: one JSON line per run.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl wobs|reference]
+
+A step is one pass of the decode path over one batch of synthetic input.
+The default workload is the Q4_0 x Q8_1 M = 1 decode of an 8B model's four
+projection shapes (4096x4096, 1024x4096, 14336x4096, 4096x14336): per
+shape, quantise the fp32 activation vector to Q8_1 and run the GEMV.  The
+weights are rotated over enough seeded copies that the working set exceeds
+1.07 GB (the batch1-cdna README rotates 32 copies of a 4096^2 fp16 matrix
+for the same reason), so every step reads its weights from HBM, not L2.
+
+Other workloads (``--workload``): fp16_4096 (dense fp16 4096x4096), nf4
+(NF4 28672x8192), q4_m_sweep (Q4_0 x Q8_1 for M in {1,..,32} on 4096x4096
+and 14336x4096), lm_head (bf16 128000x4096 with fused argmax, M = 1 and 32).
+
+Timing: W untimed warm-up steps, then exactly K steps between CUDA events
+on the launching stream, bracketed by a barrier and a device synchronise;
+the steps are replayed from CUDA graphs (one graph per rotation cycle of
+the weight copies, single-step graphs for a remainder).  The
+``value`` is bytes counted from the method (each weight, scale,
+activation and output byte once) divided by the measured time.
+
+``--impl reference`` times the CPU oracle instead (host cores, a row
+sample of the same workload per step).  With N > 1 every rank runs an
+independent replica (the path has no exchange step), ``value`` is the sum
+over ranks divided by the slowest rank's time.
+"""
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "M=1 GEMV µs/call and HBM GB/s as % of measured GB300 read ceiling (MBU)"
+ROTATE_BYTES = 1.07e9
+PROBE_BYTES = 8 << 30          # streaming-read ceiling buffer (>> L2)
+
+# ----------------------------------------------------------------- dist
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(backend):
+    import torch.distributed as dist
+    if dist.is_available() and not dist.is_initialized() and int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        dist.init_process_group(backend=backend)
+
+
+def _dist_on():
+    import torch.distributed as dist
+    return dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if _dist_on():
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_over_ranks(value, op, device=None):
+    """MAX or SUM of a float over ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not _dist_on():
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate(per_rank_bytes, per_rank_ms, device=None):
+    """Whole-job throughput: bytes of all ranks / the slowest rank's time."""
+    total = reduce_over_ranks(per_rank_bytes, "sum", device)
+    ms = reduce_over_ranks(per_rank_ms, "max", device)
+    return total / (ms * 1e-3) / 1e9, ms
+
+
+# --------------------------------------------------------------- clocks
+
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+            0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+            0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """SM clock and clock-event reasons sampled during the timed region.
+
+    NVML through ctypes (every ~2 ms); ``nvidia-smi -lms 100`` if NVML is not
+    loadable.  Reading clocks changes nothing on the GPU.
+    """
+
+    def __init__(self, device):
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thr = None
+        self._proc = None
+        self._nvml = None
+        self._handle = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                ok = False
+                props = torch.cuda.get_device_properties(device)
+                if hasattr(props, "pci_bus_id"):
+                    bus = f"{getattr(props, 'pci_domain_id', 0):08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+                    ok = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+                if not ok:
+                    ok = lib.nvmlDeviceGetHandleByIndex_v2(self._nvml_index(device), ctypes.byref(h)) == 0
+                if ok:
+                    self._nvml, self._handle = lib, h
+                    m = ctypes.c_uint()
+                    if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(m)) == 0:
+                        self.max_mhz = int(m.value)
+        except OSError:
+            self._nvml = None
+        self._index = self._nvml_index(device)
+
+    @staticmethod
+    def _nvml_index(device):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        parts = [p for p in vis.split(",") if p.strip()]
+        if parts and all(p.strip().isdigit() for p in parts):
+            return int(parts[device.index].strip())
+        return device.index
+
+    def _poll(self):
+        lib, h = self._nvml, self._handle
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        get_r = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(c)) == 0 and get_r(h, ctypes.byref(r)) == 0:
+                self.samples.append((int(c.value), int(r.value)))
+            time.sleep(0.002)
+
+    def start(self):
+        if self._nvml is not None:
+            self._thr = threading.Thread(target=self._poll, daemon=True)
+            self._thr.start()
+        else:
+            q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active")
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self._index), f"--query-gpu={q}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self._proc = None
+
+    def stop(self):
+        if self._thr is not None:
+            self._stop.set()
+            self._thr.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate(timeout=10)
+            for line in out.splitlines():
+                p = [s.strip() for s in line.split(",")]
+                try:
+                    self.samples.append((int(float(p[0])), int(p[2], 16)))
+                    self.max_mhz = int(float(p[1]))
+                except (ValueError, IndexError):
+                    pass
+
+    def report(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        seen = 0
+        for _, r in self.samples:
+            seen |= r
+        names = [n for b, n in _REASONS.items() if seen & b and b != 0x1]
+        return {"sm_mhz": statistics.median(s for s, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------- timing
+
+
+def time_steps(cycle, singles, steps, stream):
+    """Run exactly ``steps`` steps: whole rotation cycles from one graph, then
+    single-step graphs for the remainder.  Milliseconds on ``stream``."""
+    q, r = divmod(steps, len(singles))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(q):
+            cycle.replay()
+        for i in range(r):
+            singles[i].replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def read_ceiling(device, stream):
+    """Best streaming-read GB/s over load variants and grid sizes (bw_probe)."""
+    import weight_only_bit_split_gb300 as wobs
+    buf = torch.empty(PROBE_BYTES, dtype=torch.uint8, device=device)
+    buf.fill_(0x5A)
+    out = torch.zeros(1, dtype=torch.int32, device=device)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    best = (0.0, None)
+    table = []
+    with torch.cuda.stream(stream):
+        for variant in (1, 2, 3):
+            for per_sm in (1, 2, 4, 8):
+                grid = sms * per_sm
+                wobs.wobs_bw_probe(buf, grid=grid, variant=variant, xor_out=out)
+                ts = []
+                for _ in range(5):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    wobs.wobs_bw_probe(buf, grid=grid, variant=variant, xor_out=out)
+                    e1.record(stream)
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1))
+                gbs = PROBE_BYTES / (statistics.median(ts) * 1e-3) / 1e9
+                table.append({"variant": variant, "grid": grid, "gbs": round(gbs, 1)})
+                if gbs > best[0]:
+                    best = (gbs, {"variant": variant, "grid": grid})
+    if wobs.wobs_error_word(device) != 0:
+        raise RuntimeError("bw_probe reported a device error")
+    del buf
+    torch.cuda.empty_cache()
+    return best[0], best[1], table
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_record(kernel):
+    """ncu DRAM bytes per launch for ``kernel`` if recorded for the current source."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    recs = {}
+    for line in open(p):
+        if line.startswith("#") or not line.strip():
+            continue
+        parts = line.split()
+        if len(parts) >= 4:
+            recs[parts[0]] = (parts[1], parts[2], parts[3])
+    if kernel not in recs:
+        return None
+    src, digest, per_launch = recs[kernel]
+    path = os.path.join(ROOT, "weight_only_bit_split_gb300", "csrc", src)
+    if not os.path.exists(path):
+        return None
+    if hashlib.sha256(open(path, "rb").read()).hexdigest()[:16] != digest:
+        return None
+    return float(per_launch)
+
+
+# ------------------------------------------------------------ workloads
+
+
+class Q4M1:
+    """Q4_0 x Q8_1, M = 1, the four 8B projection shapes."""
+    name = "q4_0_q8_1_m1_8b_shapes"
+    shapes = [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)]
+    dtype = "int8"
+    kernel = "q4_0_q8_1_m1"
+    kernel_src = "q4_0.cu"
+    workload_id = 2
+
+    def __init__(self, device):
+        import weight_only_bit_split_gb300 as wobs
+        from weight_only_bit_split_gb300 import synth
+        self.wobs = wobs
+        wbytes = sum(0.5625 * n * k for n, k in self.shapes)
+        self.copies = max(1, math.ceil(ROTATE_BYTES / wbytes))
+        self.planes = []
+        for c in range(self.copies):
+            row = []
+            for n, k in self.shapes:
+                w = synth.weights(self.workload_id, (n, k), copy=c, device=device)
+                row.append(wobs.wobs_quantize_q4_0(w))
+                del w
+            self.planes.append(row)
+        self.x = [synth.activations(self.workload_id, (1, k), device=device) for _, k in self.shapes]
+        self.xq = [torch.empty(1, k // 32 * 36, dtype=torch.uint8, device=device) for _, k in self.shapes]
+        self.y = [torch.empty(1, n, dtype=torch.float32, device=device) for n, _ in self.shapes]
+        torch.cuda.synchronize(device)
+
+    @staticmethod
+    def gemv_bytes(n, k):
+        return int(0.5625 * n * k) + 36 * k // 32 + 4 * n
+
+    @staticmethod
+    def quant_bytes(k):
+        return 4 * k + 36 * k // 32
+
+    def bytes_per_step(self):
+        return sum(self.gemv_bytes(n, k) + self.quant_bytes(k) for n, k in self.shapes)
+
+    launches_per_step = 8
+
+    def step(self, c):
+        w = self.wobs
+        for s in range(len(self.shapes)):
+            w.wobs_quantize_q8_1(self.x[s], self.xq[s])
+            qs, d = self.planes[c][s]
+            w.wobs_gemv_q4_0_q8_1(qs, d, self.xq[s], y=self.y[s])
+
+    def kernel_calls(self):
+        """(label, bytes, fn(copy)) for each launch of the dominant kernel."""
+        out = []
+        for s, (n, k) in enumerate(self.shapes):
+            def fn(c, s=s):
+                qs, d = self.planes[c][s]
+                self.wobs.wobs_gemv_q4_0_q8_1(qs, d, self.xq[s], y=self.y[s])
+            out.append((f"{n}x{k}", self.gemv_bytes(n, k), fn))
+        return out
+
+    def e2e_setup(self):
+        self.xh = [x.cpu().pin_memory() for x in self.x]
+        self.yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in self.y]
+        return sum(x.numel() * 4 for x in self.xh), sum(y.numel() * 4 for y in self.yh)
+
+    def e2e_step(self, c):
+        w = self.wobs
+        for s in range(len(self.shapes)):
+            self.x[s].copy_(self.xh[s], non_blocking=True)
+            w.wobs_quantize_q8_1(self.x[s], self.xq[s])
+            qs, d = self.planes[c][s]
+            w.wobs_gemv_q4_0_q8_1(qs, d, self.xq[s], y=self.y[s])
+            self.yh[s].copy_(self.y[s], non_blocking=True)
+
+    def config(self):
+        return {"workload": self.name, "shapes_NxK": [f"{n}x{k}" for n, k in self.shapes], "M": 1,
+                "step": "per shape: quantize_q8_1(x) then gemv_q4_0_q8_1",
+                "weight_copies": self.copies,
+                "working_set_gb": round(self.copies * sum(0.5625 * n * k for n, k in self.shapes) / 1e9, 3),
+                "l2": "inputs larger than L2: rotated weight copies, working set above 1 GB"}
+
+    # ---- oracle (CPU) ----
+    @classmethod
+    def oracle_prepare(cls, frac):
+        import oracle
+        from weight_only_bit_split_gb300 import synth
+        prep = []
+        for n, k in cls.shapes:
+            rows = max(1, int(round(n * frac)))
+            w = synth.weights(cls.workload_id, (rows, k)).numpy()
+            q4, d4 = oracle.quantize_q4_0(w)
+            x = synth.activations(cls.workload_id, (1, k)).numpy()
+            prep.append((oracle.pack_q4_0(q4), d4, x, rows, k))
+        return prep
+
+    @classmethod
+    def oracle_step(cls, prep):
+        import oracle
+        nbytes = 0
+        for qs, d4, x, rows, k in prep:
+            q8, d8, _ = oracle.quantize_q8_1(x)
+            oracle.gemv_q4_0_q8_1(qs, d4, q8, d8)
+            nbytes += cls.gemv_bytes(rows, k) + cls.quant_bytes(k)
+        return nbytes
+
+
+class Q4Sweep(Q4M1):
+    """Q4_0 x Q8_1 for M in {1, 2, 4, 8, 12, 16, 24, 32} on two shapes."""
+    name = "q4_0_q8_1_m_sweep"
+    shapes = [(4096, 4096), (14336, 4096)]
+    Ms = (1, 2, 4, 8, 12, 16, 24, 32)
+    kernel = "q4_0_q8_1 (m1 / mn)"
+    workload_id = 4
+
+    def __init__(self, device):
+        super().__init__(device)
+        from weight_only_bit_split_gb300 import synth
+        k = self.shapes[0][1]
+        self.X = {m: synth.activations(self.workload_id, (m, k), copy=m, device=device) for m in self.Ms}
+        self.XQ = {m: torch.empty(m, k // 32 * 36, dtype=torch.uint8, device=device) for m in self.Ms}
+        self.Y = {(m, s): torch.empty(m, n, dtype=torch.float32, device=device)
+                  for m in self.Ms for s, (n, _) in enumerate(self.shapes)}
+        self.ws = {(m, s): self.wobs.workspace(self.wobs.OP_GEMV_Q4_0_Q8_1, m, n, k, device)
+                   for m in self.Ms for s, (n, _) in enumerate(self.shapes)}
+        self.ws = {key: (torch.zeros_like(v) if v is not None else None) for key, v in self.ws.items()}
+
+    @staticmethod
+    def gemv_bytes_m(n, k, m):
+        return int(0.5625 * n * k) + m * 36 * k // 32 + 4 * m * n
+
+    def bytes_per_step(self):
+        k = self.shapes[0][1]
+        return sum(self.gemv_bytes_m(n, k, m) for m in self.Ms for n, _ in self.shapes) + \
+            sum(m * self.quant_bytes(k) for m in self.Ms)
+
+    launches_per_step = len(Ms) * 3
+
+    def _gemv(self, c, s, m):
+        qs, d = self.planes[c][s]
+        ws = self.ws[(m, s)]
+        self.wobs.wobs_gemv_q4_0_q8_1(qs, d, self.XQ[m], y=self.Y[(m, s)], ws=ws)
+
+    def step(self, c):
+        for m in self.Ms:
+            self.wobs.wobs_quantize_q8_1(self.X[m], self.XQ[m])
+            for s in range(len(self.shapes)):
+                self._gemv(c, s, m)
+
+    def kernel_calls(self):
+        out = []
+        for m in self.Ms:
+            for s, (n, k) in enumerate(self.shapes):
+                out.append((f"M{m}_{n}x{k}", self.gemv_bytes_m(n, k, m),
+                            lambda c, s=s, m=m: self._gemv(c, s, m)))
+        return out
+
+    def e2e_setup(self):
+        self.xh = {m: x.cpu().pin_memory() for m, x in self.X.items()}
+        self.yh = {key: torch.empty(y.shape, dtype=y.dtype).pin_memory() for key, y in self.Y.items()}
+        return sum(x.numel() * 4 for x in self.xh.values()), sum(y.numel() * 4 for y in self.yh.values())
+
+    def e2e_step(self, c):
+        for m in self.Ms:
+            self.X[m].copy_(self.xh[m], non_blocking=True)
+            self.wobs.wobs_quantize_q8_1(self.X[m], self.XQ[m])
+            for s in range(len(self.shapes)):
+                self._gemv(c, s, m)
+                self.yh[(m, s)].copy_(self.Y[(m, s)], non_blocking=True)
+
+    def config(self):
+        c = super().config()
+        c.update({"workload": self.name, "M": list(self.Ms),
+                  "step": "per M: quantize_q8_1(X) then gemv_q4_0_q8_1 on both shapes"})
+        return c
+
+    @classmethod
+    def oracle_prepare(cls, frac):
+        import oracle
+        from weight_only_bit_split_gb300 import synth
+        prep = []
+        for n, k in cls.shapes:
+            rows = max(1, int(round(n * frac)))
+            w = synth.weights(cls.workload_id, (rows, k)).numpy()
+            q4, d4 = oracle.quantize_q4_0(w)
+            prep.append((oracle.pack_q4_0(q4), d4, rows, k))
+        xs = {m: synth.activations(cls.workload_id, (m, cls.shapes[0][1]), copy=m).numpy() for m in cls.Ms}
+        return prep, xs
+
+    @classmethod
+    def oracle_step(cls, prep):
+        import oracle
+        mats, xs = prep
+        nbytes = 0
+        for m in cls.Ms:
+            q8, d8, _ = oracle.quantize_q8_1(xs[m])
+            for qs, d4, rows, k in mats:
+                oracle.gemv_q4_0_q8_1(qs, d4, q8, d8)
+                nbytes += cls.gemv_bytes_m(rows, k, m)
+            nbytes += m * cls.quant_bytes(mats[0][3])
+        return nbytes
+
+
+class DenseF16:
+    name = "fp16_gemv_4096x4096"
+    n, k = 4096, 4096
+    dtype = "f32"
+    kernel = "dense_m1"
+    kernel_src = "dense.cu"
+    workload_id = 1
+    launches_per_step = 1
+
+    def __init__(self, device):
+        import weight_only_bit_split_gb300 as wobs
+        from weight_only_bit_split_gb300 import synth
+        self.wobs = wobs
+        self.copies = max(1, math.ceil(ROTATE_BYTES / (2 * self.n * self.k)))
+        self.W = [synth.weights(self.workload_id, (self.n, self.k), copy=c, device=device, dtype=torch.float16)
+                  for c in range(self.copies)]
+        self.x = synth.activations(self.workload_id, (1, self.k), device=device, dtype=torch.float16)
+        self.y = torch.empty(1, self.n, dtype=torch.float16, device=device)
+
+    @classmethod
+    def gemv_bytes(cls):
+        return 2 * cls.n * cls.k + 2 * cls.k + 2 * cls.n
+
+    def bytes_per_step(self):
+        return self.gemv_bytes()
+
+    def step(self, c):
+        self.wobs.wobs_gemv_f16(self.W[c], self.x, self.y)
+
+    def kernel_calls(self):
+        return [(f"{self.n}x{self.k}", self.gemv_bytes(), self.step)]
+
+    def e2e_setup(self):
+        self.xh = self.x.cpu().pin_memory()
+        self.yh = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
+        return self.xh.numel() * 2, self.yh.numel() * 2
+
+    def e2e_step(self, c):
+        self.x.copy_(self.xh, non_blocking=True)
+        self.step(c)
+        self.yh.copy_(self.y, non_blocking=True)
+
+    def config(self):
+        return {"workload": self.name, "shapes_NxK": [f"{self.n}x{self.k}"], "M": 1,
+                "weight_copies": self.copies,
+                "working_set_gb": round(self.copies * 2 * self.n * self.k / 1e9, 3),
+                "l2": "inputs larger than L2: rotated weight copies, working set above 1 GB"}
+
+    @classmethod
+    def oracle_prepare(cls, frac):
+        from weight_only_bit_split_gb300 import synth
+        rows = max(1, int(round(cls.n * frac)))
+        w = synth.weights(cls.workload_id, (rows, cls.k), dtype=torch.float16).numpy()
+        x = synth.activations(cls.workload_id, (1, cls.k), dtype=torch.float16).numpy()
+        return w, x, rows
+
+    @classmethod
+    def oracle_step(cls, prep):
+        import oracle
+        w, x, rows = prep
+        oracle.gemv_dense(w, x)
+        return 2 * rows * cls.k + 2 * cls.k + 2 * rows
+
+
+class NF4:
+    name = "nf4_gemv_28672x8192"
+    n, k = 28672, 8192
+    dtype = "f32"
+    kernel = "nf4_m1"
+    kernel_src = "nf4.cu"
+    workload_id = 3
+    launches_per_step = 1
+
+    def __init__(self, device):
+        import weight_only_bit_split_gb300 as wobs
+        from weight_only_bit_split_gb300 import synth
+        from weight_only_bit_split_gb300.nf4_levels import normal_float_levels
+        self.wobs = wobs
+        self.cb = normal_float_levels().numpy()
+        self.copies = max(1, math.ceil(ROTATE_BYTES / self.gemv_bytes()))
+        self.planes = []
+        for c in range(self.copies):
+            w = synth.weights(self.workload_id, (self.n, self.k), copy=c, device=device, dtype=torch.bfloat16)
+            self.planes.append(wobs.wobs_quantize_nf4(w, self.cb))
+            del w
+        self.x = synth.activations(self.workload_id, (self.k,), device=device, dtype=torch.bfloat16)
+        self.y = torch.empty(self.n, dtype=torch.bfloat16, device=device)
+
+    @classmethod
+    def gemv_bytes(cls):
+        return cls.n * cls.k // 2 + 4 * cls.n * cls.k // 64 + 2 * cls.k + 2 * cls.n
+
+    def bytes_per_step(self):
+        return self.gemv_bytes()
+
+    def step(self, c):
+        qs, am = self.planes[c]
+        self.wobs.wobs_gemv_nf4(qs, am, self.cb, self.x, y=self.y)
+
+    def kernel_calls(self):
+        return [(f"{self.n}x{self.k}", self.gemv_bytes(), self.step)]
+
+    def e2e_setup(self):
+        self.xh = self.x.cpu().pin_memory()
+        self.yh = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
+        return self.xh.numel() * 2, self.yh.numel() * 2
+
+    def e2e_step(self, c):
+        self.x.copy_(self.xh, non_blocking=True)
+        self.step(c)
+        self.yh.copy_(self.y, non_blocking=True)
+
+    def config(self):
+        return {"workload": self.name, "shapes_NxK": [f"{self.n}x{self.k}"], "M": 1,
+                "weight_copies": self.copies,
+                "working_set_gb": round(self.copies * self.gemv_bytes() / 1e9, 3),
+                "l2": "inputs larger than L2: rotated weight copies, working set above 1 GB"}
+
+    @classmethod
+    def oracle_prepare(cls, frac):
+        import oracle
+        from weight_only_bit_split_gb300 import synth
+        from weight_only_bit_split_gb300.nf4_levels import normal_float_levels
+        cb = normal_float_levels().numpy()
+        rows = max(1, int(round(cls.n * frac)))
+        w = synth.weights(cls.workload_id, (rows, cls.k), dtype=torch.bfloat16).float().numpy()
+        codes, absmax = oracle.quantize_nf4(w, cb)
+        x = synth.activations(cls.workload_id, (cls.k,), dtype=torch.bfloat16).float().numpy()
+        return oracle.pack_nf4(codes), absmax, cb, x, rows
+
+    @classmethod
+    def oracle_step(cls, prep):
+        import oracle
+        qs, absmax, cb, x, rows = prep
+        oracle.gemv_nf4(qs, absmax, cb, x)
+        return rows * cls.k // 2 + 4 * rows * cls.k // 64 + 2 * cls.k + 2 * rows
+
+
+class LmHead:
+    name = "bf16_lm_head_argmax_128000x4096"
+    n, k = 128000, 4096
+    Ms = (1, 32)
+    dtype = "f32"
+    kernel = "dense_m1 / dense_mn"
+    kernel_src = "dense.cu"
+    workload_id = 5
+    launches_per_step = 2
+
+    def __init__(self, device):
+        import weight_only_bit_split_gb300 as wobs
+        from weight_only_bit_split_gb300 import synth
+        self.wobs = wobs
+        self.copies = max(2, math.ceil(ROTATE_BYTES / (2 * self.n * self.k)))
+        self.W = [synth.weights(self.workload_id, (self.n, self.k), copy=c, device=device, dtype=torch.bfloat16)
+                  for c in range(self.copies)]
+        self.X = {m: synth.activations(self.workload_id, (m, self.k), copy=m, device=device, dtype=torch.bfloat16)
+                  for m in self.Ms}
+        self.L = {m: torch.empty(m, self.n, dtype=torch.float32, device=device) for m in self.Ms}
+        self.A = {m: torch.empty(m, dtype=torch.int64, device=device) for m in self.Ms}
+        self.ws = {m: torch.zeros(wobs.wobs_workspace_size(wobs.OP_GEMV_BF16, m, self.n, self.k),
+                                  dtype=torch.uint8, device=device) for m in self.Ms}
+
+    @classmethod
+    def gemv_bytes(cls, m):
+        return 2 * cls.n * cls.k + 2 * m * cls.k + 4 * m * cls.n + 8 * m
+
+    def bytes_per_step(self):
+        return sum(self.gemv_bytes(m) for m in self.Ms)
+
+    def _call(self, c, m):
+        self.wobs.wobs_gemv_bf16(self.W[c], self.X[m], logits=self.L[m], argmax=self.A[m], ws=self.ws[m])
+
+    def step(self, c):
+        for m in self.Ms:
+            self._call(c, m)
+
+    def kernel_calls(self):
+        return [(f"M{m}", self.gemv_bytes(m), lambda c, m=m: self._call(c, m)) for m in self.Ms]
+
+    def e2e_setup(self):
+        self.xh = {m: x.cpu().pin_memory() for m, x in self.X.items()}
+        self.ah = {m: torch.empty(m, dtype=torch.int64).pin_memory() for m in self.Ms}
+        return sum(x.numel() * 2 for x in self.xh.values()), sum(8 * m for m in self.Ms)
+
+    def e2e_step(self, c):
+        for m in self.Ms:
+            self.X[m].copy_(self.xh[m], non_blocking=True)
+            self._call(c, m)
+            self.ah[m].copy_(self.A[m], non_blocking=True)
+
+    def config(self):
+        return {"workload": self.name, "shapes_NxK": [f"{self.n}x{self.k}"], "M": list(self.Ms),
+                "weight_copies": self.copies, "working_set_gb": round(self.copies * 2 * self.n * self.k / 1e9, 3),
+                "l2": "inputs larger than L2: each weight copy is 1.05 GB"}
+
+    @classmethod
+    def oracle_prepare(cls, frac):
+        from weight_only_bit_split_gb300 import synth
+        rows = max(1, int(round(cls.n * frac)))
+        w = synth.weights(cls.workload_id, (rows, cls.k), dtype=torch.bfloat16).float().numpy()
+        xs = {m: synth.activations(cls.workload_id, (m, cls.k), copy=m, dtype=torch.bfloat16).float().numpy()
+              for m in cls.Ms}
+        return w, xs, rows
+
+    @classmethod
+    def oracle_step(cls, prep):
+        import oracle
+        w, xs, rows = prep
+        nbytes = 0
+        for m in cls.Ms:
+            oracle.argmax_rows(oracle.gemv_dense(w, xs[m]).astype(np.float32))
+            nbytes += 2 * rows * cls.k + 2 * m * cls.k + 4 * m * rows + 8 * m
+        return nbytes
+
+
+WORKLOADS = {"q4_m1": Q4M1, "q4_m_sweep": Q4Sweep, "fp16_4096": DenseF16, "nf4": NF4,
+             "lm_head": LmHead}
+# oracle row fraction per step (bounds the CPU time of one oracle step)
+ORACLE_FRACTION = {"q4_m1": 0.125, "q4_m_sweep": 1 / 64, "fp16_4096": 0.5, "nf4": 1 / 32,
+                   "lm_head": 1 / 256}
+
+
+def oracle_rate(cls, frac, min_seconds, max_steps=None):
+    """Run the oracle on a row sample until ``min_seconds`` pass; GB/s, steps, seconds."""
+    prep = cls.oracle_prepare(frac)
+    t0 = time.perf_counter()
+    nbytes, steps = 0, 0
+    while True:
+        nbytes += cls.oracle_step(prep)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or (max_steps is not None and steps >= max_steps):
+            break
+    return nbytes / el / 1e9, steps, el, nbytes
+
+
+# ------------------------------------------------------------------ main
+
+
+def run_reference(args, cls, key, budget_s=90.0):
+    """The CPU oracle as the reference arm: rank 0 only, a row sample per step.
+
+    The sample shrinks below the workload's default fraction when needed so
+    that warm-up plus timed steps take about ``budget_s`` seconds.
+    """
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    frac = ORACLE_FRACTION[key]
+    t0 = time.perf_counter()
+    cls.oracle_step(cls.oracle_prepare(frac))
+    per_step = time.perf_counter() - t0
+    allowed = budget_s / max(1, args.steps + args.warmup)
+    if per_step > allowed:
+        frac *= allowed / per_step
+    prep = cls.oracle_prepare(frac)
+    for _ in range(args.warmup):
+        cls.oracle_step(prep)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += cls.oracle_step(prep)
+    el = time.perf_counter() - t0
+    gbs = nbytes / el / 1e9
+    sample = f"{frac:.4g} of each weight matrix's rows per step, full K, same seeds and distributions"
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cls.name, "oracle_row_fraction": frac},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="q4_m1", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="wobs", choices=["wobs", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    cls = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, cls, args.workload)
+
+    import weight_only_bit_split_gb300 as wobs
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist("nccl")
+    stream = torch.cuda.Stream(device)
+
+    ceiling, ceil_cfg, _ = read_ceiling(device, stream)
+    wl = cls(device)
+    # eager pass first (kernel attributes, occupancy queries), then capture
+    with torch.cuda.stream(stream):
+        for c in range(wl.copies):
+            wl.step(c)
+    stream.synchronize()
+    singles = [capture(lambda c=c: wl.step(c), stream) for c in range(wl.copies)]
+    cycle = capture(lambda: [wl.step(c) for c in range(wl.copies)], stream)
+    time_steps(cycle, singles, args.warmup, stream)
+
+    barrier(device)
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(device)
+    clocks.start()
+    ms = time_steps(cycle, singles, args.steps, stream)
+    torch.cuda.synchronize(device)
+    clocks.stop()
+    barrier(device)
+    bytes_rank = wl.bytes_per_step() * args.steps
+    gbs, ms_max = aggregate(bytes_rank, ms, device)
+
+    # per-launch time of the dominant kernel: its launches alone, back to
+    # back over the rotated copies, one graph per call site
+    per_call = {}
+    tot_b, tot_ms, launches = 0, 0.0, 0
+    reps = max(3, min(20, 2000 // max(1, wl.copies)))
+    for label, nbytes, fn in wl.kernel_calls():
+        gk = capture(lambda fn=fn: [fn(c) for c in range(wl.copies)], stream)
+        time_steps(gk, [gk], 2, stream)
+        t = time_steps(gk, [gk], reps, stream)
+        us = t * 1e3 / (reps * wl.copies)
+        per_call[label] = {"us": round(us, 3), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+        tot_b += nbytes
+        tot_ms += us * 1e-3
+        launches += 1
+    achieved = tot_b / (tot_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = traffic_record(cls.kernel if isinstance(cls.kernel, str) else None)
+
+    # end to end through the public API with pinned host buffers
+    h2d, d2h = wl.e2e_setup()
+    e2e_steps = max(3, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            wl.e2e_step(i % wl.copies)
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            wl.e2e_step(i % wl.copies)
+        e1.record(stream)
+    e1.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_gbs = wl.bytes_per_step() / (e2e_ms * 1e-3) / 1e9
+    e2e_gbs = reduce_over_ranks(e2e_gbs, "sum", device) if world > 1 else e2e_gbs
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        frac = ORACLE_FRACTION[args.workload]
+        v, steps_done, el, _ = oracle_rate(cls, frac, 10.0, max_steps=200)
+        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{steps_done} oracle steps on {frac:.4g} of each weight matrix's rows "
+                         f"(full K, same seeds), {el:.1f} s, numpy fp64, one thread"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": cls.dtype, "data": "synthetic",
+            "config": wl.config(),
+            "mbu": gbs / world / ceiling,
+            "read_ceiling_gbs": round(ceiling, 1),
+            "read_ceiling_how": f"bw_probe best of variants 1-3 x grids 1-8 CTAs/SM on an "
+                                f"{PROBE_BYTES >> 30} GiB buffer: {ceil_cfg}",
+            "us_per_call": per_call,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": cls.kernel, "peak_source": f"{peak_kind} hbm_gbs",
+                         "per_launch": "algorithmic bytes per launch / CUDA-event time of the "
+                                       "kernel's launches replayed back to back"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h,
+                    "how": "public Python API per step: pinned H2D of the activations, the "
+                           "step's launches, D2H of the outputs"},
+            "gpu_launches": wl.launches_per_step * args.steps,
+            "clocks": clocks.report(),
+        }
+        print(json.dumps(line), flush=True)
+    if _dist_on():
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,237 @@
+/*
+ * wobs.h -- C ABI of the weight-only low-bit decode GEMV library (sm_103a).
+ *
+ * The library computes the batch-1 (and small-batch, M <= 32) decode
+ * matrix-vector product y = W x that the batch1-cdna README describes
+ * ("Hand-written FP16 y = Wx, batch size one ... every weight is read once
+ * and never reused, so token time is bytes divided by bandwidth"), over
+ * three weight formats:
+ *   - dense fp16 / bf16 (batch1-cdna README, "02-gemv");
+ *   - Q4_0 weights x Q8_1 activations with integer block dots ("The kernel
+ *     that waited for itself", m12-db-gemm case study, section "Seven
+ *     variants, one microbenchmark, many mistakes");
+ *   - NF4 blockwise 4-bit codebook weights (bitsandbytes issue #1842,
+ *     "Benchmark Data" and "Minimal Repro");
+ * plus an optional fused greedy argmax over the outputs ("[WIP] ArgCompare
+ * Benchmark Results and Performance Analysis", IREE discussion #23609).
+ *
+ * Conventions (every entry point):
+ *   - Returns an int status: WOBS_OK (0) or a negative WOBS_ERR_* code.
+ *     wobs_last_error() gives a message for the calling thread's last error.
+ *     No exception, abort or trap crosses the ABI.
+ *   - Pointers are DEVICE memory owned by the caller unless the argument
+ *     says "host".  The library never allocates, frees or synchronises in
+ *     these calls.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous: argument and launch errors are
+ *     reported on return; results are ready when the stream reaches them.
+ *   - Activations and outputs with M columns are row-major [M][...]: column
+ *     m of the mathematical X is the contiguous row X + m*ldx.
+ *   - Weight matrices are row-major [N][K] (one output per row).
+ *   - Alignment: every weight pointer, activation pointer and row pitch must
+ *     give 16-byte aligned rows; violations return WOBS_ERR_MISALIGNED.
+ *   - Workspace: calls that take (ws, ws_bytes) need at least
+ *     wobs_workspace_size(op, M, N, K) bytes, ZERO-FILLED before its first
+ *     use.  Every call that returns WOBS_OK leaves it zero-filled again (the
+ *     last CTA to finish clears what it used), so one zeroing serves any
+ *     number of calls.  Calls that overlap on the GPU must not share one
+ *     workspace.  Size 0 means no workspace is needed (ws may be NULL).
+ *   - Environment: WOBS_DEBUG=1 logs every dispatch (op, shape, kernel,
+ *     grid, split) to stderr; WOBS_SPLITK=<s> overrides the split-K factor
+ *     of the dense and Q4_0 multi-column kernels (testing only; the
+ *     workspace must be sized for it with the same variable set).
+ */
+#ifndef WOBS_H
+#define WOBS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define WOBS_API __attribute__((visibility("default")))
+#else
+#define WOBS_API
+#endif
+
+/* ---- status codes ---- */
+#define WOBS_OK 0
+#define WOBS_ERR_INVALID_ARG (-1)         /* null pointer, bad enum, M out of range */
+#define WOBS_ERR_MISALIGNED (-2)          /* pointer or pitch breaks 16-byte rows */
+#define WOBS_ERR_UNSUPPORTED_SHAPE (-3)   /* K not a multiple of the block size, N < 1 */
+#define WOBS_ERR_WORKSPACE_TOO_SMALL (-4)
+#define WOBS_ERR_LAUNCH_FAILED (-5)       /* cudaGetLastError() after the launch */
+#define WOBS_ERR_CUDA (-6)                /* other CUDA runtime error (device query) */
+
+/* ---- ops for wobs_workspace_size ---- */
+#define WOBS_OP_GEMV_F16 1
+#define WOBS_OP_GEMV_BF16 2
+#define WOBS_OP_GEMV_Q4_0_Q8_1 3
+#define WOBS_OP_GEMV_NF4 4
+
+/* Largest activation-column count of the multi-column entry points. */
+#define WOBS_MAX_M 32
+
+/* Message for the calling thread's most recent error ("" if none). */
+WOBS_API const char* wobs_last_error(void);
+
+/* Library ABI version (integer, increases on incompatible change). */
+WOBS_API int wobs_version(void);
+
+/*
+ * Streaming-read probe: the bandwidth ceiling used as the denominator of
+ * every bandwidth-utilisation figure (batch1-cdna README, "01-ceiling": a
+ * grid-stride read of a buffer far larger than the last-level cache, every
+ * element folded into one scalar so no load can be dropped).
+ *
+ *   buf      device buffer, 16-byte aligned; bytes a multiple of 16
+ *   grid     CTAs to launch; 0 = one wave of resident CTAs on every SM
+ *   variant  0 = plain 16-byte read-only loads (L1-cached)
+ *            1 = 16-byte loads, L1 no-allocate + L2 evict-first
+ *            2 = 32-byte loads (one 256-bit vector per iteration), same hints;
+ *                buf must be 32-byte aligned
+ *            3 = bulk asynchronous copies (cp.async.bulk) into a shared-memory
+ *                ring, completion tracked by mbarriers
+ *   xor_out  device uint32: the XOR of every little-endian 32-bit word of
+ *            buf is XOR-ed into it (zero it first to read the checksum)
+ * Errors: INVALID_ARG (null, bad variant, grid < 0), MISALIGNED.  Variant 3
+ * bounds every wait; a wait that gives up sets the device error word
+ * (wobs_error_word) instead of hanging.
+ */
+WOBS_API int wobs_bw_probe(const void* buf, size_t bytes, int grid, int variant,
+                           uint32_t* xor_out, void* stream);
+
+/*
+ * Dense fp16 GEMV, y[m][n] = sum_k W[n][k] * X[m][k], fp32 accumulation,
+ * fp16 outputs rounded to nearest even (batch1-cdna README, "02-gemv":
+ * fp16 weights and activations, fp32 accumulate).
+ *
+ *   W   fp16 [N][ldw] (ldw >= K, multiple of 8), X fp16 [M][ldx] (ldx >= K,
+ *       multiple of 8), Y fp16 [M][N]; 1 <= M <= WOBS_MAX_M; K multiple of 8.
+ *   ws  workspace (op WOBS_OP_GEMV_F16); may be NULL when the call does not
+ *       split K (wobs_workspace_size(...) <= 512).
+ */
+WOBS_API int wobs_gemv_f16(const void* W, int64_t ldw, const void* X, int64_t ldx, int M,
+                           void* Y, int N, int K, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Dense bf16 GEMV with fp32 outputs (logits) and an optional fused greedy
+ * argmax per activation column: argmax[m] = the n of the largest
+ * logits[m][n], ties to the lowest n, -0.0 equal to +0.0 (ArgCompare
+ * discussion, section "ArgMax/ArgMin Operations Analysis in real-world AI
+ * models": LLaMA-3-8B argmax over [1,128000] and [32,128000], i64 out).
+ *
+ *   W  bf16 [N][ldw], X bf16 [M][ldx] (pitches multiples of 8, >= K),
+ *   logits fp32 [M][N], argmax int64 [M] or NULL; 1 <= M <= WOBS_MAX_M,
+ *   K multiple of 8.  Logits must be finite for the argmax to be defined.
+ *   ws  workspace (op WOBS_OP_GEMV_BF16).
+ */
+WOBS_API int wobs_gemv_bf16(const void* W, int64_t ldw, const void* X, int64_t ldx, int M,
+                            float* logits, int64_t* argmax, int N, int K, void* ws,
+                            size_t ws_bytes, void* stream);
+
+/*
+ * Q8_1 activation quantisation ("The kernel that waited for itself", section
+ * "Seven variants, one microbenchmark, many mistakes": Q8_1 activations).
+ * Per block of 32 consecutive elements of a column, IEEE float32:
+ * d = max|x| / 127, q = round-half-away(x / d) (0 when d == 0),
+ * s = d * sum(q); stored as {fp16 d; fp16 s; int8 q[32]} = 36 bytes,
+ * fp16 by round-to-nearest-even.  Bit-exact with the definition.
+ *
+ *   X   fp32 [M][ldx] (ldx >= K, multiple of 4), xq  [M][K/32] blocks of 36
+ *       bytes (4-byte aligned); 1 <= M <= WOBS_MAX_M; K multiple of 32.
+ */
+WOBS_API int wobs_quantize_q8_1(const float* X, int64_t ldx, int M, int K, void* xq,
+                                void* stream);
+
+/*
+ * Q4_0 weight quantisation (same page and section: Q4_0 weights).  Per block
+ * of 32 consecutive elements of a row, IEEE float32: amax = the signed
+ * element of largest magnitude (first on ties), d = amax / -8,
+ * q = clamp(round-half-away(w / d) + 8, 0, 15) (8 when d == 0).
+ * Outputs the two planes the GEMV reads: qs [N][K/2] (byte j of a block =
+ * element j in the low nibble, element j+16 in the high nibble) and
+ * d fp16 [N][K/32].  Bit-exact with the definition.
+ *
+ *   W fp32 [N][ldw] (ldw >= K, multiple of 4); K multiple of 32.
+ */
+WOBS_API int wobs_quantize_q4_0(const float* W, int64_t ldw, int N, int K, uint8_t* qs,
+                                void* d, void* stream);
+
+/*
+ * NF4 blockwise weight quantisation (bitsandbytes issue #1842, "Minimal
+ * Repro": quantize_4bit with quant_type 'nf4', blocksize 64).  Per block of
+ * 64 consecutive bf16 elements of a row, IEEE float32: absmax = max|w|,
+ * v = w / absmax (0 when absmax == 0), code = the index k minimising
+ * |codebook[k] - v| (lowest k on ties).  Outputs qs [N][K/2] (two codes per
+ * byte, the first element in the HIGH nibble) and absmax fp32 [N][K/64].
+ * Bit-exact with the definition.
+ *
+ *   W bf16 [N][ldw] (ldw >= K, multiple of 8); codebook: HOST pointer to 16
+ *   floats (copied into the launch); K multiple of 64.
+ */
+WOBS_API int wobs_quantize_nf4(const void* W, int64_t ldw, int N, int K,
+                               const float* codebook, uint8_t* qs, float* absmax,
+                               void* stream);
+
+/*
+ * Q4_0 x Q8_1 GEMV ("The kernel that waited for itself": the decode matrix
+ * product over Q4_0 weights and Q8_1 activations, 1 to 32 columns).  Per
+ * weight block b and column m the exact integer block dot
+ * sumi = sum_i (q4_i - 8) * q8_{m,i} is formed with 4-way byte dot
+ * products, then y[m][n] += d4[n][b] * d8[m][b] * sumi in fp32.
+ *
+ *   qs  [N][K/2] nibble plane, d fp16 [N][K/32] (from wobs_quantize_q4_0 or
+ *   repacked llama.cpp blocks); xq [M][K/32] Q8_1 blocks; y fp32 [M][N];
+ *   argmax int64 [M] or NULL; 1 <= M <= WOBS_MAX_M; K multiple of 32.
+ *   ws  workspace (op WOBS_OP_GEMV_Q4_0_Q8_1).
+ */
+WOBS_API int wobs_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* xq, int M,
+                                 float* y, int64_t* argmax, int N, int K, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/*
+ * NF4 GEMV, M = 1 (bitsandbytes issue #1842: the fused 4-bit inference GEMV
+ * for one decode token): y[n] = sum_b absmax[n][b] * sum_i codebook[code_i]
+ * * x_i, fp32 accumulation, bf16 output (round to nearest even).  Optional
+ * fused argmax over the bf16 outputs (as stored).
+ *
+ *   qs [N][K/2], absmax fp32 [N][K/64], codebook HOST pointer to 16 floats,
+ *   x bf16 [K], y bf16 [N], argmax int64 [1] or NULL; K multiple of 64.
+ *   ws  workspace (op WOBS_OP_GEMV_NF4).
+ */
+WOBS_API int wobs_gemv_nf4(const uint8_t* qs, const float* absmax, const float* codebook,
+                           const void* x, void* y, int64_t* argmax, int N, int K, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * Workspace bytes needed by one call of `op` with this shape on the current
+ * device (split-K partials and counters, argmax keys and counter).  Returns
+ * 0 for an unknown op or a shape that needs none.
+ */
+WOBS_API size_t wobs_workspace_size(int op, int M, int N, int K);
+
+/*
+ * Test export: the exact int32 block dots sumi[m][n][b] =
+ * sum_i (q4_i - 8) * q8_{m,i} that the Q4_0 x Q8_1 GEMV forms ("The kernel
+ * that waited for itself", section "What correctness was measured against":
+ * CPU calculation on the quantised values).  out int32 [M][N][K/32].
+ */
+WOBS_API int wobs_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, int N, int K,
+                                      int32_t* out, void* stream);
+
+/*
+ * Device error word: kernels that give up a bounded wait record a nonzero
+ * code here instead of hanging.  Copies the word to *host_out (host pointer)
+ * and clears it; synchronises `stream` to do so.  0 = no error.
+ */
+WOBS_API int wobs_error_word(void* stream, int* host_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WOBS_H */

@@ -1,0 +1,126 @@
+"""The C ABI on the host: symbols, argument checks, workspace sizing (CPU only).
+
+No call here launches a kernel; every call returns from the library's
+argument checks before touching the GPU.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from weight_only_bit_split_gb300 import _lib
+from weight_only_bit_split_gb300.nf4_levels import normal_float_levels
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wobs.h")
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"WOBS_API\s+[\w\s\*]+?\b(wobs_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ["wobs_bw_probe", "wobs_gemv_f16", "wobs_gemv_bf16", "wobs_quantize_q8_1",
+                     "wobs_gemv_q4_0_q8_1", "wobs_gemv_nf4", "wobs_workspace_size",
+                     "wobs_q4_0_q8_1_blockdots", "wobs_error_word", "wobs_last_error"]:
+        assert required in names
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = _lib.get()
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"{name} has no ctypes signature"
+    # and nothing the binding declares is missing from the header
+    assert set(_lib.SIGNATURES) == set(declared_symbols())
+
+
+def test_version_and_empty_error():
+    lib = _lib.get()
+    assert lib.wobs_version() >= 1
+    assert isinstance(lib.wobs_last_error(), bytes)
+
+
+def _status(name, *args):
+    lib = _lib.get()
+    rc = getattr(lib, name)(*args)
+    return rc, lib.wobs_last_error().decode()
+
+
+FAKE16 = ctypes.c_void_p(0x10000)      # never dereferenced: checks fail first
+FAKE_ODD = ctypes.c_void_p(0x10001)
+
+
+def test_null_pointers_are_invalid_args():
+    rc, msg = _status("wobs_gemv_f16", None, 64, FAKE16, 64, 1, FAKE16, 8, 64, None, 0, None)
+    assert rc == -1 and "null" in msg
+    rc, _ = _status("wobs_gemv_q4_0_q8_1", FAKE16, None, FAKE16, 1, FAKE16, None, 8, 64, None, 0, None)
+    assert rc == -1
+    rc, _ = _status("wobs_bw_probe", None, 16, 0, 0, FAKE16, None)
+    assert rc == -1
+
+
+def test_shape_checks():
+    # K not a multiple of 32 for Q4_0 / Q8_1, of 64 for NF4, of 8 for dense
+    rc, _ = _status("wobs_gemv_q4_0_q8_1", FAKE16, FAKE16, FAKE16, 1, FAKE16, None, 8, 48, None, 0, None)
+    assert rc == -3
+    rc, _ = _status("wobs_quantize_q8_1", FAKE16, 48, 1, 48, FAKE16, None)
+    assert rc == -3
+    cb = (ctypes.c_float * 16)()
+    rc, _ = _status("wobs_gemv_nf4", FAKE16, FAKE16, cb, FAKE16, FAKE16, None, 8, 96, None, 0, None)
+    assert rc == -3
+    rc, _ = _status("wobs_gemv_f16", FAKE16, 12, FAKE16, 12, 1, FAKE16, 8, 12, None, 0, None)
+    assert rc == -3
+    # M outside 1..32
+    rc, _ = _status("wobs_gemv_bf16", FAKE16, 64, FAKE16, 64, 33, FAKE16, None, 8, 64, None, 0, None)
+    assert rc == -1
+    rc, _ = _status("wobs_gemv_bf16", FAKE16, 64, FAKE16, 64, 0, FAKE16, None, 8, 64, None, 0, None)
+    assert rc == -1
+
+
+def test_alignment_checks():
+    rc, _ = _status("wobs_gemv_f16", FAKE_ODD, 64, FAKE16, 64, 1, FAKE16, 8, 64, None, 0, None)
+    assert rc == -2
+    rc, _ = _status("wobs_gemv_f16", FAKE16, 60, FAKE16, 64, 1, FAKE16, 8, 56, None, 0, None)
+    assert rc == -2                       # pitch of 60 halves breaks 16-byte rows
+    rc, _ = _status("wobs_bw_probe", FAKE16, 24, 0, 0, FAKE16, None)
+    assert rc == -2                       # byte count not a multiple of 16
+    rc, _ = _status("wobs_gemv_q4_0_q8_1", FAKE_ODD, FAKE16, FAKE16, 1, FAKE16, None, 8, 64, None, 0, None)
+    assert rc == -2
+
+
+def test_argmax_needs_a_workspace():
+    rc, msg = _status("wobs_gemv_bf16", FAKE16, 64, FAKE16, 64, 1, FAKE16, FAKE16, 8, 64, None, 0, None)
+    assert rc == -1 and "workspace" in msg
+    rc, _ = _status("wobs_gemv_bf16", FAKE16, 64, FAKE16, 64, 1, FAKE16, FAKE16, 8, 64, FAKE16, 16, None)
+    assert rc == -4
+
+
+def test_workspace_size_rules():
+    lib = _lib.get()
+    assert lib.wobs_workspace_size(99, 1, 64, 64) == 0
+    assert lib.wobs_workspace_size(3, 0, 64, 64) == 0
+    assert lib.wobs_workspace_size(3, 33, 64, 64) == 0
+    for op in (1, 2, 3, 4):
+        s = lib.wobs_workspace_size(op, 1, 4096, 4096)
+        assert s >= 8 + 8 * 32 and s % 256 == 0
+
+
+def test_workspace_grows_with_forced_split(monkeypatch):
+    lib = _lib.get()
+    base = lib.wobs_workspace_size(3, 4, 1000, 4096)
+    monkeypatch.setenv("WOBS_SPLITK", "4")
+    forced = lib.wobs_workspace_size(3, 4, 1000, 4096)
+    assert forced >= base + 4 * 4 * 4 * 1000
+
+
+def test_product_codebook_equals_oracle_fixture():
+    from golden_io import nf4_codebook_fixture
+    a = normal_float_levels().numpy()
+    b = nf4_codebook_fixture()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))

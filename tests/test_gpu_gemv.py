@@ -1,0 +1,223 @@
+"""GEMV parity on the GPU against the oracle, at sizes the oracle finishes in
+seconds: several tiles, ragged tails, every kernel path, edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_only_bit_split_gb300 as wobs
+from golden_io import load, nf4_codebook_fixture
+from parity import assert_within, dev, f16_to_dev, q4_inputs_from_oracle, to_dev, w_x_fp32
+from weight_only_bit_split_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+# ----------------------------------------------------------------- dense
+
+@pytest.mark.parametrize("n,k", [(1, 8), (37, 264), (300, 4096), (1000, 4104), (4096, 4096)])
+def test_gemv_f16_m1(n, k):
+    w = synth.weights(1, (n, k), dtype=torch.float16)
+    x = synth.activations(1, (1, k), dtype=torch.float16)
+    y = wobs.wobs_gemv_f16(w.to(dev()), x.to(dev())).cpu().float().numpy()
+    ref = oracle.gemv_dense(w.numpy(), x.numpy())
+    assert_within(y, ref, oracle.abs_dot_dense(w.numpy(), x.numpy()), "f16", "gemv_f16 M=1")
+
+
+@pytest.mark.parametrize("m,n,k", [(2, 300, 520), (3, 513, 1024), (8, 64, 4096)])
+def test_gemv_f16_multi_column_strided(m, n, k):
+    w = synth.weights(1, (n, k + 8), dtype=torch.float16)[:, :k]       # pitch k+8
+    x = synth.activations(1, (m, k + 16), dtype=torch.float16)[:, :k]
+    y = wobs.wobs_gemv_f16(w.to(dev()), x.to(dev())).cpu().float().numpy()
+    wn, xn = w.contiguous().numpy(), x.contiguous().numpy()
+    assert_within(y, oracle.gemv_dense(wn, xn), oracle.abs_dot_dense(wn, xn), "f16", "gemv_f16 M>1")
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 1, 8), (1, 5000, 1024), (2, 777, 512), (5, 1200, 2048),
+                                   (32, 2000, 4096)])
+def test_gemv_bf16_logits_and_argmax(m, n, k):
+    w = synth.weights(5, (n, k), dtype=torch.bfloat16)
+    x = synth.activations(5, (m, k), dtype=torch.bfloat16)
+    logits, am = wobs.wobs_gemv_bf16(w.to(dev()), x.to(dev()), want_argmax=True)
+    lg = logits.cpu().numpy()
+    wf, xf = w.float().numpy(), x.float().numpy()
+    assert_within(lg, oracle.gemv_dense(wf, xf), oracle.abs_dot_dense(wf, xf), "f32", "gemv_bf16")
+    assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(lg))
+
+
+def test_gemv_bf16_argmax_ties_go_to_the_lowest_row():
+    n, k = 6000, 256
+    w = synth.weights(5, (n, k), dtype=torch.bfloat16)
+    x = synth.activations(5, (2, k), dtype=torch.bfloat16)
+    w[5900] = w[5900] * 4            # make row 5900 the winner for both columns
+    w[100] = w[5900]                 # an identical earlier row, far away (other CTA)
+    w[5999] = w[5900]
+    logits, am = wobs.wobs_gemv_bf16(w.to(dev()), x.to(dev()), want_argmax=True)
+    lg = logits.cpu().numpy()
+    assert lg[0, 100] == lg[0, 5900] == lg[0, 5999]
+    ref = oracle.argmax_rows(lg)
+    assert np.array_equal(am.cpu().numpy(), ref)
+    assert ref[0] == 100 or lg[0].max() > lg[0, 100]
+
+
+def test_gemv_bf16_workspace_is_left_clean_and_reusable():
+    n, k = 3000, 512
+    w = synth.weights(5, (n, k), dtype=torch.bfloat16).to(dev())
+    ws = torch.zeros(wobs.wobs_workspace_size(wobs.OP_GEMV_BF16, 4, n, k), dtype=torch.uint8, device=dev())
+    for m in (1, 4):
+        x = synth.activations(5, (m, k), copy=m, dtype=torch.bfloat16).to(dev())
+        for _ in range(3):
+            lg, am = wobs.wobs_gemv_bf16(w, x, want_argmax=True, ws=ws)
+            assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(lg.cpu().numpy()))
+            assert int(ws.count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("splits", ["2", "3", "7"])
+def test_dense_forced_split_k(monkeypatch, splits):
+    monkeypatch.setenv("WOBS_SPLITK", splits)
+    for m in (1, 3):
+        w = synth.weights(5, (700, 2048), dtype=torch.bfloat16)
+        x = synth.activations(5, (m, 2048), dtype=torch.bfloat16)
+        lg, am = wobs.wobs_gemv_bf16(w.to(dev()), x.to(dev()), want_argmax=True)
+        lgn = lg.cpu().numpy()
+        wf, xf = w.float().numpy(), x.float().numpy()
+        assert_within(lgn, oracle.gemv_dense(wf, xf), oracle.abs_dot_dense(wf, xf), "f32", "split-K")
+        assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(lgn))
+
+
+# ------------------------------------------------------------------ Q4_0
+
+def _q4_case(n, k, m, seed_copy=0):
+    w, x = w_x_fp32(2, n, k, m, copy=seed_copy)
+    qs, d4, q8, d8, xq = q4_inputs_from_oracle(w, x)
+    ref = oracle.gemv_q4_0_q8_1(qs, d4, q8, d8)
+    ad = oracle.abs_dot_q4_0_q8_1(qs, d4, q8, d8)
+    return (to_dev(qs), f16_to_dev(d4), to_dev(xq)), ref, ad, (qs, q8)
+
+
+@pytest.mark.parametrize("n,k", [(1, 32), (7, 64), (100, 4096), (33, 14336), (64, 4160),
+                                 (1024, 4096), (300, 1024)])
+def test_gemv_q4_0_m1(n, k):
+    (qs, d, xq), ref, ad, _ = _q4_case(n, k, 1)
+    y, am = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq, want_argmax=True)
+    yn = y.cpu().numpy()
+    assert_within(yn, ref, ad, "f32", f"q4_0 M=1 {n}x{k}")
+    assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
+
+
+def test_blockdots_bit_exact():
+    for (n, k, m) in [(5, 64, 1), (70, 1024, 3), (33, 4096, 32)]:
+        (qs, d, xq), _, _, (qsn, q8) = _q4_case(n, k, m)
+        got = wobs.wobs_q4_0_q8_1_blockdots(qs, xq).cpu().numpy()
+        assert np.array_equal(got, oracle.q4_0_q8_1_blockdots(qsn, q8))
+
+
+def test_q4_0_h4_worked_example_on_gpu():
+    g = load("q4_0_q8_1_h4.json")
+    w = np.empty((2, 64), np.float32)
+    w[0] = np.tile(np.array([-1.0, 0.5], np.float32), 32)
+    w[1] = 0.5
+    w[1, 0] = w[1, 32] = 1.0
+    qs, d4, q8, d8, xq = q4_inputs_from_oracle(w, np.ones((1, 64), np.float32))
+    y, _ = wobs.wobs_gemv_q4_0_q8_1(to_dev(qs), f16_to_dev(d4), to_dev(xq))
+    assert abs(float(y[0, 0]) - g["y"][0]) < 1e-5 and abs(float(y[0, 1]) - g["y"][1]) < 1e-5
+    sumi = wobs.wobs_q4_0_q8_1_blockdots(to_dev(qs), to_dev(xq)).cpu().numpy()
+    assert np.array_equal(sumi[0], np.asarray(g["sumi"]))
+
+
+@pytest.mark.parametrize("m", [2, 4, 8, 12, 16, 24, 32])
+def test_gemv_q4_0_multi_column(m):
+    (qs, d, xq), ref, ad, _ = _q4_case(600, 2048, m)
+    y, am = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq, want_argmax=True)
+    yn = y.cpu().numpy()
+    assert_within(yn, ref, ad, "f32", f"q4_0 M={m}")
+    assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
+
+
+@pytest.mark.parametrize("splits", ["2", "5", "64"])
+def test_gemv_q4_0_forced_split_k(monkeypatch, splits):
+    monkeypatch.setenv("WOBS_SPLITK", splits)
+    for m in (1, 6):
+        (qs, d, xq), ref, ad, _ = _q4_case(517, 2048, m)
+        y, am = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq, want_argmax=True)
+        yn = y.cpu().numpy()
+        assert_within(yn, ref, ad, "f32", f"q4_0 split {splits} M={m}")
+        assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
+
+
+def test_q4_0_column_symmetry_and_determinism():
+    n, k = 1000, 4096
+    w, x = w_x_fp32(4, n, k, 1)
+    xs = np.repeat(x, 16, axis=0)
+    qs, d4, q8, d8, xq = q4_inputs_from_oracle(w, xs)
+    args = (to_dev(qs), f16_to_dev(d4), to_dev(xq))
+    y1, _ = wobs.wobs_gemv_q4_0_q8_1(*args)
+    y2, _ = wobs.wobs_gemv_q4_0_q8_1(*args)
+    a = y1.cpu().numpy()
+    assert np.array_equal(a, y2.cpu().numpy())                    # run to run
+    assert all(np.array_equal(a[0], a[i]) for i in range(16))   # identical columns
+    # a column permutation permutes the outputs bit for bit
+    x2 = np.concatenate([xs[:1], x * 0.5], axis=0)
+    _, _, _, _, xq2 = q4_inputs_from_oracle(w, x2)
+    _, _, _, _, xq3 = q4_inputs_from_oracle(w, x2[::-1].copy())
+    p, _ = wobs.wobs_gemv_q4_0_q8_1(args[0], args[1], to_dev(xq2))
+    r, _ = wobs.wobs_gemv_q4_0_q8_1(args[0], args[1], to_dev(xq3))
+    assert np.array_equal(p.cpu().numpy(), r.cpu().numpy()[::-1])
+
+
+def test_q4_0_gpu_quantised_weights_match_oracle_path():
+    # the product path (GPU quantisers) feeding the GEMV equals the oracle path
+    n, k = 256, 4096
+    w, x = w_x_fp32(2, n, k, 1)
+    qs, d = wobs.wobs_quantize_q4_0(torch.from_numpy(w).to(dev()))
+    xq = wobs.wobs_quantize_q8_1(torch.from_numpy(x).to(dev()))
+    y, _ = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq)
+    qsn, d4, q8, d8, xqn = q4_inputs_from_oracle(w, x)
+    assert np.array_equal(xq.cpu().numpy(), xqn)
+    assert_within(y.cpu().numpy(), oracle.gemv_q4_0_q8_1(qsn, d4, q8, d8),
+                  oracle.abs_dot_q4_0_q8_1(qsn, d4, q8, d8), "f32", "q4 product path")
+
+
+# ------------------------------------------------------------------- NF4
+
+def _nf4_case(n, k, copy=0):
+    cb = nf4_codebook_fixture()
+    w = synth.weights(3, (n, k), copy=copy, dtype=torch.bfloat16).float().numpy()
+    x = synth.activations(3, (1, k), copy=copy, dtype=torch.bfloat16)
+    codes, absmax = oracle.quantize_nf4(w, cb)
+    qs = oracle.pack_nf4(codes)
+    xf = x.float().numpy()
+    ref = oracle.gemv_nf4(qs, absmax, cb, xf)[0]
+    ad = oracle.abs_dot_nf4(qs, absmax, cb, xf)[0]
+    return cb, to_dev(qs), to_dev(absmax), x.to(dev()).reshape(-1), ref, ad
+
+
+@pytest.mark.parametrize("n,k", [(1, 64), (31, 1024), (100, 8192), (33, 1088), (257, 4096),
+                                 (70, 16384)])
+def test_gemv_nf4(n, k):
+    cb, qs, am, x, ref, ad = _nf4_case(n, k)
+    y, idx = wobs.wobs_gemv_nf4(qs, am, cb, x, want_argmax=True)
+    yf = y.float().cpu().numpy()
+    assert_within(yf, ref, ad, "bf16", f"nf4 {n}x{k}")
+    assert int(idx.item()) == int(oracle.argmax_rows(yf)[0])
+
+
+def test_gemv_nf4_deterministic():
+    cb, qs, am, x, _, _ = _nf4_case(500, 8192)
+    a, _ = wobs.wobs_gemv_nf4(qs, am, cb, x)
+    b, _ = wobs.wobs_gemv_nf4(qs, am, cb, x)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ----------------------------------------------------------------- probe
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+@pytest.mark.parametrize("nbytes", [16, 4112, 1 << 20, (32 << 20) + 48])
+def test_bw_probe_reads_every_word(variant, nbytes):
+    g = torch.Generator(device=dev()).manual_seed(nbytes + variant)
+    buf = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device=dev(), generator=g)
+    for grid in (0, 3):
+        out = wobs.wobs_bw_probe(buf, grid=grid, variant=variant)
+        got = int(out.cpu().numpy().view(np.uint32)[0])
+        assert got == int(oracle.xor_words(buf.cpu().numpy()))
+    assert wobs.wobs_error_word() == 0

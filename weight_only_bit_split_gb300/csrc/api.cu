@@ -1,0 +1,355 @@
+// C ABI of the library: argument checks, workspace layout, split-K choice,
+// dispatch logging, status codes.  Declarations and full contracts are in
+// include/wobs.h.  No allocation, no synchronisation (except
+// wobs_error_word, which says so), no exception crosses this file.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/wobs.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where, int code) {
+  return fail(code, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool debug_on() {
+  const char* v = std::getenv("WOBS_DEBUG");
+  return v && v[0] && v[0] != '0';
+}
+
+int env_splits() {
+  const char* v = std::getenv("WOBS_SPLITK");
+  if (!v || !v[0]) return 0;
+  int s = std::atoi(v);
+  return s > 0 ? s : 0;
+}
+
+void log_dispatch(const char* op, int M, int N, int K, const wobs::Launch& L, int splits) {
+  if (!debug_on()) return;
+  std::fprintf(stderr,
+               "wobs: op=%s M=%d N=%d K=%d kernel=%s grid=(%d,%d) block=%d smem=%d splits=%d\n",
+               op, M, N, K, L.kernel, L.grid_x, L.grid_y, L.block, L.smem, splits);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+constexpr int kRowsPerGroup = 256;   // rows per CTA in the multi-column kernels
+
+struct WsLayout {
+  size_t counter = 0, keys = 0, groups = 0, partials = 0, total = 0;
+  int splits = 1;
+  int ngroups = 0;
+};
+
+WsLayout ws_layout(int op, int M, int N, int K) {
+  WsLayout L;
+  L.splits = wobs::choose_splits(op, M, N, K);
+  L.ngroups = L.splits > 1 ? (N + kRowsPerGroup - 1) / kRowsPerGroup : 0;
+  size_t off = 0;
+  L.counter = off;
+  off += 8;
+  L.keys = off;
+  off += 8 * WOBS_MAX_M;
+  L.groups = off;
+  off += 4 * static_cast<size_t>(L.ngroups);
+  off = (off + 255) & ~static_cast<size_t>(255);
+  L.partials = off;
+  if (L.splits > 1) off += 4ull * L.splits * M * N;
+  L.total = off;
+  return L;
+}
+
+struct Prepared {
+  wobs::SplitArgs sk;
+  wobs::ArgmaxArgs am;
+};
+
+int prepare_ws(int op, int M, int N, int K, int64_t* argmax, void* ws, size_t ws_bytes,
+               Prepared* out) {
+  const WsLayout L = ws_layout(op, M, N, K);
+  const bool need = argmax != nullptr || L.splits > 1;
+  out->sk = wobs::SplitArgs{nullptr, nullptr, L.splits};
+  out->am = wobs::ArgmaxArgs{nullptr, nullptr, nullptr};
+  if (!need) return WOBS_OK;
+  if (!ws) return fail(WOBS_ERR_INVALID_ARG, "workspace required (%zu bytes) but ws is NULL", L.total);
+  if (!aligned16(ws)) return fail(WOBS_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+  if (ws_bytes < L.total)
+    return fail(WOBS_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes, L.total);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  out->sk.partials = reinterpret_cast<float*>(base + L.partials);
+  out->sk.counters = reinterpret_cast<unsigned*>(base + L.groups);
+  if (argmax) {
+    out->am.out = argmax;
+    out->am.keys = reinterpret_cast<uint64_t*>(base + L.keys);
+    out->am.counter = reinterpret_cast<unsigned*>(base + L.counter);
+  }
+  return WOBS_OK;
+}
+
+int finish_launch(cudaError_t e, const char* op, int M, int N, int K, const wobs::Launch& L,
+                  int splits) {
+  if (e != cudaSuccess) return cuda_fail(e, op, WOBS_ERR_LAUNCH_FAILED);
+  log_dispatch(op, M, N, K, L, splits);
+  g_err[0] = '\0';
+  return WOBS_OK;
+}
+
+}  // namespace
+
+namespace wobs {
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+int max_resident_ctas(const void* kernel, int block, int smem) {
+  struct Entry { const void* k; int dev, block, smem, n; };
+  static Entry table[128];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (table[i].k == kernel && table[i].dev == dev && table[i].block == block && table[i].smem == smem)
+      return table[i].n;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, smem) != cudaSuccess) {
+    cudaGetLastError();
+    n = 1;
+  }
+  if (n <= 0) n = 1;
+  if (used < 128) table[used++] = Entry{kernel, dev, block, smem, n};
+  return n;
+}
+
+int choose_splits(int op, int M, int N, int K) {
+  const int forced = env_splits();
+  const int groups = (N + kRowsPerGroup - 1) / kRowsPerGroup;
+  const int target = 2 * device_sm_count();
+  switch (op) {
+    case WOBS_OP_GEMV_F16:
+    case WOBS_OP_GEMV_BF16: {
+      const int kmax = K / 8 > 0 ? K / 8 : 1;
+      if (forced) return forced < kmax ? forced : kmax;
+      if (M == 1) return 1;
+      int s = (target + groups - 1) / groups;
+      const int cap = K / 512 > 0 ? K / 512 : 1;
+      if (s > cap) s = cap;
+      return s < 1 ? 1 : s;
+    }
+    case WOBS_OP_GEMV_Q4_0_Q8_1: {
+      const int nb = K / 32 > 0 ? K / 32 : 1;
+      // shared-memory bound of the multi-column kernel: 48 bytes per block
+      // per padded column, at most 144 KB
+      int nc = 1;
+      while (nc < M) nc = nc < 8 ? nc * 2 : (nc == 8 ? 12 : (nc == 12 ? 16 : (nc == 16 ? 24 : 32)));
+      const int bps_max = (144 * 1024) / (48 * nc);
+      const int smin = (nb + bps_max - 1) / bps_max;
+      int s;
+      if (forced) s = forced < nb ? forced : nb;
+      else if (M == 1) return 1;
+      else {
+        s = (target + groups - 1) / groups;
+        const int cap = nb / 4 > 0 ? nb / 4 : 1;
+        if (s > cap) s = cap;
+      }
+      if (s < smin) s = smin;
+      return s < 1 ? 1 : s;
+    }
+    default:
+      return 1;
+  }
+}
+
+}  // namespace wobs
+
+extern "C" {
+
+const char* wobs_last_error(void) { return g_err; }
+
+int wobs_version(void) { return 1; }
+
+size_t wobs_workspace_size(int op, int M, int N, int K) {
+  if (op < WOBS_OP_GEMV_F16 || op > WOBS_OP_GEMV_NF4 || M < 1 || M > WOBS_MAX_M || N < 1 || K < 1)
+    return 0;
+  return ws_layout(op, M, N, K).total;
+}
+
+int wobs_bw_probe(const void* buf, size_t bytes, int grid, int variant, uint32_t* xor_out,
+                  void* stream) {
+  if (!buf || !xor_out) return fail(WOBS_ERR_INVALID_ARG, "bw_probe: null pointer");
+  if (variant < 0 || variant > 3) return fail(WOBS_ERR_INVALID_ARG, "bw_probe: variant %d", variant);
+  if (grid < 0) return fail(WOBS_ERR_INVALID_ARG, "bw_probe: grid %d", grid);
+  if (!aligned16(buf) || (bytes & 15u)) return fail(WOBS_ERR_MISALIGNED, "bw_probe: buffer/bytes not 16-byte aligned");
+  if (!aligned4(xor_out)) return fail(WOBS_ERR_MISALIGNED, "bw_probe: xor_out not 4-byte aligned");
+  if (variant == 2 && (reinterpret_cast<uintptr_t>(buf) & 31u))
+    return fail(WOBS_ERR_MISALIGNED, "bw_probe: variant 2 (32-byte loads) needs a 32-byte aligned buffer");
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_bw_probe(buf, bytes, grid, variant, xor_out,
+                                        static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "bw_probe", 0, static_cast<int>(bytes > 0x7fffffff ? 0x7fffffff : bytes), 0, L, 1);
+}
+
+static int check_dense(const char* op, const void* W, int64_t ldw, const void* X, int64_t ldx,
+                       int M, const void* Y, int N, int K) {
+  if (!W || !X || !Y) return fail(WOBS_ERR_INVALID_ARG, "%s: null pointer", op);
+  if (M < 1 || M > WOBS_MAX_M) return fail(WOBS_ERR_INVALID_ARG, "%s: M=%d outside 1..%d", op, M, WOBS_MAX_M);
+  if (N < 1 || K < 8 || (K % 8)) return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "%s: N=%d K=%d (K must be a positive multiple of 8)", op, N, K);
+  if (ldw < K || (M > 1 && ldx < K)) return fail(WOBS_ERR_INVALID_ARG, "%s: pitch smaller than K", op);
+  if (!aligned16(W) || !aligned16(X) || (ldw % 8) || (M > 1 && (ldx % 8)))
+    return fail(WOBS_ERR_MISALIGNED, "%s: W/X rows must be 16-byte aligned", op);
+  if (!aligned4(Y)) return fail(WOBS_ERR_MISALIGNED, "%s: output not aligned", op);
+  return WOBS_OK;
+}
+
+int wobs_gemv_f16(const void* W, int64_t ldw, const void* X, int64_t ldx, int M, void* Y, int N,
+                  int K, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_dense("gemv_f16", W, ldw, X, ldx, M, Y, N, K);
+  if (rc) return rc;
+  Prepared p;
+  rc = prepare_ws(WOBS_OP_GEMV_F16, M, N, K, nullptr, ws, ws_bytes, &p);
+  if (rc) return rc;
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_gemv_dense(0, W, ldw, X, ldx, M, Y, 0, N, K, p.sk, p.am,
+                                          static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "gemv_f16", M, N, K, L, p.sk.splits);
+}
+
+int wobs_gemv_bf16(const void* W, int64_t ldw, const void* X, int64_t ldx, int M, float* logits,
+                   int64_t* argmax, int N, int K, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_dense("gemv_bf16", W, ldw, X, ldx, M, logits, N, K);
+  if (rc) return rc;
+  if (argmax && (reinterpret_cast<uintptr_t>(argmax) & 7u))
+    return fail(WOBS_ERR_MISALIGNED, "gemv_bf16: argmax not 8-byte aligned");
+  Prepared p;
+  rc = prepare_ws(WOBS_OP_GEMV_BF16, M, N, K, argmax, ws, ws_bytes, &p);
+  if (rc) return rc;
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_gemv_dense(1, W, ldw, X, ldx, M, logits, 1, N, K, p.sk, p.am,
+                                          static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "gemv_bf16", M, N, K, L, p.sk.splits);
+}
+
+int wobs_quantize_q8_1(const float* X, int64_t ldx, int M, int K, void* xq, void* stream) {
+  if (!X || !xq) return fail(WOBS_ERR_INVALID_ARG, "quantize_q8_1: null pointer");
+  if (M < 1 || M > WOBS_MAX_M) return fail(WOBS_ERR_INVALID_ARG, "quantize_q8_1: M=%d outside 1..%d", M, WOBS_MAX_M);
+  if (K < 32 || (K % 32)) return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "quantize_q8_1: K=%d not a positive multiple of 32", K);
+  if (ldx < K) return fail(WOBS_ERR_INVALID_ARG, "quantize_q8_1: ldx < K");
+  if (!aligned16(X) || (ldx % 4)) return fail(WOBS_ERR_MISALIGNED, "quantize_q8_1: X rows must be 16-byte aligned");
+  if (!aligned4(xq)) return fail(WOBS_ERR_MISALIGNED, "quantize_q8_1: xq not 4-byte aligned");
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_quantize_q8_1(X, ldx, M, K, xq, static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "quantize_q8_1", M, 0, K, L, 1);
+}
+
+int wobs_quantize_q4_0(const float* W, int64_t ldw, int N, int K, uint8_t* qs, void* d,
+                       void* stream) {
+  if (!W || !qs || !d) return fail(WOBS_ERR_INVALID_ARG, "quantize_q4_0: null pointer");
+  if (N < 1 || K < 32 || (K % 32)) return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "quantize_q4_0: N=%d K=%d", N, K);
+  if (ldw < K) return fail(WOBS_ERR_INVALID_ARG, "quantize_q4_0: ldw < K");
+  if (!aligned4(W) || !aligned16(qs) || (reinterpret_cast<uintptr_t>(d) & 1u))
+    return fail(WOBS_ERR_MISALIGNED, "quantize_q4_0: misaligned pointer");
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_quantize_q4_0(W, ldw, N, K, qs, d, static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "quantize_q4_0", 0, N, K, L, 1);
+}
+
+int wobs_quantize_nf4(const void* W, int64_t ldw, int N, int K, const float* codebook,
+                      uint8_t* qs, float* absmax, void* stream) {
+  if (!W || !codebook || !qs || !absmax) return fail(WOBS_ERR_INVALID_ARG, "quantize_nf4: null pointer");
+  if (N < 1 || K < 64 || (K % 64)) return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "quantize_nf4: N=%d K=%d", N, K);
+  if (ldw < K || (ldw % 2)) return fail(WOBS_ERR_INVALID_ARG, "quantize_nf4: ldw");
+  if (!aligned4(W) || !aligned4(absmax)) return fail(WOBS_ERR_MISALIGNED, "quantize_nf4: misaligned pointer");
+  wobs::Codebook16 cb;
+  std::memcpy(cb.v, codebook, sizeof(cb.v));
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_quantize_nf4(W, ldw, N, K, cb, qs, absmax, static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "quantize_nf4", 0, N, K, L, 1);
+}
+
+int wobs_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* xq, int M, float* y,
+                        int64_t* argmax, int N, int K, void* ws, size_t ws_bytes, void* stream) {
+  if (!qs || !d || !xq || !y) return fail(WOBS_ERR_INVALID_ARG, "gemv_q4_0_q8_1: null pointer");
+  if (M < 1 || M > WOBS_MAX_M) return fail(WOBS_ERR_INVALID_ARG, "gemv_q4_0_q8_1: M=%d outside 1..%d", M, WOBS_MAX_M);
+  if (N < 1 || K < 32 || (K % 32)) return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "gemv_q4_0_q8_1: N=%d K=%d (K must be a positive multiple of 32)", N, K);
+  if (!aligned16(qs) || (reinterpret_cast<uintptr_t>(d) & 1u) || !aligned4(xq) || !aligned4(y))
+    return fail(WOBS_ERR_MISALIGNED, "gemv_q4_0_q8_1: misaligned pointer");
+  if (argmax && (reinterpret_cast<uintptr_t>(argmax) & 7u))
+    return fail(WOBS_ERR_MISALIGNED, "gemv_q4_0_q8_1: argmax not 8-byte aligned");
+  Prepared p;
+  int rc = prepare_ws(WOBS_OP_GEMV_Q4_0_Q8_1, M, N, K, argmax, ws, ws_bytes, &p);
+  if (rc) return rc;
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_gemv_q4_0_q8_1(qs, d, xq, M, y, N, K, p.sk, p.am,
+                                              static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "gemv_q4_0_q8_1", M, N, K, L, p.sk.splits);
+}
+
+int wobs_gemv_nf4(const uint8_t* qs, const float* absmax, const float* codebook, const void* x,
+                  void* y, int64_t* argmax, int N, int K, void* ws, size_t ws_bytes,
+                  void* stream) {
+  if (!qs || !absmax || !codebook || !x || !y) return fail(WOBS_ERR_INVALID_ARG, "gemv_nf4: null pointer");
+  if (N < 1 || K < 64 || (K % 64) || K > 32768)
+    return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "gemv_nf4: N=%d K=%d (K a multiple of 64, at most 32768)", N, K);
+  if (!aligned16(qs) || !aligned4(absmax) || (reinterpret_cast<uintptr_t>(x) & 1u) ||
+      (reinterpret_cast<uintptr_t>(y) & 1u))
+    return fail(WOBS_ERR_MISALIGNED, "gemv_nf4: misaligned pointer");
+  if (argmax && (reinterpret_cast<uintptr_t>(argmax) & 7u))
+    return fail(WOBS_ERR_MISALIGNED, "gemv_nf4: argmax not 8-byte aligned");
+  Prepared p;
+  int rc = prepare_ws(WOBS_OP_GEMV_NF4, 1, N, K, argmax, ws, ws_bytes, &p);
+  if (rc) return rc;
+  wobs::Codebook16 cb;
+  std::memcpy(cb.v, codebook, sizeof(cb.v));
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_gemv_nf4(qs, absmax, cb, x, y, N, K, p.am,
+                                        static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "gemv_nf4", 1, N, K, L, 1);
+}
+
+int wobs_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, int N, int K, int32_t* out,
+                             void* stream) {
+  if (!qs || !xq || !out) return fail(WOBS_ERR_INVALID_ARG, "q4_0_q8_1_blockdots: null pointer");
+  if (M < 1 || M > WOBS_MAX_M) return fail(WOBS_ERR_INVALID_ARG, "q4_0_q8_1_blockdots: M=%d", M);
+  if (N < 1 || K < 32 || (K % 32)) return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "q4_0_q8_1_blockdots: N=%d K=%d", N, K);
+  if (!aligned16(qs) || !aligned4(xq) || !aligned4(out))
+    return fail(WOBS_ERR_MISALIGNED, "q4_0_q8_1_blockdots: misaligned pointer");
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_q4_0_q8_1_blockdots(qs, xq, M, N, K, out, static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "q4_0_q8_1_blockdots", M, N, K, L, 1);
+}
+
+int wobs_error_word(void* stream, int* host_out) {
+  if (!host_out) return fail(WOBS_ERR_INVALID_ARG, "error_word: null pointer");
+  cudaError_t e = wobs::read_and_clear_error_word(static_cast<cudaStream_t>(stream), host_out);
+  if (e != cudaSuccess) return cuda_fail(e, "error_word", WOBS_ERR_CUDA);
+  g_err[0] = '\0';
+  return WOBS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,173 @@
+// Device helpers shared by the GEMV kernels (sm_103a).
+//
+// Streaming loads with cache hints, warp reductions, the greedy-argmax key,
+// and the "last arriving CTA finishes the job" epilogue used for split-K and
+// for the fused argmax.  No spin-waits anywhere: cross-CTA completion is an
+// arrival counter, never a barrier.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace wobs {
+
+// ---------------------------------------------------------------- loads
+
+// L2 policy for bytes that are read exactly once (weights): evict first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 16-byte read-only load that does not allocate in L1 and is marked
+// evict-first in L2: the weight stream.
+__device__ __forceinline__ uint4 ld_stream16(const void* p, uint64_t pol) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p), "l"(pol));
+  return r;
+}
+
+// 16-byte read-only load through L1 (activations, re-read by many warps).
+__device__ __forceinline__ uint4 ld_nc16(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// --------------------------------------------------------- conversions
+
+__device__ __forceinline__ float2 to_float2(uint32_t v, const __half*) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+__device__ __forceinline__ float2 to_float2(uint32_t v, const __nv_bfloat16*) {
+  // bf16 is the upper half of a float32: widening is a shift / mask
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+__device__ __forceinline__ float to_float(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_float(float v) { return v; }
+
+template <typename TO> __device__ __forceinline__ TO from_float(float v);
+template <> __device__ __forceinline__ float from_float<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_float<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// 8 packed 16-bit values (one 16-byte chunk) dotted with 8 floats.
+template <typename T>
+__device__ __forceinline__ float dot8(uint4 w, const float* x, float acc) {
+  const T* tag = nullptr;
+  float2 a = to_float2(w.x, tag), b = to_float2(w.y, tag);
+  float2 c = to_float2(w.z, tag), d = to_float2(w.w, tag);
+  acc = fmaf(a.x, x[0], acc); acc = fmaf(a.y, x[1], acc);
+  acc = fmaf(b.x, x[2], acc); acc = fmaf(b.y, x[3], acc);
+  acc = fmaf(c.x, x[4], acc); acc = fmaf(c.y, x[5], acc);
+  acc = fmaf(d.x, x[6], acc); acc = fmaf(d.y, x[7], acc);
+  return acc;
+}
+
+// Two 16-byte chunks of 16-bit values, element-wise products summed.
+template <typename T>
+__device__ __forceinline__ float dot8x8(uint4 w, uint4 x, float acc) {
+  const T* tag = nullptr;
+  float2 w0 = to_float2(w.x, tag), x0 = to_float2(x.x, tag);
+  float2 w1 = to_float2(w.y, tag), x1 = to_float2(x.y, tag);
+  float2 w2 = to_float2(w.z, tag), x2 = to_float2(x.z, tag);
+  float2 w3 = to_float2(w.w, tag), x3 = to_float2(x.w, tag);
+  acc = fmaf(w0.x, x0.x, acc); acc = fmaf(w0.y, x0.y, acc);
+  acc = fmaf(w1.x, x1.x, acc); acc = fmaf(w1.y, x1.y, acc);
+  acc = fmaf(w2.x, x2.x, acc); acc = fmaf(w2.y, x2.y, acc);
+  acc = fmaf(w3.x, x3.x, acc); acc = fmaf(w3.y, x3.y, acc);
+  return acc;
+}
+
+// ---------------------------------------------------------- reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    uint64_t t = __shfl_xor_sync(0xffffffffu, v, o);
+    v = t > v ? t : v;
+  }
+  return v;
+}
+
+// ------------------------------------------------------- argmax key
+
+// Greedy-argmax key: the float maps to an unsigned integer with the same
+// order (-0.0 folded onto +0.0), in the high word; the low word holds
+// 0xFFFFFFFF - index, so the maximum key is the largest value and, among
+// equal values, the lowest index.  Every finite float maps above 0, so a
+// zeroed key is the identity of the max.
+__device__ __forceinline__ uint64_t argmax_key(float v, uint32_t idx) {
+  uint32_t b = __float_as_uint(v);
+  if (b == 0x80000000u) b = 0u;
+  uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<uint64_t>(ord) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - idx);
+}
+__device__ __forceinline__ int64_t argmax_key_index(uint64_t key) {
+  return static_cast<int64_t>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFu));
+}
+
+// ------------------------------------------------ cross-CTA epilogues
+
+// Publish this CTA's per-column best keys (one per column, held in `cta_key`
+// in shared memory) and count the CTA as finished; the CTA that arrives
+// last writes the argmax indices and returns the keys and its counter to
+// zero, so the workspace is clean for the next call.  Must be called by all
+// threads of the CTA.  `expected` = number of CTAs that call it.
+__device__ __forceinline__ void argmax_publish(const uint64_t* cta_key, int ncols,
+                                               const ArgmaxArgs& am, unsigned expected) {
+  __shared__ int s_last;
+  if (threadIdx.x < 32) {
+    if (static_cast<int>(threadIdx.x) < ncols) {
+      atomicMax(reinterpret_cast<unsigned long long*>(am.keys + threadIdx.x),
+                static_cast<unsigned long long>(cta_key[threadIdx.x]));
+    }
+    __threadfence();
+    __syncwarp();
+    if (threadIdx.x == 0) {
+      unsigned prev = atomicAdd(am.counter, 1u);
+      s_last = (prev == expected - 1u);
+    }
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    if (static_cast<int>(threadIdx.x) < ncols) {
+      uint64_t k = atomicExch(reinterpret_cast<unsigned long long*>(am.keys + threadIdx.x), 0ull);
+      am.out[threadIdx.x] = argmax_key_index(k);
+    }
+    if (threadIdx.x == 0) *am.counter = 0u;
+  }
+}
+
+// Split-K arrival for one row group: returns true (in every thread) for
+// the CTA that arrives last among the `splits` CTAs of `group`; that CTA
+// resets the counter.  Call after the partial stores, from all threads.
+__device__ __forceinline__ bool splitk_arrive_last(unsigned* counters, int group, int splits) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned prev = atomicAdd(counters + group, 1u);
+    s_last = (prev == static_cast<unsigned>(splits) - 1u);
+    if (s_last) counters[group] = 0u;
+  }
+  __syncthreads();
+  if (s_last) __threadfence();
+  return s_last != 0;
+}
+
+}  // namespace wobs

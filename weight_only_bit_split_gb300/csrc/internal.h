@@ -1,0 +1,73 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Host and device visible; no torch types anywhere.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace wobs {
+
+// Fused greedy-argmax epilogue state (all pointers device memory, inside
+// the caller's workspace except `out`).
+struct ArgmaxArgs {
+  int64_t* out;        // [M] argmax indices (caller's output); null = off
+  uint64_t* keys;      // [32] running best keys, zero between calls
+  unsigned* counter;   // CTA arrival counter, zero between calls
+};
+
+// Split-K state: fp32 partial sums and one arrival counter per row group.
+struct SplitArgs {
+  float* partials;     // [splits][M][N]
+  unsigned* counters;  // [row groups], zero between calls
+  int splits;          // 1 = no split
+};
+
+struct Launch {
+  int grid_x = 0, grid_y = 1, block = 0, smem = 0;
+  const char* kernel = "";
+};
+
+// 16-entry codebook passed by value as a kernel parameter.
+struct Codebook16 {
+  float v[16];
+};
+
+// ---- launchers (each returns cudaGetLastError() after the launch) ----
+
+cudaError_t launch_bw_probe(const void* buf, size_t bytes, int grid, int variant,
+                            uint32_t* xor_out, cudaStream_t st, Launch* info);
+
+// dense: T = 0 fp16 inputs, 1 bf16 inputs; out_f32 = 1 writes float, else
+// the input type.
+cudaError_t launch_gemv_dense(int dtype, const void* W, int64_t ldw, const void* X, int64_t ldx,
+                              int M, void* Y, int out_f32, int N, int K, const SplitArgs& sk,
+                              const ArgmaxArgs& am, cudaStream_t st, Launch* info);
+
+cudaError_t launch_quantize_q8_1(const float* X, int64_t ldx, int M, int K, void* xq,
+                                 cudaStream_t st, Launch* info);
+cudaError_t launch_quantize_q4_0(const float* W, int64_t ldw, int N, int K, uint8_t* qs,
+                                 void* d, cudaStream_t st, Launch* info);
+cudaError_t launch_quantize_nf4(const void* W, int64_t ldw, int N, int K, const Codebook16& cb,
+                                uint8_t* qs, float* absmax, cudaStream_t st, Launch* info);
+
+cudaError_t launch_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* xq, int M,
+                                  float* Y, int N, int K, const SplitArgs& sk,
+                                  const ArgmaxArgs& am, cudaStream_t st, Launch* info);
+cudaError_t launch_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, int N, int K,
+                                       int32_t* out, cudaStream_t st, Launch* info);
+
+cudaError_t launch_gemv_nf4(const uint8_t* qs, const float* absmax, const Codebook16& cb,
+                            const void* x, void* y, int N, int K, const ArgmaxArgs& am,
+                            cudaStream_t st, Launch* info);
+
+cudaError_t read_and_clear_error_word(cudaStream_t st, int* host_out);
+
+// ---- shared launch-shape helpers (api.cu) ----
+int device_sm_count();                       // current device, cached
+int max_resident_ctas(const void* kernel, int block, int smem);  // per SM
+
+// Split factor chosen for an op (also sizes the workspace).
+int choose_splits(int op, int M, int N, int K);
+
+}  // namespace wobs

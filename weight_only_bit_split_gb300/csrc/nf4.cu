@@ -1,0 +1,207 @@
+// NF4 blockwise 4-bit decode GEMV, M = 1.
+//
+// bitsandbytes issue #1842 ("70B 4-bit LLM decode bottlenecked by HIP kernel
+// (kgemm_4bit_inference_naive) efficiency"): the fused 4-bit inference GEMV
+// for one decode token, 64-element blocks with a float absmax each, codes
+// looked up in a 16-entry float codebook, float accumulation.  The issue and
+// its comments locate the losses in narrow loads, bf16 <-> float conversions
+// in the inner loop, and too little latency hiding; a later comment asks for
+// consecutive threads reading consecutive 128-bit chunks.
+//
+// sm_103a design:
+//   * a warp owns a 1024-element K slice (32 lanes x 32 codes = one 16-byte
+//     load per lane per row, 512 contiguous bytes per warp instruction);
+//   * the CTA processes rows in batches of 32: each lane keeps its 32
+//     activation values in registers (converted to float once) and one
+//     partial sum per row of the batch, so activations are never re-read
+//     per row;
+//   * codes are decoded two at a time through a 256-entry byte -> (level,
+//     level) float table in shared memory, replicated 16 times so the 16
+//     lanes of a half-warp never share a bank; the pair goes straight into
+//     a packed two-wide fp32 FMA;
+//   * at the end of a batch a 31-shuffle reduce-scatter leaves row r's warp
+//     partial in lane r; warps combine through shared memory in a fixed
+//     order, so the result does not depend on timing.
+#include "common.cuh"
+
+namespace wobs {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kBatch = 32;        // rows per batch (one per lane after the reduction)
+constexpr int kRowUnroll = 8;     // rows whose codes are in flight at once
+constexpr int kLutCopies = 16;
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n"
+      " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p, uint64_t pol) {
+  uint32_t r;
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(r) : "l"(p), "l"(pol));
+  return r;
+}
+
+template <bool kArgmax>
+__global__ void __launch_bounds__(kThreads, 2) nf4_m1_kernel(const uint8_t* __restrict__ qs,
+                                                              const float* __restrict__ absmax,
+                                                              Codebook16 cb,
+                                                              const __nv_bfloat16* __restrict__ x,
+                                                              __nv_bfloat16* __restrict__ y,
+                                                              int N, int K, ArgmaxArgs am) {
+  extern __shared__ __align__(16) float smem_f[];
+  float2* lut = reinterpret_cast<float2*>(smem_f);                 // [256][16]
+  float* xsm = smem_f + 2 * 256 * kLutCopies;                        // permuted x, K floats
+  __shared__ float red[kWarps][kBatch];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nsl = (K + 1023) >> 10;        // 1024-element slices
+  const int kh = K >> 1;                   // code bytes per row
+  const int nab = K >> 6;                  // absmax per row
+  const uint64_t pol = l2_evict_first_policy();
+
+  for (int i = threadIdx.x; i < 256 * kLutCopies; i += kThreads) {
+    const int e = i / kLutCopies;
+    lut[i] = make_float2(cb.v[e >> 4], cb.v[e & 15]);
+  }
+  // x element k = sl*1024 + l*32 + 4*j + t  ->  xsm[((sl*8 + j)*32 + l)*4 + t]
+  for (int k = threadIdx.x; k < nsl * 1024; k += kThreads) {
+    const int sl = k >> 10, l = (k >> 5) & 31, j = (k >> 2) & 7, t = k & 3;
+    xsm[((sl * 8 + j) * 32 + l) * 4 + t] = k < K ? __bfloat162float(x[k]) : 0.f;
+  }
+  __syncthreads();
+
+  const float2* lut_l = lut + (lane & (kLutCopies - 1));
+  const int nbatch = (N + kBatch - 1) / kBatch;
+  uint64_t best = 0;
+  float2 xr[16];
+  int loaded_slice = -1;
+  for (int bt = blockIdx.x; bt < nbatch; bt += gridDim.x) {
+    const int row0 = bt * kBatch;
+    float p[kBatch];
+#pragma unroll
+    for (int r = 0; r < kBatch; ++r) p[r] = 0.f;
+    for (int sl = warp; sl < nsl; sl += kWarps) {
+      if (sl != loaded_slice) {
+        const float4* xp = reinterpret_cast<const float4*>(xsm) + (sl * 8) * 32 + lane;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 v = xp[j * 32];
+          xr[2 * j] = make_float2(v.x, v.y);
+          xr[2 * j + 1] = make_float2(v.z, v.w);
+        }
+        loaded_slice = sl;
+      }
+      const int chunk = sl * 32 + lane;              // 16-byte chunk index within a row
+      const bool lane_ok = chunk * 32 < K;
+#pragma unroll
+      for (int r0 = 0; r0 < kBatch; r0 += kRowUnroll) {
+        uint4 q[kRowUnroll];
+        float a[kRowUnroll];
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; ++u) {
+          const int row = row0 + r0 + u;
+          if (lane_ok && row < N) {
+            q[u] = ld_stream16(qs + static_cast<int64_t>(row) * kh + chunk * 16, pol);
+            a[u] = __uint_as_float(ld_stream_u32(absmax + static_cast<int64_t>(row) * nab + (chunk >> 1), pol));
+          } else {
+            q[u] = make_uint4(0u, 0u, 0u, 0u);
+            a[u] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; ++u) {
+          float2 acc = make_float2(0.f, 0.f);
+          const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t e = (w[i] >> (8 * j)) & 0xFFu;
+              acc = ffma2(lut_l[e * kLutCopies], xr[4 * i + j], acc);
+            }
+          }
+          p[r0 + u] = fmaf(a[u], acc.x + acc.y, p[r0 + u]);
+        }
+      }
+    }
+    // reduce-scatter: lane r ends with the warp's sum for row r
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < off; ++i) {
+        const float send = upper ? p[i] : p[i + off];
+        const float keep = upper ? p[i + off] : p[i];
+        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    }
+    red[warp][lane] = p[0];
+    __syncthreads();
+    if (warp == 0) {
+      float t = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; ++w2) t += red[w2][lane];
+      const int row = row0 + lane;
+      if (row < N) {
+        const __nv_bfloat16 o = __float2bfloat16_rn(t);
+        y[row] = o;
+        if (kArgmax) {
+          const uint64_t k = argmax_key(__bfloat162float(o), static_cast<uint32_t>(row));
+          best = k > best ? k : best;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (kArgmax) {
+    __shared__ uint64_t s_cta[1];
+    if (warp == 0) {
+      best = warp_max_u64(best);
+      if (lane == 0) s_cta[0] = best;
+    }
+    __syncthreads();
+    argmax_publish(s_cta, 1, am, gridDim.x);
+  }
+}
+
+template <bool kArgmax>
+cudaError_t run(const uint8_t* qs, const float* absmax, const Codebook16& cb, const void* x,
+                void* y, int N, int K, const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
+  const int nsl = (K + 1023) / 1024;
+  const int smem = (2 * 256 * kLutCopies + nsl * 1024) * static_cast<int>(sizeof(float));
+  cudaError_t e = cudaFuncSetAttribute(nf4_m1_kernel<kArgmax>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int per_sm = max_resident_ctas(reinterpret_cast<const void*>(nf4_m1_kernel<kArgmax>),
+                                       kThreads, smem);
+  int grid = device_sm_count() * (per_sm > 0 ? per_sm : 1);
+  const int need = (N + kBatch - 1) / kBatch;
+  if (grid > need) grid = need;
+  info->grid_x = grid;
+  info->block = kThreads;
+  info->smem = smem;
+  info->kernel = "nf4_m1";
+  nf4_m1_kernel<kArgmax><<<grid, kThreads, smem, st>>>(
+      qs, absmax, cb, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, K,
+      am);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_nf4(const uint8_t* qs, const float* absmax, const Codebook16& cb,
+                            const void* x, void* y, int N, int K, const ArgmaxArgs& am,
+                            cudaStream_t st, Launch* info) {
+  if (am.out) return run<true>(qs, absmax, cb, x, y, N, K, am, st, info);
+  return run<false>(qs, absmax, cb, x, y, N, K, am, st, info);
+}
+
+}  // namespace wobs

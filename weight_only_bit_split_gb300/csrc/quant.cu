@@ -1,0 +1,154 @@
+// Quantisers: Q8_1 activations (hot path, once per decode step) and the
+// Q4_0 / NF4 weight formats (once per model load).
+//
+// Formats: "The kernel that waited for itself" (m12-db-gemm case study),
+// section "Seven variants, one microbenchmark, many mistakes" -- Q4_0
+// weights, Q8_1 activations; bitsandbytes issue #1842, "Minimal Repro" --
+// NF4 blockwise (64) quantisation.  Every decision is taken in IEEE float32
+// exactly as the format defines it (true division, roundf, no contraction),
+// so the outputs are bit-identical to the definition.
+#include "common.cuh"
+
+namespace wobs {
+namespace {
+
+constexpr int kThreads = 256;
+
+// ---------------------------------------------------------------- Q8_1
+// Eight threads per 32-element block, four elements each.
+__global__ void __launch_bounds__(kThreads) q8_1_kernel(const float* __restrict__ X, int64_t ldx,
+                                                         int M, int K, uint8_t* __restrict__ xq) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  const int per_col = K >> 2;
+  const int64_t total = static_cast<int64_t>(M) * per_col;
+  const bool valid = t < total;   // groups of 8 are either all valid or all not
+  const int m = valid ? static_cast<int>(t / per_col) : 0;
+  const int k4 = valid ? static_cast<int>(t - static_cast<int64_t>(m) * per_col) : 0;
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (valid) v = *reinterpret_cast<const float4*>(X + static_cast<int64_t>(m) * ldx + 4 * k4);
+  float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float d = amax / 127.0f;
+  int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+  if (d != 0.0f) {
+    q0 = static_cast<int>(roundf(v.x / d));
+    q1 = static_cast<int>(roundf(v.y / d));
+    q2 = static_cast<int>(roundf(v.z / d));
+    q3 = static_cast<int>(roundf(v.w / d));
+  }
+  int sum = q0 + q1 + q2 + q3;
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (!valid) return;
+  uint8_t* blk = xq + (static_cast<int64_t>(m) * (K >> 5) + (k4 >> 3)) * 36;
+  if ((k4 & 7) == 0) {
+    const float s = d * static_cast<float>(sum);
+    const __half2 ds = __halves2half2(__float2half_rn(d), __float2half_rn(s));
+    *reinterpret_cast<__half2*>(blk) = ds;
+  }
+  const uint32_t packed = (static_cast<uint32_t>(q0) & 0xFFu) | ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
+                          ((static_cast<uint32_t>(q2) & 0xFFu) << 16) | (static_cast<uint32_t>(q3) << 24);
+  *reinterpret_cast<uint32_t*>(blk + 4 + 4 * (k4 & 7)) = packed;
+}
+
+// ---------------------------------------------------------------- Q4_0
+// One warp per 32-element block, one element per lane.
+__global__ void __launch_bounds__(kThreads) q4_0_quant_kernel(const float* __restrict__ W,
+                                                               int64_t ldw, int N, int K,
+                                                               uint8_t* __restrict__ qs,
+                                                               __half* __restrict__ d) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int nb = K >> 5;
+  if (wid >= static_cast<int64_t>(N) * nb) return;   // whole warp
+  const int n = static_cast<int>(wid / nb);
+  const int b = static_cast<int>(wid - static_cast<int64_t>(n) * nb);
+  const float w = W[static_cast<int64_t>(n) * ldw + 32 * b + lane];
+  // largest magnitude, lowest index on ties
+  uint64_t key = (static_cast<uint64_t>(__float_as_uint(fabsf(w))) << 32) | static_cast<uint64_t>(31 - lane);
+  key = warp_max_u64(key);
+  const int src = 31 - static_cast<int>(key & 0xFFFFFFFFu);
+  const float amax = __shfl_sync(0xffffffffu, w, src);
+  const float dd = amax / -8.0f;
+  int q = 8;
+  if (dd != 0.0f) q = min(15, max(0, static_cast<int>(roundf(w / dd)) + 8));
+  const int qhi = __shfl_down_sync(0xffffffffu, q, 16);
+  if (lane < 16) qs[static_cast<int64_t>(n) * (K >> 1) + 16 * b + lane] = static_cast<uint8_t>(q | (qhi << 4));
+  if (lane == 0) d[static_cast<int64_t>(n) * nb + b] = __float2half_rn(dd);
+}
+
+// ----------------------------------------------------------------- NF4
+// One warp per 64-element block, two elements per lane.
+__device__ __forceinline__ int nearest_level(float v, const Codebook16& cb) {
+  float best = fabsf(cb.v[0] - v);
+  int code = 0;
+#pragma unroll
+  for (int k = 1; k < 16; ++k) {
+    const float dist = fabsf(cb.v[k] - v);
+    if (dist < best) { best = dist; code = k; }
+  }
+  return code;
+}
+
+__global__ void __launch_bounds__(kThreads) nf4_quant_kernel(const __nv_bfloat16* __restrict__ W,
+                                                              int64_t ldw, int N, int K,
+                                                              Codebook16 cb,
+                                                              uint8_t* __restrict__ qs,
+                                                              float* __restrict__ absmax) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int nb = K >> 6;
+  if (wid >= static_cast<int64_t>(N) * nb) return;
+  const int n = static_cast<int>(wid / nb);
+  const int b = static_cast<int>(wid - static_cast<int64_t>(n) * nb);
+  const uint32_t pair = *reinterpret_cast<const uint32_t*>(W + static_cast<int64_t>(n) * ldw + 64 * b + 2 * lane);
+  const float w0 = __uint_as_float(pair << 16), w1 = __uint_as_float(pair & 0xFFFF0000u);
+  float amax = fmaxf(fabsf(w0), fabsf(w1));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  float v0 = 0.f, v1 = 0.f;
+  if (amax != 0.0f) { v0 = w0 / amax; v1 = w1 / amax; }
+  const int c0 = nearest_level(v0, cb), c1 = nearest_level(v1, cb);
+  qs[static_cast<int64_t>(n) * (K >> 1) + 32 * b + lane] = static_cast<uint8_t>((c0 << 4) | c1);
+  if (lane == 0) absmax[static_cast<int64_t>(n) * nb + b] = amax;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_q8_1(const float* X, int64_t ldx, int M, int K, void* xq,
+                                 cudaStream_t st, Launch* info) {
+  const int64_t threads = static_cast<int64_t>(M) * (K / 4);
+  const int grid = static_cast<int>((threads + kThreads - 1) / kThreads);
+  info->grid_x = grid;
+  info->block = kThreads;
+  info->kernel = "quantize_q8_1";
+  q8_1_kernel<<<grid, kThreads, 0, st>>>(X, ldx, M, K, static_cast<uint8_t*>(xq));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_q4_0(const float* W, int64_t ldw, int N, int K, uint8_t* qs, void* d,
+                                 cudaStream_t st, Launch* info) {
+  const int64_t warps = static_cast<int64_t>(N) * (K / 32);
+  const int64_t grid = (warps * 32 + kThreads - 1) / kThreads;
+  info->grid_x = static_cast<int>(grid);
+  info->block = kThreads;
+  info->kernel = "quantize_q4_0";
+  q4_0_quant_kernel<<<static_cast<unsigned>(grid), kThreads, 0, st>>>(W, ldw, N, K, qs,
+                                                                       static_cast<__half*>(d));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_nf4(const void* W, int64_t ldw, int N, int K, const Codebook16& cb,
+                                uint8_t* qs, float* absmax, cudaStream_t st, Launch* info) {
+  const int64_t warps = static_cast<int64_t>(N) * (K / 64);
+  const int64_t grid = (warps * 32 + kThreads - 1) / kThreads;
+  info->grid_x = static_cast<int>(grid);
+  info->block = kThreads;
+  info->kernel = "quantize_nf4";
+  nf4_quant_kernel<<<static_cast<unsigned>(grid), kThreads, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(W), ldw, N, K, cb, qs, absmax);
+  return cudaGetLastError();
+}
+
+}  // namespace wobs
