@@ -226,10 +226,10 @@ def capture(fn, stream):
     return g
 
 
-def read_ceiling(device, stream):
+def read_ceiling(device, stream, nbytes=PROBE_BYTES):
     """Best streaming-read GB/s over load variants and grid sizes (bw_probe)."""
     import weight_only_bit_split_gb300 as wobs
-    buf = torch.empty(PROBE_BYTES, dtype=torch.uint8, device=device)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
     buf.fill_(0x5A)
     out = torch.zeros(1, dtype=torch.int32, device=device)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
@@ -249,7 +249,7 @@ def read_ceiling(device, stream):
                     e1.record(stream)
                     e1.synchronize()
                     ts.append(e0.elapsed_time(e1))
-                gbs = PROBE_BYTES / (statistics.median(ts) * 1e-3) / 1e9
+                gbs = nbytes / (statistics.median(ts) * 1e-3) / 1e9
                 table.append({"variant": variant, "grid": grid, "gbs": round(gbs, 1)})
                 if gbs > best[0]:
                     best = (gbs, {"variant": variant, "grid": grid})
@@ -779,8 +779,13 @@ def main(argv=None):
     ap.add_argument("--workload", default="q4_m1", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="wobs", choices=["wobs", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--probe-gib", type=int, default=PROBE_BYTES >> 30,
+                    help="size of the streaming-read ceiling buffer")
+    ap.add_argument("--profile", action="store_true",
+                    help="profiling case for ncu: build the workload, run --warmup + --steps "
+                         "steps eagerly on the default stream, no probe, no timing")
     args = ap.parse_args(argv)
-    if args.warmup < 3:
+    if args.warmup < 3 and not args.profile:
         ap.error("--warmup must be at least 3")
     cls = WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -790,10 +795,18 @@ def main(argv=None):
     rank, world, local = dist_env()
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.profile:
+        wl = cls(device)
+        for i in range(args.warmup + args.steps):
+            wl.step(i % wl.copies)
+        torch.cuda.synchronize(device)
+        print(f"profile case done: {cls.name}, {args.warmup + args.steps} steps, "
+              f"{wl.launches_per_step} launches per step", flush=True)
+        return 0
     init_dist("nccl")
     stream = torch.cuda.Stream(device)
 
-    ceiling, ceil_cfg, _ = read_ceiling(device, stream)
+    ceiling, ceil_cfg, ceil_table = read_ceiling(device, stream, args.probe_gib << 30)
     wl = cls(device)
     # eager pass first (kernel attributes, occupancy queries), then capture
     with torch.cuda.stream(stream):
@@ -868,7 +881,8 @@ def main(argv=None):
             "mbu": gbs / world / ceiling,
             "read_ceiling_gbs": round(ceiling, 1),
             "read_ceiling_how": f"bw_probe best of variants 1-3 x grids 1-8 CTAs/SM on an "
-                                f"{PROBE_BYTES >> 30} GiB buffer: {ceil_cfg}",
+                                f"{args.probe_gib} GiB buffer: {ceil_cfg}",
+            "read_ceiling_table": ceil_table,
             "us_per_call": per_call,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
