@@ -134,6 +134,35 @@ WOBS_API int wobs_gemv_bf16(const void* W, int64_t ldw, const void* X, int64_t l
                             size_t ws_bytes, void* stream);
 
 /*
+ * wobs_gemv_bf16 for callers that cannot give the library a workspace: the
+ * same computation, outputs and argmax rule, with the workspace taken from a
+ * fixed scratch array of WOBS_NOALLOC_SCRATCH_BYTES that the library keeps
+ * in device memory.  The pages have no counterpart to this entry point; it
+ * exists for code that may not allocate device memory when it calls the
+ * GEMV -- code running inside a CUDA graph capture, engines that reserve all
+ * their memory once at start-up through their own allocator, and plugins in
+ * a host process that owns every device allocation.
+ *
+ *   Arguments as wobs_gemv_bf16, without (ws, ws_bytes).  No cudaMalloc,
+ *   cudaFree or other allocating call is made.
+ *   - Shapes whose workspace (wobs_workspace_size(WOBS_OP_GEMV_BF16, M, N,
+ *     K)) exceeds WOBS_NOALLOC_SCRATCH_BYTES return
+ *     WOBS_ERR_WORKSPACE_TOO_SMALL.
+ *   - The first call made with a given device current looks up the scratch
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array: each call clears its counters and
+ *     keys on `stream` before the kernel, and calls that may overlap on the
+ *     GPU (unordered streams) race on the scratch and must not be issued.
+ *   - Every GPU that loads the library holds the array until the process
+ *     exits.
+ */
+#define WOBS_NOALLOC_SCRATCH_BYTES (4u << 20)
+WOBS_API int wobs_gemv_bf16_noalloc(const void* W, int64_t ldw, const void* X, int64_t ldx,
+                                    int M, float* logits, int64_t* argmax, int N, int K,
+                                    void* stream);
+
+/*
  * Q8_1 activation quantisation ("The kernel that waited for itself", section
  * "Seven variants, one microbenchmark, many mistakes": Q8_1 activations).
  * Per block of 32 consecutive elements of a column, IEEE float32:

@@ -178,6 +178,33 @@ def wobs_gemv_bf16(W, X, logits=None, argmax=None, want_argmax=False, ws=None):
     return logits, argmax
 
 
+def wobs_gemv_bf16_noalloc(W, X, logits=None, argmax=None, want_argmax=False):
+    """wobs_gemv_bf16 with the library's fixed scratch in place of a workspace.
+
+    For callers that may not allocate device memory at call time (inside a
+    CUDA graph capture, or under an engine that owns all device memory).
+    Pass preallocated ``logits`` / ``argmax`` to allocate nothing here either.
+    Calls that may overlap on the GPU share the scratch and must not be issued.
+    """
+    lib = _lib.get()
+    _need(W, "W", torch.bfloat16, 2)
+    X2 = X if X.dim() == 2 else X.view(1, -1)
+    _need(X2, "X", torch.bfloat16, 2, W.device)
+    M, K = X2.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError("W and X disagree on K")
+    if logits is None:
+        logits = torch.empty(M, N, dtype=torch.float32, device=W.device)
+    _need(logits, "logits", torch.float32, None, W.device)
+    if argmax is None and want_argmax:
+        argmax = torch.empty(M, dtype=torch.int64, device=W.device)
+    rc = lib.wobs_gemv_bf16_noalloc(_ptr(W), _rows(W), _ptr(X2), _rows(X2), M, _ptr(logits),
+                                    _ptr(argmax), N, K, _stream(W.device))
+    _check(rc, lib)
+    return logits, argmax
+
+
 def wobs_quantize_q8_1(X, xq=None):
     """Q8_1 blocks of fp32 activations X[M, K]: uint8 [M, K/32*36]."""
     lib = _lib.get()

@@ -26,6 +26,8 @@ SIGNATURES = {
                               c_void_p, c_size_t, c_void_p]),
     "wobs_gemv_bf16": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_int, c_void_p, c_void_p,
                                c_int, c_int, c_void_p, c_size_t, c_void_p]),
+    "wobs_gemv_bf16_noalloc": (c_int, [c_void_p, c_int64, c_void_p, c_int64, c_int, c_void_p,
+                                       c_void_p, c_int, c_int, c_void_p]),
     "wobs_quantize_q8_1": (c_int, [c_void_p, c_int64, c_int, c_int, c_void_p, c_void_p]),
     "wobs_quantize_q4_0": (c_int, [c_void_p, c_int64, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "wobs_quantize_nf4": (c_int, [c_void_p, c_int64, c_int, c_int, c_float_p, c_void_p, c_void_p,

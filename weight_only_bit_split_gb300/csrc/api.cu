@@ -186,6 +186,32 @@ int choose_splits(int op, int M, int N, int K) {
   }
 }
 
+// ---- helpers for entry points defined in other files ----
+
+size_t workspace_layout(int op, int M, int N, int K, size_t* zero_prefix_bytes) {
+  const WsLayout L = ws_layout(op, M, N, K);
+  if (zero_prefix_bytes) *zero_prefix_bytes = L.partials;
+  return L.total;
+}
+
+int prepare_workspace(int op, int M, int N, int K, int64_t* argmax, void* ws, size_t ws_bytes,
+                      SplitArgs* sk, ArgmaxArgs* am) {
+  Prepared p;
+  const int rc = prepare_ws(op, M, N, K, argmax, ws, ws_bytes, &p);
+  *sk = p.sk;
+  *am = p.am;
+  return rc;
+}
+
+int check_dense_args(const char* op, const void* W, int64_t ldw, const void* X, int64_t ldx, int M,
+                     const void* Y, int N, int K);
+
+int report_launch(cudaError_t e, const char* op, int M, int N, int K, const Launch& L, int splits) {
+  return finish_launch(e, op, M, N, K, L, splits);
+}
+
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 }  // namespace wobs
 
 extern "C" {
@@ -226,6 +252,17 @@ static int check_dense(const char* op, const void* W, int64_t ldw, const void* X
   if (!aligned4(Y)) return fail(WOBS_ERR_MISALIGNED, "%s: output not aligned", op);
   return WOBS_OK;
 }
+
+}  // extern "C"
+
+namespace wobs {
+int check_dense_args(const char* op, const void* W, int64_t ldw, const void* X, int64_t ldx, int M,
+                     const void* Y, int N, int K) {
+  return check_dense(op, W, ldw, X, ldx, M, Y, N, K);
+}
+}  // namespace wobs
+
+extern "C" {
 
 int wobs_gemv_f16(const void* W, int64_t ldw, const void* X, int64_t ldx, int M, void* Y, int N,
                   int K, void* ws, size_t ws_bytes, void* stream) {

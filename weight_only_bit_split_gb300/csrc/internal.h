@@ -70,4 +70,15 @@ int max_resident_ctas(const void* kernel, int block, int smem);  // per SM
 // Split factor chosen for an op (also sizes the workspace).
 int choose_splits(int op, int M, int N, int K);
 
+// Workspace bytes for (op, M, N, K); *zero_prefix_bytes receives how many
+// leading bytes hold counters and keys that must be zero before a call.
+size_t workspace_layout(int op, int M, int N, int K, size_t* zero_prefix_bytes);
+// Validates a workspace and points the split-K / argmax state into it.
+int prepare_workspace(int op, int M, int N, int K, int64_t* argmax, void* ws, size_t ws_bytes,
+                      SplitArgs* sk, ArgmaxArgs* am);
+int check_dense_args(const char* op, const void* W, int64_t ldw, const void* X, int64_t ldx, int M,
+                     const void* Y, int N, int K);
+int report_launch(cudaError_t e, const char* op, int M, int N, int K, const Launch& L, int splits);
+int set_error(int code, const char* msg);
+
 }  // namespace wobs
