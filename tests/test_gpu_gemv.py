@@ -13,10 +13,20 @@ from weight_only_bit_split_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["cp", "ldg"])
+def m1_path(request, monkeypatch):
+    """Run an M = 1 test through the async-copy kernels and the direct-load ones."""
+    if request.param == "ldg":
+        monkeypatch.setenv("WOBS_M1", "ldg")
+    else:
+        monkeypatch.delenv("WOBS_M1", raising=False)
+    return request.param
+
+
 # ----------------------------------------------------------------- dense
 
 @pytest.mark.parametrize("n,k", [(1, 8), (37, 264), (300, 4096), (1000, 4104), (4096, 4096)])
-def test_gemv_f16_m1(n, k):
+def test_gemv_f16_m1(n, k, m1_path):
     w = synth.weights(1, (n, k), dtype=torch.float16)
     x = synth.activations(1, (1, k), dtype=torch.float16)
     y = wobs.wobs_gemv_f16(w.to(dev()), x.to(dev())).cpu().float().numpy()
@@ -33,9 +43,9 @@ def test_gemv_f16_multi_column_strided(m, n, k):
     assert_within(y, oracle.gemv_dense(wn, xn), oracle.abs_dot_dense(wn, xn), "f16", "gemv_f16 M>1")
 
 
-@pytest.mark.parametrize("m,n,k", [(1, 1, 8), (1, 5000, 1024), (2, 777, 512), (5, 1200, 2048),
-                                   (32, 2000, 4096)])
-def test_gemv_bf16_logits_and_argmax(m, n, k):
+@pytest.mark.parametrize("m,n,k", [(1, 1, 8), (1, 5000, 1024), (1, 3001, 4104), (2, 777, 512),
+                                   (5, 1200, 2048), (32, 2000, 4096)])
+def test_gemv_bf16_logits_and_argmax(m, n, k, m1_path):
     w = synth.weights(5, (n, k), dtype=torch.bfloat16)
     x = synth.activations(5, (m, k), dtype=torch.bfloat16)
     logits, am = wobs.wobs_gemv_bf16(w.to(dev()), x.to(dev()), want_argmax=True)
@@ -43,6 +53,27 @@ def test_gemv_bf16_logits_and_argmax(m, n, k):
     wf, xf = w.float().numpy(), x.float().numpy()
     assert_within(lg, oracle.gemv_dense(wf, xf), oracle.abs_dot_dense(wf, xf), "f32", "gemv_bf16")
     assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(lg))
+
+
+def test_m1_dispatch_coverage(monkeypatch, capfd):
+    """The dispatch log names the kernel that ran (coverage, not assumption)."""
+    monkeypatch.setenv("WOBS_DEBUG", "1")
+    monkeypatch.delenv("WOBS_M1", raising=False)
+    (qs, d, xq), _, _, _ = _q4_case(64, 4096, 1)
+    wobs.wobs_gemv_q4_0_q8_1(qs, d, xq)
+    (qs2, d2, xq2), _, _, _ = _q4_case(64, 4160, 1)
+    wobs.wobs_gemv_q4_0_q8_1(qs2, d2, xq2)
+    w = synth.weights(5, (64, 512), dtype=torch.bfloat16).to(dev())
+    wobs.wobs_gemv_bf16(w, synth.activations(5, (1, 512), dtype=torch.bfloat16).to(dev()))
+    wobs.wobs_gemv_bf16(w, synth.activations(5, (3, 512), dtype=torch.bfloat16).to(dev()))
+    monkeypatch.setenv("WOBS_M1", "ldg")
+    wobs.wobs_gemv_q4_0_q8_1(qs, d, xq)
+    torch.cuda.synchronize()
+    err = capfd.readouterr().err
+    lines = [ln for ln in err.splitlines() if ln.startswith("wobs: op=")]
+    kernels = [ln.split("kernel=")[1].split()[0] for ln in lines]
+    assert kernels == ["q4_0_q8_1_m1_cp", "q4_0_q8_1_m1", "dense_m1_cp", "dense_mn",
+                       "q4_0_q8_1_m1"], kernels
 
 
 def test_gemv_bf16_argmax_ties_go_to_the_lowest_row():
@@ -97,7 +128,7 @@ def _q4_case(n, k, m, seed_copy=0):
 
 @pytest.mark.parametrize("n,k", [(1, 32), (7, 64), (100, 4096), (33, 14336), (64, 4160),
                                  (1024, 4096), (300, 1024)])
-def test_gemv_q4_0_m1(n, k):
+def test_gemv_q4_0_m1(n, k, m1_path):
     (qs, d, xq), ref, ad, _ = _q4_case(n, k, 1)
     y, am = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq, want_argmax=True)
     yn = y.cpu().numpy()

@@ -147,6 +147,11 @@ int max_resident_ctas(const void* kernel, int block, int smem) {
   return n;
 }
 
+bool m1_ldg_forced() {
+  const char* v = std::getenv("WOBS_M1");
+  return v && std::strcmp(v, "ldg") == 0;
+}
+
 int choose_splits(int op, int M, int N, int K) {
   const int forced = env_splits();
   const int groups = (N + kRowsPerGroup - 1) / kRowsPerGroup;

@@ -7,12 +7,52 @@
 #pragma once
 
 #include <cstdint>
+#include <cstdlib>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <utility>
 
 #include "internal.h"
 
 namespace wobs {
+
+// ------------------------------------------- programmatic dependent launch
+//
+// Decode-path kernels are launched with programmatic stream serialisation:
+// a kernel may start while the previous kernel on the stream is finishing.
+// Before pdl_wait() a kernel only reads its weight planes (never written by
+// a decode-path kernel); activations, outputs and the workspace are touched
+// only after pdl_wait(), which returns once the previous kernel has
+// completed and its writes are visible.  Kernels that write weights (the
+// Q4_0 / NF4 quantisers) never call pdl_launch_dependents, so a GEMV right
+// after them starts only when they are done.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+inline bool pdl_enabled() {
+  const char* v = std::getenv("WOBS_PDL");
+  return !(v && v[0] == '0');
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = (pdl && pdl_enabled()) ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 // ---------------------------------------------------------------- loads
 

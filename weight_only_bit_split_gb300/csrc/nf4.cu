@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(kThreads, 2) nf4_m1_kernel(const uint8_t* __re
     const int e = i / kLutCopies;
     lut[i] = make_float2(cb.v[e >> 4], cb.v[e & 15]);
   }
+  pdl_launch_dependents();
+  pdl_wait();
   // x element k = sl*1024 + l*32 + 4*j + t  ->  xsm[((sl*8 + j)*32 + l)*4 + t]
   for (int k = threadIdx.x; k < nsl * 1024; k += kThreads) {
     const int sl = k >> 10, l = (k >> 5) & 31, j = (k >> 2) & 7, t = k & 3;
@@ -189,10 +191,9 @@ cudaError_t run(const uint8_t* qs, const float* absmax, const Codebook16& cb, co
   info->block = kThreads;
   info->smem = smem;
   info->kernel = "nf4_m1";
-  nf4_m1_kernel<kArgmax><<<grid, kThreads, smem, st>>>(
-      qs, absmax, cb, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, K,
-      am);
-  return cudaGetLastError();
+  return launch_k(nf4_m1_kernel<kArgmax>, dim3(grid), dim3(kThreads), smem, st, true, qs, absmax,
+                  cb, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, K,
+                  am);
 }
 
 }  // namespace

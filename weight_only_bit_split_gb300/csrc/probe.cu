@@ -153,9 +153,10 @@ __global__ void __launch_bounds__(kProbeThreads) probe_bulk_kernel(const uint8_t
   for (size_t i = 0; i < mine; ++i) {
     const int s = static_cast<int>(i % kBulkStages);
     const uint32_t ph = static_cast<uint32_t>((i / kBulkStages) & 1);
-    if (!mbar_wait(&full[s], ph)) { s_abort = 1; }
+    const bool got = mbar_wait(&full[s], ph);
+    if (!got) s_abort = 1;
     __syncwarp();
-    if (s_abort) break;
+    if (__any_sync(0xffffffffu, !got || s_abort != 0)) break;   // warp-uniform exit
     const uint4* st = reinterpret_cast<const uint4*>(ring + s * kBulkChunk);
 #pragma unroll
     for (int u = 0; u < kBulkChunk / 16 / kProbeThreads; ++u) acc ^= xor4(st[u * kProbeThreads + threadIdx.x]);
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kProbeThreads) probe_bulk_kernel(const uint8_t
     }
   }
   if (threadIdx.x == 0 && s_abort) {
-    atomicExch(&g_error_word, 1);  // 1 = bulk-copy wait gave up
+    atomicExch(&g_error_word, kErrProbeWait);
     // let copies still in flight land before the CTA's shared memory goes
     for (size_t i = 0; i < issued && i < kBulkStages; ++i) {
       size_t j = issued - 1 - i;

@@ -76,7 +76,37 @@ __device__ __forceinline__ XBlock load_xblock(const uint8_t* blk) {
 
 // ------------------------------------------------------------- M = 1
 
-template <int U>
+constexpr int kU = 4;   // 16-byte chunks per lane per pipeline stage
+
+// One pipeline stage: kU blocks of one row (lane-strided) and their scales.
+struct Q4Stage {
+  uint4 q[kU];
+  uint16_t d[kU];
+};
+
+__device__ __forceinline__ void q4_load_stage(Q4Stage& st, const uint8_t* __restrict__ qs,
+                                              const uint16_t* __restrict__ d4, int row, int it,
+                                              int nb, int kh, int lane, uint64_t pol) {
+  const uint4* qr = reinterpret_cast<const uint4*>(qs + static_cast<int64_t>(row) * kh);
+  const uint16_t* dr = d4 + static_cast<int64_t>(row) * nb;
+#pragma unroll
+  for (int u = 0; u < kU; ++u) {
+    const int b = it * (32 * kU) + 32 * u + lane;
+    if (b < nb) {
+      st.q[u] = ld_stream16(qr + b, pol);
+      st.d[u] = ld_stream_u16(dr + b, pol);
+    } else {
+      st.q[u] = make_uint4(0u, 0u, 0u, 0u);
+      st.d[u] = 0;
+    }
+  }
+}
+
+// Each warp walks the (row, stage) sequence of its rows with two register
+// stages: the loads of stage t+1 are in flight while stage t is consumed, so
+// a warp always has 2 * kU * 16 bytes per lane outstanding, across row
+// boundaries too.  The first stage is issued before pdl_wait(), so it
+// overlaps the end of the previous kernel on the stream.
 __global__ void __launch_bounds__(kThreads) q4_m1_kernel(const uint8_t* __restrict__ qs,
                                                           const uint16_t* __restrict__ d4,
                                                           const uint8_t* __restrict__ xq,
@@ -84,6 +114,7 @@ __global__ void __launch_bounds__(kThreads) q4_m1_kernel(const uint8_t* __restri
                                                           ArgmaxArgs am) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int nb = K >> 5;
+  const int kh = K >> 1;
   int4* x_lo = reinterpret_cast<int4*>(smem);
   int4* x_hi = x_lo + nb;
   float* x_d = reinterpret_cast<float*>(x_hi + nb);
@@ -92,21 +123,19 @@ __global__ void __launch_bounds__(kThreads) q4_m1_kernel(const uint8_t* __restri
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int total_warps = gridDim.x * kWarps;
-  int row = blockIdx.x * kWarps + warp;
+  const int wg = blockIdx.x * kWarps + warp;
+  const int n_it = (nb + 32 * kU - 1) / (32 * kU);
+  const int rows_w = wg < N ? (N - 1 - wg) / total_warps + 1 : 0;
+  const int T = rows_w * n_it;
 
-  // Weight loads of this warp's first row go out before the activation
-  // staging, which only depends on a small L2-resident vector.
-  uint4 q[U];
-  uint16_t dh[U];
-  const bool full = (nb % (32 * U)) == 0;
-  if (full && row < N) {
-    const uint4* qrow = reinterpret_cast<const uint4*>(qs + static_cast<int64_t>(row) * (K >> 1));
-    const uint16_t* drow = d4 + static_cast<int64_t>(row) * nb;
-#pragma unroll
-    for (int u = 0; u < U; ++u) q[u] = ld_stream16(qrow + lane + 32 * u, pol);
-#pragma unroll
-    for (int u = 0; u < U; ++u) dh[u] = ld_stream_u16(drow + lane + 32 * u, pol);
-  }
+  Q4Stage sa, sb;
+  int lrow = wg, lit = 0;  // next stage to load
+  auto advance = [&](int& r, int& it) {
+    if (++it == n_it) { it = 0; r += total_warps; }
+  };
+  if (T > 0) { q4_load_stage(sa, qs, d4, lrow, lit, nb, kh, lane, pol); advance(lrow, lit); }
+  pdl_launch_dependents();
+  pdl_wait();
   for (int b = threadIdx.x; b < nb; b += kThreads) {
     const XBlock xb = load_xblock(xq + 36 * static_cast<int64_t>(b));
     x_lo[b] = xb.lo;
@@ -116,52 +145,37 @@ __global__ void __launch_bounds__(kThreads) q4_m1_kernel(const uint8_t* __restri
   }
   __syncthreads();
 
+  int crow = wg, cit = 0;
+  float acc0 = 0.f, acc1 = 0.f;
   uint64_t best = 0;
-  for (; row < N; row += total_warps) {
-    const uint4* qrow = reinterpret_cast<const uint4*>(qs + static_cast<int64_t>(row) * (K >> 1));
-    const uint16_t* drow = d4 + static_cast<int64_t>(row) * nb;
-    float acc0 = 0.f, acc1 = 0.f;
-    int b = lane;
-    if (full) {
-      for (; b < nb; b += 32 * U) {
-        if (b != lane) {
+  auto consume = [&](const Q4Stage& st) {
 #pragma unroll
-          for (int u = 0; u < U; ++u) q[u] = ld_stream16(qrow + b + 32 * u, pol);
-#pragma unroll
-          for (int u = 0; u < U; ++u) dh[u] = ld_stream_u16(drow + b + 32 * u, pol);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int bb = b + 32 * u;
-          const int dot = q4_dot_u(q[u], x_lo[bb], x_hi[bb]) - 8 * x_s[bb];
-          const float sc = half_bits_to_float(dh[u]) * x_d[bb];
-          if (u & 1) acc1 = fmaf(static_cast<float>(dot), sc, acc1);
-          else acc0 = fmaf(static_cast<float>(dot), sc, acc0);
-        }
-      }
-      // prefetch the next row's first chunk before the reduction
-      const int nrow = row + total_warps;
-      if (nrow < N) {
-        const uint4* nq = reinterpret_cast<const uint4*>(qs + static_cast<int64_t>(nrow) * (K >> 1));
-        const uint16_t* nd = d4 + static_cast<int64_t>(nrow) * nb;
-#pragma unroll
-        for (int u = 0; u < U; ++u) q[u] = ld_stream16(nq + lane + 32 * u, pol);
-#pragma unroll
-        for (int u = 0; u < U; ++u) dh[u] = ld_stream_u16(nd + lane + 32 * u, pol);
-      }
-    } else {
-      for (; b < nb; b += 32) {
-        const uint4 qq = ld_stream16(qrow + b, pol);
-        const uint16_t dd = ld_stream_u16(drow + b, pol);
-        const int dot = q4_dot_u(qq, x_lo[b], x_hi[b]) - 8 * x_s[b];
-        acc0 = fmaf(static_cast<float>(dot), half_bits_to_float(dd) * x_d[b], acc0);
+    for (int u = 0; u < kU; ++u) {
+      const int b = cit * (32 * kU) + 32 * u + lane;
+      if (b < nb) {
+        const int dot = q4_dot_u(st.q[u], x_lo[b], x_hi[b]) - 8 * x_s[b];
+        const float sc = half_bits_to_float(st.d[u]) * x_d[b];
+        if (u & 1) acc1 = fmaf(static_cast<float>(dot), sc, acc1);
+        else acc0 = fmaf(static_cast<float>(dot), sc, acc0);
       }
     }
-    const float s = warp_sum(acc0 + acc1);
-    if (lane == 0) y[row] = s;
-    if (am.out) {
-      const uint64_t k = argmax_key(s, static_cast<uint32_t>(row));
-      best = k > best ? k : best;
+    if (cit == n_it - 1) {
+      const float s = warp_sum(acc0 + acc1);
+      if (lane == 0) y[crow] = s;
+      if (am.out) {
+        const uint64_t k = argmax_key(s, static_cast<uint32_t>(crow));
+        best = k > best ? k : best;
+      }
+      acc0 = acc1 = 0.f;
+    }
+    advance(crow, cit);
+  };
+  for (int t = 0; t < T; t += 2) {
+    if (t + 1 < T) { q4_load_stage(sb, qs, d4, lrow, lit, nb, kh, lane, pol); advance(lrow, lit); }
+    consume(sa);
+    if (t + 1 < T) {
+      if (t + 2 < T) { q4_load_stage(sa, qs, d4, lrow, lit, nb, kh, lane, pol); advance(lrow, lit); }
+      consume(sb);
     }
   }
   if (am.out) {
@@ -177,6 +191,165 @@ __global__ void __launch_bounds__(kThreads) q4_m1_kernel(const uint8_t* __restri
     __syncthreads();
     argmax_publish(s_cta, 1, am, gridDim.x);
   }
+}
+
+// ------------------------------------------- M = 1, cp.async staging
+
+// The warp-per-row computation with the weight stream staged through
+// shared memory by asynchronous copies (cp.async, 16 bytes per lane): each
+// warp owns a ring of kRing segments of kSegBlocks blocks (2048 bytes of
+// nibbles + 256 bytes of scales).  All kRing segments are requested before
+// pdl_wait, so the stream starts while the previous kernel finishes; each
+// segment is refilled with the one kRing further on while the next is
+// consumed.  Reads from the ring are lane-contiguous 16-byte loads (no bank
+// conflicts).  16 warps per CTA and two CTAs per SM: the measured optimum
+// on GB300 between bytes in flight and warps available to consume them.
+constexpr int kCpWarps = 16;
+constexpr int kCpThreads = kCpWarps * 32;
+constexpr int kSegBlocks = 128;
+constexpr int kSegQs = kSegBlocks * 16;
+constexpr int kSegBytes = kSegQs + kSegBlocks * 2;
+constexpr int kRing = 2;
+constexpr int kRingBytes = kCpWarps * kRing * kSegBytes;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+               :: "r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+template <bool kArgmax>
+__global__ void __launch_bounds__(kCpThreads) q4_m1_cp_kernel(const uint8_t* __restrict__ qs,
+                                                               const uint16_t* __restrict__ d4,
+                                                               const uint8_t* __restrict__ xq,
+                                                               float* __restrict__ y, int N, int K,
+                                                               ArgmaxArgs am) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int nb = K >> 5;
+  const int kh = K >> 1;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int total_warps = gridDim.x * kCpWarps;
+  const int wg = blockIdx.x * kCpWarps + warp;
+  const int nseg = (nb + kSegBlocks - 1) / kSegBlocks;
+  const int rows_w = wg < N ? (N - 1 - wg) / total_warps + 1 : 0;
+  const int T = rows_w * nseg;
+  uint8_t* myring = smem + warp * (kRing * kSegBytes);
+  int4* x_lo = reinterpret_cast<int4*>(smem + kRingBytes);
+  int4* x_hi = x_lo + nb;
+  float* x_d = reinterpret_cast<float*>(x_hi + nb);
+  int* x_s = reinterpret_cast<int*>(x_d + nb);
+
+  int prow = wg, pseg = 0;   // next segment to request
+  auto issue = [&](int slot) {
+    uint8_t* st = myring + slot * kSegBytes;
+    const int b0 = pseg * kSegBlocks;
+    const int n = min(kSegBlocks, nb - b0);
+    const uint8_t* qr = qs + static_cast<int64_t>(prow) * kh + b0 * 16;
+#pragma unroll
+    for (int u = 0; u < kSegBlocks / 32; ++u) {
+      const int bl = 32 * u + lane;
+      if (bl < n) cp_async16(st + 16 * bl, qr + 16 * bl);
+    }
+    const uint8_t* dr = reinterpret_cast<const uint8_t*>(d4 + static_cast<int64_t>(prow) * nb + b0);
+    if (lane < n / 8) cp_async16(st + kSegQs + 16 * lane, dr + 16 * lane);
+    if (++pseg == nseg) { pseg = 0; prow += total_warps; }
+  };
+  // request the first kRing-1 segments before waiting for the previous kernel
+#pragma unroll
+  for (int i = 0; i < kRing - 1; ++i) {
+    if (i < T) issue(i);
+    cp_async_commit();
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  for (int b = threadIdx.x; b < nb; b += kCpThreads) {
+    const XBlock xb = load_xblock(xq + 36 * static_cast<int64_t>(b));
+    x_lo[b] = xb.lo;
+    x_hi[b] = xb.hi;
+    x_d[b] = xb.d;
+    x_s[b] = xb.s;
+  }
+  __syncthreads();
+
+  int crow = wg, cseg = 0;
+  float acc0 = 0.f, acc1 = 0.f;
+  uint64_t best = 0;
+  for (int t = 0; t < T; ++t) {
+    // request segment t+kRing-1 (into the slot consumed last), then wait for segment t
+    if (t + kRing - 1 < T) issue((t + kRing - 1) % kRing);
+    cp_async_commit();
+    cp_async_wait<kRing - 1>();
+    __syncwarp();
+    const uint8_t* st = myring + (t % kRing) * kSegBytes;
+    const int b0 = cseg * kSegBlocks;
+    const int n = min(kSegBlocks, nb - b0);
+#pragma unroll
+    for (int u = 0; u < kSegBlocks / 32; ++u) {
+      const int bl = 32 * u + lane;
+      if (bl < n) {
+        const uint4 q = *reinterpret_cast<const uint4*>(st + 16 * bl);
+        const uint16_t dh = *reinterpret_cast<const uint16_t*>(st + kSegQs + 2 * bl);
+        const int b = b0 + bl;
+        const int dot = q4_dot_u(q, x_lo[b], x_hi[b]) - 8 * x_s[b];
+        const float sc = half_bits_to_float(dh) * x_d[b];
+        if (u & 1) acc1 = fmaf(static_cast<float>(dot), sc, acc1);
+        else acc0 = fmaf(static_cast<float>(dot), sc, acc0);
+      }
+    }
+    if (cseg == nseg - 1) {
+      const float sum = warp_sum(acc0 + acc1);
+      if (lane == 0) y[crow] = sum;
+      if (kArgmax) {
+        const uint64_t k = argmax_key(sum, static_cast<uint32_t>(crow));
+        best = k > best ? k : best;
+      }
+      acc0 = acc1 = 0.f;
+    }
+    if (++cseg == nseg) { cseg = 0; crow += total_warps; }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  if (kArgmax) {
+    __shared__ uint64_t s_best[kCpWarps];
+    __shared__ uint64_t s_cta[1];
+    if (lane == 0) s_best[warp] = best;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint64_t bk = 0;
+      for (int i = 0; i < kCpWarps; ++i) bk = s_best[i] > bk ? s_best[i] : bk;
+      s_cta[0] = bk;
+    }
+    __syncthreads();
+    argmax_publish(s_cta, 1, am, gridDim.x);
+  }
+}
+
+template <bool kArgmax>
+cudaError_t run_m1_cp_t(const uint8_t* qs, const void* d, const void* xq, float* y, int N, int K,
+                        const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
+  const int nb = K / 32;
+  const int smem = kRingBytes + nb * 40;
+  cudaError_t e = cudaFuncSetAttribute(q4_m1_cp_kernel<kArgmax>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int grid = 2 * device_sm_count();
+  const int need = (N + kCpWarps - 1) / kCpWarps;
+  if (grid > need) grid = need;
+  info->grid_x = grid;
+  info->block = kCpThreads;
+  info->smem = smem;
+  info->kernel = "q4_0_q8_1_m1_cp";
+  return launch_k(q4_m1_cp_kernel<kArgmax>, dim3(grid), dim3(kCpThreads), smem, st, true, qs,
+                  static_cast<const uint16_t*>(d), static_cast<const uint8_t*>(xq), y, N, K, am);
+}
+
+cudaError_t run_m1_cp(const uint8_t* qs, const void* d, const void* xq, float* y, int N, int K,
+                      const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
+  return am.out ? run_m1_cp_t<true>(qs, d, xq, y, N, K, am, st, info)
+                : run_m1_cp_t<false>(qs, d, xq, y, N, K, am, st, info);
 }
 
 // --------------------------------------------------------- M columns
@@ -202,6 +375,8 @@ __global__ void __launch_bounds__(kThreads) q4_mn_kernel(const uint8_t* __restri
   const int s = blockIdx.y;
   const int b0 = s * bps;
   const int b1 = min(nb, b0 + bps);
+  pdl_launch_dependents();
+  pdl_wait();
   for (int i = threadIdx.x; i < (b1 - b0) * NC; i += kThreads) {
     const int bl = i / NC, m = i - bl * NC;
     XS v;
@@ -299,33 +474,29 @@ cudaError_t run_mn(const uint8_t* qs, const void* d, const void* xq, int M, floa
   info->block = kThreads;
   info->smem = smem;
   info->kernel = "q4_0_q8_1_mn";
-  q4_mn_kernel<NC><<<grid, kThreads, smem, st>>>(qs, static_cast<const uint16_t*>(d),
-                                                  static_cast<const uint8_t*>(xq), M, Y, N, K,
-                                                  bps, s2, am);
-  return cudaGetLastError();
+  return launch_k(q4_mn_kernel<NC>, grid, dim3(kThreads), smem, st, true, qs,
+                  static_cast<const uint16_t*>(d), static_cast<const uint8_t*>(xq), M, Y, N, K,
+                  bps, s2, am);
 }
 
-template <int U>
 cudaError_t run_m1(const uint8_t* qs, const void* d, const void* xq, float* y, int N, int K,
                    const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   const int nb = K / 32;
   const int smem = nb * 40;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(q4_m1_kernel<U>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(q4_m1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  const int per_sm = max_resident_ctas(reinterpret_cast<const void*>(q4_m1_kernel<U>), kThreads, smem);
+  const int per_sm = max_resident_ctas(reinterpret_cast<const void*>(q4_m1_kernel), kThreads, smem);
   int grid = device_sm_count() * (per_sm > 0 ? per_sm : 1);
   const int need = (N + kWarps - 1) / kWarps;
   if (grid > need) grid = need;
   info->grid_x = grid;
   info->block = kThreads;
   info->smem = smem;
-  info->kernel = U == 4 ? "q4_0_q8_1_m1_u4" : (U == 2 ? "q4_0_q8_1_m1_u2" : "q4_0_q8_1_m1_u1");
-  q4_m1_kernel<U><<<grid, kThreads, smem, st>>>(qs, static_cast<const uint16_t*>(d),
-                                                 static_cast<const uint8_t*>(xq), y, N, K, am);
-  return cudaGetLastError();
+  info->kernel = "q4_0_q8_1_m1";
+  return launch_k(q4_m1_kernel, dim3(grid), dim3(kThreads), smem, st, true, qs,
+                  static_cast<const uint16_t*>(d), static_cast<const uint8_t*>(xq), y, N, K, am);
 }
 
 // ------------------------------------------------------- block dots
@@ -353,10 +524,12 @@ cudaError_t launch_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* 
                                   float* Y, int N, int K, const SplitArgs& sk,
                                   const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   if (M == 1 && sk.splits <= 1) {
-    const int nb = K / 32;
-    if (nb % 128 == 0) return run_m1<4>(qs, d, xq, Y, N, K, am, st, info);
-    if (nb % 64 == 0) return run_m1<2>(qs, d, xq, Y, N, K, am, st, info);
-    return run_m1<1>(qs, d, xq, Y, N, K, am, st, info);
+    
+    // 16-byte asynchronous copies need 16-byte aligned scale segments
+    const bool cp_ok = (K % 256 == 0) && (reinterpret_cast<uintptr_t>(d) % 16 == 0) &&
+                       (kRingBytes + (K / 32) * 40 <= 200 * 1024);
+    if (cp_ok && !m1_ldg_forced()) return run_m1_cp(qs, d, xq, Y, N, K, am, st, info);
+    return run_m1(qs, d, xq, Y, N, K, am, st, info);
   }
   if (M <= 1) return run_mn<1>(qs, d, xq, M, Y, N, K, sk, am, st, info);
   if (M <= 2) return run_mn<2>(qs, d, xq, M, Y, N, K, sk, am, st, info);

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kThreads) q8_1_kernel(const float* __restrict_
   const int m = valid ? static_cast<int>(t / per_col) : 0;
   const int k4 = valid ? static_cast<int>(t - static_cast<int64_t>(m) * per_col) : 0;
   float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  pdl_launch_dependents();
+  pdl_wait();
   if (valid) v = *reinterpret_cast<const float4*>(X + static_cast<int64_t>(m) * ldx + 4 * k4);
   float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 #pragma unroll
@@ -123,8 +125,8 @@ cudaError_t launch_quantize_q8_1(const float* X, int64_t ldx, int M, int K, void
   info->grid_x = grid;
   info->block = kThreads;
   info->kernel = "quantize_q8_1";
-  q8_1_kernel<<<grid, kThreads, 0, st>>>(X, ldx, M, K, static_cast<uint8_t*>(xq));
-  return cudaGetLastError();
+  return launch_k(q8_1_kernel, dim3(grid), dim3(kThreads), 0, st, true, X, ldx, M, K,
+                  static_cast<uint8_t*>(xq));
 }
 
 cudaError_t launch_quantize_q4_0(const float* W, int64_t ldw, int N, int K, uint8_t* qs, void* d,
