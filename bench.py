@@ -301,7 +301,7 @@ class Q4M1:
     name = "q4_0_q8_1_m1_8b_shapes"
     shapes = [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)]
     dtype = "int8"
-    kernel = "q4_0_q8_1_m1"
+    kernel = "q4_0_q8_1_m1_cp"
     kernel_src = "q4_0.cu"
     workload_id = 2
 
