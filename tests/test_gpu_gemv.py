@@ -72,7 +72,7 @@ def test_m1_dispatch_coverage(monkeypatch, capfd):
     err = capfd.readouterr().err
     lines = [ln for ln in err.splitlines() if ln.startswith("wobs: op=")]
     kernels = [ln.split("kernel=")[1].split()[0] for ln in lines]
-    assert kernels == ["q4_0_q8_1_m1_cp", "q4_0_q8_1_m1", "dense_m1_cp", "dense_mn",
+    assert kernels == ["q4_0_q8_1_m1_cp", "q4_0_q8_1_m1", "dense_m1_cp", "dense_mma",
                        "q4_0_q8_1_m1"], kernels
 
 

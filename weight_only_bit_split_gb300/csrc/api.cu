@@ -49,7 +49,7 @@ void log_dispatch(const char* op, int M, int N, int K, const wobs::Launch& L, in
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-constexpr int kRowsPerGroup = 256;   // rows per CTA in the multi-column kernels
+constexpr int kRowsPerGroup = 128;   // smallest row group of the multi-column kernels
 
 struct WsLayout {
   size_t counter = 0, keys = 0, groups = 0, partials = 0, total = 0;

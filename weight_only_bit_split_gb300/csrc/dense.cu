@@ -15,6 +15,7 @@
 // registers.  K is split over CTAs when the rows alone cannot fill the GPU;
 // the last CTA of a row group adds the partial sums in a fixed order.
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace wobs {
 namespace {
@@ -22,7 +23,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnroll = 8;    // 16-byte chunks per lane per pipeline stage
-constexpr int kTileK = 256;   // activation elements staged per K tile
 
 // ------------------------------------------------------------- M = 1
 
@@ -263,133 +263,245 @@ cudaError_t run_m1_cp(const void* W, int64_t ldw, const void* x, void* y, int N,
 
 // --------------------------------------------------------- M columns
 
-// Per-column best keys of the rows this CTA finalised, then publish.
-template <int NC>
-__device__ __forceinline__ void cta_argmax_cols(const float* v, bool valid, int row, int M,
-                                                const ArgmaxArgs& am) {
-  __shared__ uint64_t s_key[kWarps][NC];
-  __shared__ uint64_t s_cta[NC];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int m = 0; m < NC; ++m) {
-    uint64_t k = valid ? argmax_key(v[m], static_cast<uint32_t>(row)) : 0ull;
-    k = warp_max_u64(k);
-    if (lane == 0) s_key[warp][m] = k;
-  }
-  __syncthreads();
-  if (threadIdx.x < NC) {
-    uint64_t b = 0;
-    for (int w = 0; w < kWarps; ++w) b = s_key[w][threadIdx.x] > b ? s_key[w][threadIdx.x] : b;
-    s_cta[threadIdx.x] = b;
-  }
-  __syncthreads();
-  argmax_publish(s_cta, M, am, gridDim.x);
+// M > 1: tensor cores (mma.sync m16n8k16, fp32 accumulate).  Each warp owns
+// 16 weight rows, a CTA 256 rows; the activation columns (padded to
+// multiples of 8, one n-tile each) are the MMA's N side.  The contraction
+// order inside an MMA is free, so k-slots are permuted to make every
+// fragment one contiguous 16-byte piece: for each 32-element chunk, lane
+// (g, t) takes elements 8t..8t+7 of weight rows g and g+8 and of activation
+// column g; the first four feed MMA 0, the last four MMA 1.
+//
+// Weights: every lane streams its own two 16-byte pieces per chunk through
+// a private ring of kWS slots in shared memory with cp.async (zero-filled
+// past K), kWS-1 chunks ahead, across K-tile and row-tile boundaries; the
+// first kWS-1 are requested before pdl_wait.  Activations: K tiles of 512
+// elements per column, brought in by 1-D bulk copies (TMA) into two
+// alternating buffers completed on mbarriers (waits are bounded), one tile
+// ahead.  Outputs go straight from the accumulator fragments to memory (8
+// consecutive rows per column = one 32-byte sector).  K is split over CTAs
+// when the row tiles alone cannot fill the GPU.
+constexpr int kMW = 16;
+constexpr int kMThreads = kMW * 32;
+constexpr int kMRows = kMW * 16;             // rows per CTA tile
+constexpr int kWS = 8;                       // weight ring slots per lane (32 bytes each)
+constexpr int kKT = 512;                     // activation K tile (elements)
+constexpr int kXStride = kKT * 2 + 64;       // bytes per staged column (bank-conflict free)
+
+template <typename T>
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1);
+template <>
+__device__ __forceinline__ void mma16816<__half>(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                                 uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float* d, uint32_t a0, uint32_t a1,
+                                                        uint32_t a2, uint32_t a3, uint32_t b0,
+                                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <typename T, typename TO, int NC>
-__global__ void __launch_bounds__(kThreads) dense_mn_kernel(const T* __restrict__ W, int64_t ldw,
-                                                             const T* __restrict__ X, int64_t ldx,
-                                                             int M, TO* __restrict__ Y, int N,
-                                                             int K, int kps, SplitArgs sk,
-                                                             ArgmaxArgs am) {
-  __shared__ __align__(16) float xs[NC][kTileK];
-  const int row = blockIdx.x * kThreads + threadIdx.x;
-  const bool valid = row < N;
+template <typename T, typename TO, int NT>
+__global__ void __launch_bounds__(kMThreads, 1) dense_mma_kernel(const T* __restrict__ W, int64_t ldw,
+                                                                  const T* __restrict__ X, int64_t ldx,
+                                                                  int M, TO* __restrict__ Y, int N,
+                                                                  int K, int kps, SplitArgs sk,
+                                                                  ArgmaxArgs am, int* err) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int kXBuf = NT * 8 * kXStride;
+  uint8_t* xbuf = smem;                                  // [2][NT*8][kXStride]
+  uint8_t* wring = smem + 2 * kXBuf;                     // [kMThreads][kWS][32]
+  __shared__ __align__(8) uint64_t xbar[2];
+  __shared__ uint64_t s_cta[NT * 8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
   const int s = blockIdx.y;
   const int k0 = s * kps;
   const int k1 = min(K, k0 + kps);
-  float acc[NC];
+  const int nch = (k1 - k0 + 31) / 32;
+  const int nkt = (k1 - k0 + kKT - 1) / kKT;
+  const int ntiles = (N + kMRows - 1) / kMRows;
+  const int my_tiles = static_cast<int>(blockIdx.x) < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  uint8_t* myw = wring + tid * (kWS * 32);
+
+  int ptile = blockIdx.x, pch = 0;        // weight chunk producer cursor
+  auto wissue = [&](int slot) {
+    const int r0 = ptile * kMRows + warp * 16;
+    const int ra = min(r0 + g, N - 1), rb = min(r0 + g + 8, N - 1);
+    const int e = k0 + 32 * pch + 8 * t;
+    const bool v = e < k1;
+    const T* pa = W + static_cast<int64_t>(ra) * ldw + (v ? e : 0);
+    const T* pb = W + static_cast<int64_t>(rb) * ldw + (v ? e : 0);
+    cp_async16_zfill(myw + slot * 32, pa, v);
+    cp_async16_zfill(myw + slot * 32 + 16, pb, v);
+    if (++pch == nch) { pch = 0; ptile += gridDim.x; }
+  };
+  const int TW = my_tiles * nch;
 #pragma unroll
-  for (int m = 0; m < NC; ++m) acc[m] = 0.f;
-  const T* wr = W + static_cast<int64_t>(valid ? row : 0) * ldw;
+  for (int i = 0; i < kWS - 1; ++i) {
+    if (i < TW) wissue(i);
+    cp_async_commit_group();
+  }
+  for (int i = tid; i < 2 * kXBuf / 16; i += kMThreads)
+    reinterpret_cast<uint4*>(xbuf)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (tid == 0) {
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
   pdl_launch_dependents();
   pdl_wait();
 
-  for (int kt = k0; kt < k1; kt += kTileK) {
-    const int kn = min(kTileK, k1 - kt);
-    __syncthreads();
-    for (int i = threadIdx.x; i < NC * kn; i += kThreads) {
-      const int m = i / kn, k = i - m * kn;
-      xs[m][k] = m < M ? to_float(X[static_cast<int64_t>(m) * ldx + kt + k]) : 0.f;
-    }
-    __syncthreads();
-    if (valid) {
-      for (int c = 0; c < kn; c += 8) {
-        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wr + kt + c));
-        const T* tag = nullptr;
-        const float2 a = to_float2(wv.x, tag), b = to_float2(wv.y, tag);
-        const float2 e = to_float2(wv.z, tag), f = to_float2(wv.w, tag);
+  const int TX = my_tiles * nkt;
+  auto xissue = [&](int q) {              // thread 0: activation tile q into buffer q & 1
+    const int kb = k0 + (q % nkt) * kKT;
+    const int kn = min(kKT, k1 - kb);
+    uint64_t* bar = &xbar[q & 1];
+    uint8_t* dst = xbuf + (q & 1) * kXBuf;
+    mbar_expect_tx(bar, static_cast<uint32_t>(M * kn * 2));
+    for (int col = 0; col < M; ++col)
+      bulk_g2s(dst + col * kXStride, X + static_cast<int64_t>(col) * ldx + kb, kn * 2, bar);
+  };
+  if (tid == 0) {
+    if (TX > 0) xissue(0);
+    if (TX > 1) xissue(1);
+  }
+
+  bool ok = true;
+  int q = 0, wi = 0;
+  for (int j = 0; j < my_tiles; ++j) {
+    const int tile = blockIdx.x + j * gridDim.x;
+    float d[NT][4];
 #pragma unroll
-        for (int m = 0; m < NC; ++m) {
-          const float4 x0 = *reinterpret_cast<const float4*>(&xs[m][c]);
-          const float4 x1 = *reinterpret_cast<const float4*>(&xs[m][c + 4]);
-          float t = acc[m];
-          t = fmaf(a.x, x0.x, t); t = fmaf(a.y, x0.y, t);
-          t = fmaf(b.x, x0.z, t); t = fmaf(b.y, x0.w, t);
-          t = fmaf(e.x, x1.x, t); t = fmaf(e.y, x1.y, t);
-          t = fmaf(f.x, x1.z, t); t = fmaf(f.y, x1.w, t);
-          acc[m] = t;
+    for (int n = 0; n < NT; ++n) d[n][0] = d[n][1] = d[n][2] = d[n][3] = 0.f;
+    for (int kt = 0; kt < nkt; ++kt, ++q) {
+      if (ok) ok = mbar_wait(&xbar[q & 1], static_cast<uint32_t>((q >> 1) & 1));
+      const uint8_t* xs = xbuf + (q & 1) * kXBuf + g * kXStride + 16 * t;
+      const int kc = (min(kKT, k1 - k0 - kt * kKT) + 31) / 32;
+      for (int cc = 0; cc < kc; ++cc, ++wi) {
+        if (wi + kWS - 1 < TW) wissue((wi + kWS - 1) % kWS);
+        cp_async_commit_group();
+        cp_async_wait_group<kWS - 1>();
+        const uint8_t* wsl = myw + (wi % kWS) * 32;
+        const uint4 a = *reinterpret_cast<const uint4*>(wsl);
+        const uint4 b = *reinterpret_cast<const uint4*>(wsl + 16);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + n * 8 * kXStride + 64 * cc);
+          mma16816<T>(d[n], a.x, b.x, a.y, b.y, xv.x, xv.y);
+          mma16816<T>(d[n], a.z, b.z, a.w, b.w, xv.z, xv.w);
         }
       }
+      __syncthreads();                     // everyone is done with buffer q & 1
+      if (tid == 0 && q + 2 < TX) {
+        fence_proxy_async_smem();
+        xissue(q + 2);
+      }
     }
-  }
-
-  if (sk.splits > 1) {
-    if (valid) {
+    // outputs of this tile, straight from the fragments
+    const int rbase = tile * kMRows;
+    const int rg = rbase + warp * 16 + g;
+    bool finish = true;
+    if (sk.splits > 1) {
 #pragma unroll
-      for (int m = 0; m < NC; ++m)
-        if (m < M) sk.partials[(static_cast<int64_t>(s) * M + m) * N + row] = acc[m];
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int col = n * 8 + 2 * t + (h & 1), row = rg + 8 * (h >> 1);
+          if (col < M && row < N) sk.partials[(static_cast<int64_t>(s) * M + col) * N + row] = d[n][h];
+        }
+      finish = splitk_arrive_last(sk.counters, tile, sk.splits);
+      if (finish) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int col = n * 8 + 2 * t + (h & 1), row = rg + 8 * (h >> 1);
+            float acc = 0.f;
+            if (col < M && row < N)
+              for (int sp = 0; sp < sk.splits; ++sp)
+                acc += __ldcg(sk.partials + (static_cast<int64_t>(sp) * M + col) * N + row);
+            d[n][h] = acc;
+          }
+      }
     }
-    if (!splitk_arrive_last(sk.counters, blockIdx.x, sk.splits)) return;
-    if (valid) {
+    if (finish) {
 #pragma unroll
-      for (int m = 0; m < NC; ++m) {
-        float t = 0.f;
-        if (m < M)
-          for (int j = 0; j < sk.splits; ++j)
-            t += __ldcg(sk.partials + (static_cast<int64_t>(j) * M + m) * N + row);
-        acc[m] = t;
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int col = n * 8 + 2 * t + (h & 1), row = rg + 8 * (h >> 1);
+          if (col < M && row < N) Y[static_cast<int64_t>(col) * N + row] = from_float<TO>(d[n][h]);
+        }
+      if (am.out) {
+        __syncthreads();                   // this tile's outputs are written
+        for (int col = warp; col < M; col += kMW) {
+          uint64_t k = 0;
+          for (int rl = lane; rl < kMRows; rl += 32) {
+            const int row = rbase + rl;
+            if (row < N) {
+              const uint64_t kk = argmax_key(to_float(Y[static_cast<int64_t>(col) * N + row]),
+                                             static_cast<uint32_t>(row));
+              k = kk > k ? kk : k;
+            }
+          }
+          k = warp_max_u64(k);
+          if (lane == 0) s_cta[col] = k;
+        }
+        __syncthreads();
+        argmax_publish(s_cta, M, am, ntiles);
       }
     }
   }
-  float out[NC];
-#pragma unroll
-  for (int m = 0; m < NC; ++m) {
-    const TO o = from_float<TO>(acc[m]);
-    out[m] = to_float(o);
-    if (valid && m < M) Y[static_cast<int64_t>(m) * N + row] = o;
-  }
-  if (am.out) cta_argmax_cols<NC>(out, valid, row, M, am);
+  cp_async_wait_group<0>();
+  if (!ok && err) atomicExch(err, kErrGemvWait);
 }
 
-template <typename T, typename TO, int NC>
-cudaError_t run_mn(const void* W, int64_t ldw, const void* X, int64_t ldx, int M, void* Y, int N,
-                   int K, const SplitArgs& sk, const ArgmaxArgs& am, cudaStream_t st,
-                   Launch* info) {
-  const int kps = (((K + sk.splits - 1) / sk.splits) + 7) / 8 * 8;
+template <typename T, typename TO, int NT>
+cudaError_t run_mma(const void* W, int64_t ldw, const void* X, int64_t ldx, int M, void* Y, int N,
+                    int K, const SplitArgs& sk, const ArgmaxArgs& am, cudaStream_t st,
+                    Launch* info) {
+  // K range per split: a multiple of the activation tile
+  const int kps = (((K + sk.splits - 1) / sk.splits) + kKT - 1) / kKT * kKT;
   const int splits = (K + kps - 1) / kps;
-  dim3 grid((N + kThreads - 1) / kThreads, splits);
+  const int ntiles = (N + kMRows - 1) / kMRows;
+  const int smem = 2 * NT * 8 * kXStride + kMThreads * kWS * 32;
+  cudaError_t e = cudaFuncSetAttribute(dense_mma_kernel<T, TO, NT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int gx = device_sm_count();
+  if (splits > 1 || gx > ntiles) gx = ntiles;   // split-K: one CTA per (tile, split)
   SplitArgs s2 = sk;
   s2.splits = splits;
-  info->grid_x = grid.x;
-  info->grid_y = grid.y;
-  info->block = kThreads;
-  info->kernel = "dense_mn";
-  return launch_k(dense_mn_kernel<T, TO, NC>, grid, dim3(kThreads), 0, st, true,
+  info->grid_x = gx;
+  info->grid_y = splits;
+  info->block = kMThreads;
+  info->smem = smem;
+  info->kernel = "dense_mma";
+  return launch_k(dense_mma_kernel<T, TO, NT>, dim3(gx, splits), dim3(kMThreads), smem, st, true,
                   static_cast<const T*>(W), ldw, static_cast<const T*>(X), ldx, M,
-                  static_cast<TO*>(Y), N, K, kps, s2, am);
+                  static_cast<TO*>(Y), N, K, kps, s2, am, error_word_ptr());
 }
 
 template <typename T, typename TO>
 cudaError_t dispatch_mn(const void* W, int64_t ldw, const void* X, int64_t ldx, int M, void* Y,
                         int N, int K, const SplitArgs& sk, const ArgmaxArgs& am, cudaStream_t st,
                         Launch* info) {
-  if (M <= 1) return run_mn<T, TO, 1>(W, ldw, X, ldx, M, Y, N, K, sk, am, st, info);
-  if (M <= 2) return run_mn<T, TO, 2>(W, ldw, X, ldx, M, Y, N, K, sk, am, st, info);
-  if (M <= 4) return run_mn<T, TO, 4>(W, ldw, X, ldx, M, Y, N, K, sk, am, st, info);
-  if (M <= 8) return run_mn<T, TO, 8>(W, ldw, X, ldx, M, Y, N, K, sk, am, st, info);
-  if (M <= 16) return run_mn<T, TO, 16>(W, ldw, X, ldx, M, Y, N, K, sk, am, st, info);
-  return run_mn<T, TO, 32>(W, ldw, X, ldx, M, Y, N, K, sk, am, st, info);
+  if (M <= 8) return run_mma<T, TO, 1>(W, ldw, X, ldx, M, Y, N, K, sk, am, st, info);
+  if (M <= 16) return run_mma<T, TO, 2>(W, ldw, X, ldx, M, Y, N, K, sk, am, st, info);
+  if (M <= 24) return run_mma<T, TO, 3>(W, ldw, X, ldx, M, Y, N, K, sk, am, st, info);
+  return run_mma<T, TO, 4>(W, ldw, X, ldx, M, Y, N, K, sk, am, st, info);
 }
 
 template <typename T, typename TO>

@@ -237,6 +237,21 @@ cudaError_t launch_bw_probe(const void* buf, size_t bytes, int grid, int variant
   return cudaGetLastError();
 }
 
+int* error_word_ptr() {
+  static int* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
 cudaError_t read_and_clear_error_word(cudaStream_t st, int* host_out) {
   int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbolAsync(host_out, g_error_word, sizeof(int), 0,
