@@ -32,9 +32,10 @@
  *     give 16-byte aligned rows; violations return WOBS_ERR_MISALIGNED.
  *   - Workspace: calls that take (ws, ws_bytes) need at least
  *     wobs_workspace_size(op, M, N, K) bytes, ZERO-FILLED before its first
- *     use.  Every call that returns WOBS_OK leaves it zero-filled again (the
- *     last CTA to finish clears what it used), so one zeroing serves any
- *     number of calls.  Calls that overlap on the GPU must not share one
+ *     use.  Every call that returns WOBS_OK leaves it zero-filled again
+ *     (counters and argmax keys are reset by the last arrival, and split-K
+ *     partials are cleared by the warp that adds them up), so one zeroing
+ *     serves any number of calls, whatever their shapes.  Calls that overlap on the GPU must not share one
  *     workspace.  Size 0 means no workspace is needed (ws may be NULL).
  *   - Environment: WOBS_DEBUG=1 logs every dispatch (op, shape, kernel,
  *     grid, split) to stderr; WOBS_SPLITK=<s> overrides the split-K factor

@@ -114,7 +114,7 @@ def test_workspace_size_rules():
 def test_workspace_grows_with_forced_split(monkeypatch):
     lib = _lib.get()
     base = lib.wobs_workspace_size(3, 4, 1000, 4096)
-    monkeypatch.setenv("WOBS_SPLITK", "4")
+    monkeypatch.setenv("WOBS_SPLITK", "8")
     forced = lib.wobs_workspace_size(3, 4, 1000, 4096)
     assert forced >= base + 4 * 4 * 4 * 1000
 

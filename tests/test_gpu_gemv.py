@@ -165,6 +165,64 @@ def test_gemv_q4_0_multi_column(m):
     assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
 
 
+def _q4_unit_scale_case(n, k, m, seed):
+    """Random codes with every scale exactly 1: y is the integer sum of the block dots."""
+    rng = np.random.default_rng(seed)
+    q4 = rng.integers(0, 16, size=(n, k), dtype=np.uint8)
+    q8 = rng.integers(-127, 128, size=(m, k)).astype(np.int8)
+    qs = oracle.pack_q4_0(q4)
+    d4 = np.ones((n, k // 32), np.float16)
+    d8 = np.ones((m, k // 32), np.float16)
+    s8 = q8.reshape(m, k // 32, 32).astype(np.int64).sum(axis=2).astype(np.float16)
+    xq = oracle.pack_q8_1(q8, d8, s8)
+    exact = oracle.q4_0_q8_1_blockdots(qs, q8).sum(axis=2)
+    assert np.abs(exact).max() < 2 ** 24
+    return (to_dev(qs), f16_to_dev(d4), to_dev(xq)), exact
+
+
+@pytest.mark.parametrize("m", [2, 3, 8, 9, 16, 17, 24, 32])
+@pytest.mark.parametrize("n,k", [(16, 256), (37, 1024), (300, 4096), (129, 14336)])
+def test_q4_0_multi_column_block_dots_are_exact(n, k, m):
+    # unit scales make every output an integer below 2^24, so any exact block
+    # dot and any summation order give the same float: equality, not tolerance
+    (qs, d, xq), exact = _q4_unit_scale_case(n, k, m, seed=n * 1000 + m)
+    y, am = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq, want_argmax=True)
+    yn = y.cpu().numpy()
+    assert np.array_equal(yn.astype(np.int64), exact) and np.array_equal(yn, exact.astype(np.float32))
+    assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
+
+
+@pytest.mark.parametrize("m,n,k", [(2, 1, 256), (5, 15, 512), (7, 17, 768), (32, 4100, 4096),
+                                   (12, 1000, 14336), (32, 333, 8192)])
+def test_gemv_q4_0_multi_column_ragged(m, n, k):
+    (qs, d, xq), ref, ad, _ = _q4_case(n, k, m)
+    y, am = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq, want_argmax=True)
+    yn = y.cpu().numpy()
+    assert_within(yn, ref, ad, "f32", f"q4_0 M={m} {n}x{k}")
+    assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
+
+
+def test_q4_0_multi_column_fallbacks_match(monkeypatch, capfd):
+    """K not a multiple of 256, and a scale plane that is only 2-byte aligned,
+    take the CUDA-core kernel; the dispatch log names each kernel."""
+    monkeypatch.setenv("WOBS_DEBUG", "1")
+    (qs, d, xq), exact = _q4_unit_scale_case(70, 2048, 6, seed=11)
+    y1, _ = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq)
+    buf = torch.empty(d.numel() + 8, dtype=torch.float16, device=d.device)
+    d_odd = buf[1:1 + d.numel()].view(d.shape)
+    d_odd.copy_(d)
+    y2, _ = wobs.wobs_gemv_q4_0_q8_1(qs, d_odd, xq)
+    (qs3, d3, xq3), exact3 = _q4_unit_scale_case(70, 2080, 6, seed=12)
+    y3, _ = wobs.wobs_gemv_q4_0_q8_1(qs3, d3, xq3)
+    torch.cuda.synchronize()
+    assert np.array_equal(y1.cpu().numpy(), exact.astype(np.float32))
+    assert np.array_equal(y2.cpu().numpy(), exact.astype(np.float32))
+    assert np.array_equal(y3.cpu().numpy(), exact3.astype(np.float32))
+    err = capfd.readouterr().err
+    kernels = [ln.split("kernel=")[1].split()[0] for ln in err.splitlines() if ln.startswith("wobs: op=")]
+    assert kernels == ["q4_0_q8_1_mma", "q4_0_q8_1_mn", "q4_0_q8_1_mn"], kernels
+
+
 @pytest.mark.parametrize("splits", ["2", "5", "64"])
 def test_gemv_q4_0_forced_split_k(monkeypatch, splits):
     monkeypatch.setenv("WOBS_SPLITK", splits)

@@ -49,7 +49,7 @@ void log_dispatch(const char* op, int M, int N, int K, const wobs::Launch& L, in
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-constexpr int kRowsPerGroup = 128;   // smallest row group of the multi-column kernels
+constexpr int kRowsPerGroup = 16;    // smallest row group of the multi-column kernels
 
 struct WsLayout {
   size_t counter = 0, keys = 0, groups = 0, partials = 0, total = 0;
@@ -70,7 +70,14 @@ WsLayout ws_layout(int op, int M, int N, int K) {
   off += 4 * static_cast<size_t>(L.ngroups);
   off = (off + 255) & ~static_cast<size_t>(255);
   L.partials = off;
-  if (L.splits > 1) off += 4ull * L.splits * M * N;
+  if (L.splits > 1) {
+    size_t pb = 4ull * L.splits * M * N;
+    if (op == WOBS_OP_GEMV_Q4_0_Q8_1 && M >= 2 && K % 256 == 0) {
+      const size_t tb = wobs::q4_mma_partial_bytes(M, N, K, env_splits());
+      if (tb > pb) pb = tb;
+    }
+    off += pb;
+  }
   L.total = off;
   return L;
 }
@@ -147,6 +154,8 @@ int max_resident_ctas(const void* kernel, int block, int smem) {
   return n;
 }
 
+int forced_splits() { return env_splits(); }
+
 bool m1_ldg_forced() {
   const char* v = std::getenv("WOBS_M1");
   return v && std::strcmp(v, "ldg") == 0;
@@ -154,7 +163,9 @@ bool m1_ldg_forced() {
 
 int choose_splits(int op, int M, int N, int K) {
   const int forced = env_splits();
-  const int groups = (N + kRowsPerGroup - 1) / kRowsPerGroup;
+  // row groups of 128 for the split heuristics (the counters themselves are
+  // sized per kRowsPerGroup rows)
+  const int groups = (N + 127) / 128;
   const int target = 2 * device_sm_count();
   switch (op) {
     case WOBS_OP_GEMV_F16:
@@ -169,15 +180,23 @@ int choose_splits(int op, int M, int N, int K) {
     }
     case WOBS_OP_GEMV_Q4_0_Q8_1: {
       const int nb = K / 32 > 0 ? K / 32 : 1;
-      // shared-memory bound of the multi-column kernel: 48 bytes per block
-      // per padded column, at most 144 KB
+      if (M == 1 && !forced) return 1;
+      int s;
+      if (M == 1) return forced < nb ? forced : nb;
+      if (K % 256 == 0) {
+        // tensor-core kernel (its own plan); the CUDA-core fallback, taken
+        // for a misaligned scale plane, accepts any split
+        const int sm = q4_mma_splits(M, N, K, forced);
+        s = forced ? (forced < nb ? forced : nb) : sm;
+        return s > sm ? s : sm;
+      }
+      // CUDA-core kernel: 48 bytes of shared memory per block per padded
+      // column, at most 144 KB
       int nc = 1;
       while (nc < M) nc = nc < 8 ? nc * 2 : (nc == 8 ? 12 : (nc == 12 ? 16 : (nc == 16 ? 24 : 32)));
       const int bps_max = (144 * 1024) / (48 * nc);
       const int smin = (nb + bps_max - 1) / bps_max;
-      int s;
       if (forced) s = forced < nb ? forced : nb;
-      else if (M == 1) return 1;
       else {
         s = (target + groups - 1) / groups;
         const int cap = nb / 4 > 0 ? nb / 4 : 1;

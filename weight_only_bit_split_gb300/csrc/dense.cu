@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kMThreads, 1) dense_mma_kernel(const T* __rest
             float acc = 0.f;
             if (col < M && row < N)
               for (int sp = 0; sp < sk.splits; ++sp)
-                acc += __ldcg(sk.partials + (static_cast<int64_t>(sp) * M + col) * N + row);
+                acc += take_partial(sk.partials + (static_cast<int64_t>(sp) * M + col) * N + row);
             d[n][h] = acc;
           }
       }

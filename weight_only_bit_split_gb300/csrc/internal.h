@@ -54,6 +54,17 @@ cudaError_t launch_quantize_nf4(const void* W, int64_t ldw, int N, int K, const 
 cudaError_t launch_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* xq, int M,
                                   float* Y, int N, int K, const SplitArgs& sk,
                                   const ArgmaxArgs& am, cudaStream_t st, Launch* info);
+// Multi-column (M >= 2) tensor-core kernel; K % 256 == 0 and a 16-byte
+// aligned scale plane.  q4_mma_splits gives the K split it launches with
+// (forced > 0: the WOBS_SPLITK override), which sizes the workspace.
+cudaError_t launch_q4_mma(const uint8_t* qs, const void* d, const void* xq, int M, float* Y, int N,
+                          int K, int forced, const SplitArgs& sk, const ArgmaxArgs& am,
+                          cudaStream_t st, Launch* info);
+int q4_mma_splits(int M, int N, int K, int forced);
+// Split-K partial bytes of its launch (fragment-ordered, padded columns).
+size_t q4_mma_partial_bytes(int M, int N, int K, int forced);
+// WOBS_SPLITK, or 0 when unset.
+int forced_splits();
 cudaError_t launch_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, int N, int K,
                                        int32_t* out, cudaStream_t st, Launch* info);
 

@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kThreads) q4_mn_kernel(const uint8_t* __restri
         float t = 0.f;
         if (m < M)
           for (int j = 0; j < sk.splits; ++j)
-            t += __ldcg(sk.partials + (static_cast<int64_t>(j) * M + m) * N + row);
+            t += take_partial(sk.partials + (static_cast<int64_t>(j) * M + m) * N + row);
         acc[m] = t;
       }
     }
@@ -524,13 +524,15 @@ cudaError_t launch_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* 
                                   float* Y, int N, int K, const SplitArgs& sk,
                                   const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   if (M == 1 && sk.splits <= 1) {
-    
     // 16-byte asynchronous copies need 16-byte aligned scale segments
     const bool cp_ok = (K % 256 == 0) && (reinterpret_cast<uintptr_t>(d) % 16 == 0) &&
                        (kRingBytes + (K / 32) * 40 <= 200 * 1024);
     if (cp_ok && !m1_ldg_forced()) return run_m1_cp(qs, d, xq, Y, N, K, am, st, info);
     return run_m1(qs, d, xq, Y, N, K, am, st, info);
   }
+  // tensor-core path: whole 8-block stages and 16-byte scale copies
+  if (M >= 2 && K % 256 == 0 && reinterpret_cast<uintptr_t>(d) % 16 == 0)
+    return launch_q4_mma(qs, d, xq, M, Y, N, K, forced_splits(), sk, am, st, info);
   if (M <= 1) return run_mn<1>(qs, d, xq, M, Y, N, K, sk, am, st, info);
   if (M <= 2) return run_mn<2>(qs, d, xq, M, Y, N, K, sk, am, st, info);
   if (M <= 4) return run_mn<4>(qs, d, xq, M, Y, N, K, sk, am, st, info);
