@@ -405,7 +405,7 @@ class Q4Sweep(Q4M1):
     name = "q4_0_q8_1_m_sweep"
     shapes = [(4096, 4096), (14336, 4096)]
     Ms = (1, 2, 4, 8, 12, 16, 24, 32)
-    kernel = "q4_0_q8_1 (m1 / mn)"
+    kernel = "q4_0_q8_1 (m1_cp / mc_cp / mma)"
     workload_id = 4
 
     def __init__(self, device):

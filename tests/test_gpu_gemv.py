@@ -202,25 +202,31 @@ def test_gemv_q4_0_multi_column_ragged(m, n, k):
     assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
 
 
-def test_q4_0_multi_column_fallbacks_match(monkeypatch, capfd):
-    """K not a multiple of 256, and a scale plane that is only 2-byte aligned,
-    take the CUDA-core kernel; the dispatch log names each kernel."""
+def test_q4_0_multi_column_paths_agree_exactly(monkeypatch, capfd):
+    """Every multi-column kernel gives the exact integer answer on unit-scale
+    inputs: the few-column whole-row kernel (M <= 8), the tensor-core kernel,
+    and the CUDA-core fallback (K not a multiple of 256, or a scale plane
+    that is only 2-byte aligned); the dispatch log names each kernel."""
     monkeypatch.setenv("WOBS_DEBUG", "1")
-    (qs, d, xq), exact = _q4_unit_scale_case(70, 2048, 6, seed=11)
-    y1, _ = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq)
-    buf = torch.empty(d.numel() + 8, dtype=torch.float16, device=d.device)
-    d_odd = buf[1:1 + d.numel()].view(d.shape)
-    d_odd.copy_(d)
-    y2, _ = wobs.wobs_gemv_q4_0_q8_1(qs, d_odd, xq)
-    (qs3, d3, xq3), exact3 = _q4_unit_scale_case(70, 2080, 6, seed=12)
-    y3, _ = wobs.wobs_gemv_q4_0_q8_1(qs3, d3, xq3)
-    torch.cuda.synchronize()
-    assert np.array_equal(y1.cpu().numpy(), exact.astype(np.float32))
-    assert np.array_equal(y2.cpu().numpy(), exact.astype(np.float32))
-    assert np.array_equal(y3.cpu().numpy(), exact3.astype(np.float32))
+    expect = []
+    for m, k, odd, kern in [(4, 2048, False, "q4_0_q8_1_mc_cp"), (2, 4096, False, "q4_0_q8_1_mc_cp"),
+                            (3, 4096, False, "q4_0_q8_1_mc_cp"), (12, 2048, False, "q4_0_q8_1_mma"),
+                            (6, 2048, False, "q4_0_q8_1_mma"),
+                            (6, 2048, True, "q4_0_q8_1_mn"), (6, 2080, False, "q4_0_q8_1_mn")]:
+        (qs, d, xq), exact = _q4_unit_scale_case(70, k, m, seed=m * 31 + k)
+        if odd:
+            buf = torch.empty(d.numel() + 8, dtype=torch.float16, device=d.device)
+            d_odd = buf[1:1 + d.numel()].view(d.shape)
+            d_odd.copy_(d)
+            d = d_odd
+        y, am = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq, want_argmax=True)
+        yn = y.cpu().numpy()
+        assert np.array_equal(yn, exact.astype(np.float32)), kern
+        assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn)), kern
+        expect.append(kern)
     err = capfd.readouterr().err
     kernels = [ln.split("kernel=")[1].split()[0] for ln in err.splitlines() if ln.startswith("wobs: op=")]
-    assert kernels == ["q4_0_q8_1_mma", "q4_0_q8_1_mn", "q4_0_q8_1_mn"], kernels
+    assert kernels == expect, kernels
 
 
 @pytest.mark.parametrize("splits", ["2", "5", "64"])

@@ -183,6 +183,7 @@ int choose_splits(int op, int M, int N, int K) {
       if (M == 1 && !forced) return 1;
       int s;
       if (M == 1) return forced < nb ? forced : nb;
+      if (!forced && q4_mc_applies(M, K)) return 1;
       if (K % 256 == 0) {
         // tensor-core kernel (its own plan); the CUDA-core fallback, taken
         // for a misaligned scale plane, accepts any split

@@ -63,6 +63,8 @@ cudaError_t launch_q4_mma(const uint8_t* qs, const void* d, const void* xq, int 
 int q4_mma_splits(int M, int N, int K, int forced);
 // Split-K partial bytes of its launch (fragment-ordered, padded columns).
 size_t q4_mma_partial_bytes(int M, int N, int K, int forced);
+// The few-column (2..8) whole-row kernel applies (it needs no K split).
+bool q4_mc_applies(int M, int K);
 // WOBS_SPLITK, or 0 when unset.
 int forced_splits();
 cudaError_t launch_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, int N, int K,

@@ -352,6 +352,186 @@ cudaError_t run_m1_cp(const uint8_t* qs, const void* d, const void* xq, float* y
                 : run_m1_cp_t<false>(qs, d, xq, y, N, K, am, st, info);
 }
 
+// ------------------------------------- 2..8 columns, cp.async staging
+
+// The M = 1 structure (warp per row, lanes along K, per-warp cp.async ring,
+// whole rows so no K split) for a few activation columns: each weight block
+// is unpacked once and dotted with MC columns.  The activation planes
+// ([MC][nb] each) stay in shared memory; columns past M are zero.
+template <int MC>
+struct McShape {
+  static constexpr int kWarps = MC >= 8 ? 12 : 16;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kRingBytes = kWarps * kRing * kSegBytes;
+};
+
+template <int MC, bool kArgmax>
+__global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc_cp_kernel(
+    const uint8_t* __restrict__ qs, const uint16_t* __restrict__ d4, const uint8_t* __restrict__ xq,
+    int M, float* __restrict__ Y, int N, int K, ArgmaxArgs am) {
+  constexpr int W = McShape<MC>::kWarps;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int nb = K >> 5;
+  const int kh = K >> 1;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int total_warps = gridDim.x * W;
+  const int wg = blockIdx.x * W + warp;
+  const int nseg = (nb + kSegBlocks - 1) / kSegBlocks;
+  const int rows_w = wg < N ? (N - 1 - wg) / total_warps + 1 : 0;
+  const int T = rows_w * nseg;
+  uint8_t* myring = smem + warp * (kRing * kSegBytes);
+  int4* x_lo = reinterpret_cast<int4*>(smem + McShape<MC>::kRingBytes);   // [MC][nb]
+  int4* x_hi = x_lo + MC * nb;
+  float2* x_ds = reinterpret_cast<float2*>(x_hi + MC * nb);               // (d, exact sum)
+
+  int prow = wg, pseg = 0;
+  auto issue = [&](int slot) {
+    uint8_t* st = myring + slot * kSegBytes;
+    const int b0 = pseg * kSegBlocks;
+    const int n = min(kSegBlocks, nb - b0);
+    const uint8_t* qr = qs + static_cast<int64_t>(prow) * kh + b0 * 16;
+#pragma unroll
+    for (int u = 0; u < kSegBlocks / 32; ++u) {
+      const int bl = 32 * u + lane;
+      if (bl < n) cp_async16(st + 16 * bl, qr + 16 * bl);
+    }
+    const uint8_t* dr = reinterpret_cast<const uint8_t*>(d4 + static_cast<int64_t>(prow) * nb + b0);
+    if (lane < n / 8) cp_async16(st + kSegQs + 16 * lane, dr + 16 * lane);
+    if (++pseg == nseg) { pseg = 0; prow += total_warps; }
+  };
+#pragma unroll
+  for (int i = 0; i < kRing - 1; ++i) {
+    if (i < T) issue(i);
+    cp_async_commit();
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  for (int i = threadIdx.x; i < MC * nb; i += W * 32) {
+    const int m = i / nb, b = i - m * nb;
+    if (m < M) {
+      const XBlock xb = load_xblock(xq + 36 * (static_cast<int64_t>(m) * nb + b));
+      x_lo[i] = xb.lo;
+      x_hi[i] = xb.hi;
+      x_ds[i] = make_float2(xb.d, __int_as_float(xb.s));
+    } else {
+      x_lo[i] = make_int4(0, 0, 0, 0);
+      x_hi[i] = make_int4(0, 0, 0, 0);
+      x_ds[i] = make_float2(0.f, __int_as_float(0));
+    }
+  }
+  __syncthreads();
+
+  int crow = wg, cseg = 0;
+  float acc[MC];
+#pragma unroll
+  for (int m = 0; m < MC; ++m) acc[m] = 0.f;
+  uint64_t best[MC];
+#pragma unroll
+  for (int m = 0; m < MC; ++m) best[m] = 0ull;
+  for (int t = 0; t < T; ++t) {
+    if (t + kRing - 1 < T) issue((t + kRing - 1) % kRing);
+    cp_async_commit();
+    cp_async_wait<kRing - 1>();
+    __syncwarp();
+    const uint8_t* st = myring + (t % kRing) * kSegBytes;
+    const int b0 = cseg * kSegBlocks;
+    const int n = min(kSegBlocks, nb - b0);
+#pragma unroll
+    for (int u = 0; u < kSegBlocks / 32; ++u) {
+      const int bl = 32 * u + lane;
+      if (bl < n) {
+        const uint4 q = *reinterpret_cast<const uint4*>(st + 16 * bl);
+        const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t*>(st + kSegQs + 2 * bl));
+        const int b = b0 + bl;
+        const int lo0 = static_cast<int>(q.x & 0x0F0F0F0Fu), lo1 = static_cast<int>(q.y & 0x0F0F0F0Fu);
+        const int lo2 = static_cast<int>(q.z & 0x0F0F0F0Fu), lo3 = static_cast<int>(q.w & 0x0F0F0F0Fu);
+        const int hi0 = static_cast<int>((q.x >> 4) & 0x0F0F0F0Fu), hi1 = static_cast<int>((q.y >> 4) & 0x0F0F0F0Fu);
+        const int hi2 = static_cast<int>((q.z >> 4) & 0x0F0F0F0Fu), hi3 = static_cast<int>((q.w >> 4) & 0x0F0F0F0Fu);
+#pragma unroll
+        for (int m = 0; m < MC; ++m) {
+          const int4 xl = x_lo[m * nb + b], xh = x_hi[m * nb + b];
+          const float2 ds = x_ds[m * nb + b];
+          int sdot = -8 * __float_as_int(ds.y);
+          sdot = __dp4a(lo0, xl.x, sdot); sdot = __dp4a(lo1, xl.y, sdot);
+          sdot = __dp4a(lo2, xl.z, sdot); sdot = __dp4a(lo3, xl.w, sdot);
+          sdot = __dp4a(hi0, xh.x, sdot); sdot = __dp4a(hi1, xh.y, sdot);
+          sdot = __dp4a(hi2, xh.z, sdot); sdot = __dp4a(hi3, xh.w, sdot);
+          acc[m] = fmaf(static_cast<float>(sdot), dw * ds.x, acc[m]);
+        }
+      }
+    }
+    if (cseg == nseg - 1) {
+#pragma unroll
+      for (int m = 0; m < MC; ++m) {
+        const float sum = warp_sum(acc[m]);
+        if (m < M) {
+          if (lane == m) Y[static_cast<int64_t>(m) * N + crow] = sum;
+          if (kArgmax) {
+            const uint64_t k = argmax_key(sum, static_cast<uint32_t>(crow));
+            best[m] = k > best[m] ? k : best[m];
+          }
+        }
+        acc[m] = 0.f;
+      }
+    }
+    if (++cseg == nseg) { cseg = 0; crow += total_warps; }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  if (kArgmax) {
+    __shared__ uint64_t s_best[W][MC];
+    __shared__ uint64_t s_cta[MC];
+    if (lane == 0) {
+#pragma unroll
+      for (int m = 0; m < MC; ++m) s_best[warp][m] = best[m];
+    }
+    __syncthreads();
+    if (threadIdx.x < MC) {
+      uint64_t bk = 0;
+      for (int i = 0; i < W; ++i) bk = s_best[i][threadIdx.x] > bk ? s_best[i][threadIdx.x] : bk;
+      s_cta[threadIdx.x] = bk;
+    }
+    __syncthreads();
+    argmax_publish(s_cta, M, am, gridDim.x);
+  }
+}
+
+template <int MC>
+int mc_smem(int K) {
+  return McShape<MC>::kRingBytes + MC * (K / 32) * 40;
+}
+
+template <int MC, bool kArgmax>
+cudaError_t run_mc_t(const uint8_t* qs, const void* d, const void* xq, int M, float* y, int N,
+                     int K, const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
+  constexpr int W = McShape<MC>::kWarps;
+  const int smem = mc_smem<MC>(K);
+  auto kern = q4_mc_cp_kernel<MC, kArgmax>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int per_sm = max_resident_ctas(reinterpret_cast<const void*>(kern), W * 32, smem);
+  int grid = device_sm_count() * (per_sm > 0 ? per_sm : 1);
+  const int need = (N + W - 1) / W;
+  if (grid > need) grid = need;
+  info->grid_x = grid;
+  info->block = W * 32;
+  info->smem = smem;
+  info->kernel = "q4_0_q8_1_mc_cp";
+  return launch_k(kern, dim3(grid), dim3(W * 32), smem, st, true, qs,
+                  static_cast<const uint16_t*>(d), static_cast<const uint8_t*>(xq), M, y, N, K, am);
+}
+
+template <int MC>
+cudaError_t run_mc(const uint8_t* qs, const void* d, const void* xq, int M, float* y, int N, int K,
+                   const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
+  return am.out ? run_mc_t<MC, true>(qs, d, xq, M, y, N, K, am, st, info)
+                : run_mc_t<MC, false>(qs, d, xq, M, y, N, K, am, st, info);
+}
+
+// Two CTAs of the few-column kernel fit on an SM with this much shared memory each.
+constexpr int kMcSmemMax = 110 * 1024;
+
 // --------------------------------------------------------- M columns
 
 struct __align__(16) XS {
@@ -520,6 +700,12 @@ __global__ void __launch_bounds__(kThreads) q4_blockdots_kernel(const uint8_t* _
 
 }  // namespace
 
+bool q4_mc_applies(int M, int K) {
+  if (M < 2 || M > 4 || K % 256 != 0) return false;
+  const int smem = M == 2 ? mc_smem<2>(K) : mc_smem<4>(K);
+  return smem <= kMcSmemMax;
+}
+
 cudaError_t launch_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* xq, int M,
                                   float* Y, int N, int K, const SplitArgs& sk,
                                   const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
@@ -530,8 +716,14 @@ cudaError_t launch_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* 
     if (cp_ok && !m1_ldg_forced()) return run_m1_cp(qs, d, xq, Y, N, K, am, st, info);
     return run_m1(qs, d, xq, Y, N, K, am, st, info);
   }
+  const bool cp_shape = K % 256 == 0 && reinterpret_cast<uintptr_t>(d) % 16 == 0;
+  // a few columns: whole rows per warp, no K split
+  if (cp_shape && sk.splits <= 1 && q4_mc_applies(M, K)) {
+    if (M == 2) return run_mc<2>(qs, d, xq, M, Y, N, K, am, st, info);
+    return run_mc<4>(qs, d, xq, M, Y, N, K, am, st, info);
+  }
   // tensor-core path: whole 8-block stages and 16-byte scale copies
-  if (M >= 2 && K % 256 == 0 && reinterpret_cast<uintptr_t>(d) % 16 == 0)
+  if (M >= 2 && cp_shape)
     return launch_q4_mma(qs, d, xq, M, Y, N, K, forced_splits(), sk, am, st, info);
   if (M <= 1) return run_mn<1>(qs, d, xq, M, Y, N, K, sk, am, st, info);
   if (M <= 2) return run_mn<2>(qs, d, xq, M, Y, N, K, sk, am, st, info);

@@ -341,43 +341,65 @@ __global__ void __launch_bounds__(kQThreads, NT == 1 ? 2 : 1) q4_mma_kernel(cons
   cp_async_wait_group<0>();
 
   if (sk.splits > 1 && my_groups > 0) {
-    // arrivals after all of this warp's partials: one fence, no stall inside
-    // the streaming loop; the last split of a group adds all partials in
-    // split order
+    // Arrivals after all of this warp's partials (no fence inside the
+    // streaming loop): every lane arrives for one of the warp's groups at
+    // once, then the warp adds up the groups it completed, all splits of a
+    // group loaded together where registers allow, in split order.
     __threadfence();
-    for (int grp = gr0 + warp; grp < gr1; grp += kQW) {
-      if (!splitk_arrive_last_warp(sk.counters, grp, sk.splits)) continue;
-      // all of one split's fragments are loaded together; splits are added
-      // in order, then their slots are cleared
-      for (int sp = 0; sp < sk.splits; ++sp) {
-        const float4* pp = reinterpret_cast<const float4*>(sk.partials) +
-                           (static_cast<int64_t>(sp) * ngr + grp) * (R * NT * 32) + lane;
-        float4 v[R][NT];
+    __syncwarp();
+    for (int base = 0; base < my_groups; base += 32) {
+      const int gi = base + lane;
+      bool last = false;
+      if (gi < my_groups) {
+        const int grp = gr0 + warp + gi * kQW;
+        const unsigned prev = atomicAdd(sk.counters + grp, 1u);
+        last = prev == static_cast<unsigned>(sk.splits) - 1u;
+        if (last) sk.counters[grp] = 0u;
+      }
+      unsigned mask = __ballot_sync(0xffffffffu, last);
+      if (mask) __threadfence();
+      while (mask) {
+        const int gi2 = base + __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int grp = gr0 + warp + gi2 * kQW;
+        constexpr int kB = (16 / (R * NT)) > 0 ? 16 / (R * NT) : 1;
+        for (int sp0 = 0; sp0 < sk.splits; sp0 += kB) {
+          float4 v[kB][R][NT];
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+          for (int b = 0; b < kB; ++b) {
+            const int sp = sp0 + b;
+            const float4* pp = reinterpret_cast<const float4*>(sk.partials) +
+                               (static_cast<int64_t>(sp < sk.splits ? sp : 0) * ngr + grp) * (R * NT * 32) + lane;
 #pragma unroll
-          for (int n = 0; n < NT; ++n) v[r][n] = __ldcg(pp + (r * NT + n) * 32);
+            for (int r = 0; r < R; ++r)
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            acc[r][n][0] += v[r][n].x; acc[r][n][1] += v[r][n].y;
-            acc[r][n][2] += v[r][n].z; acc[r][n][3] += v[r][n].w;
+              for (int n = 0; n < NT; ++n)
+                v[b][r][n] = sp < sk.splits ? __ldcg(pp + (r * NT + n) * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-      }
-      for (int sp = 0; sp < sk.splits; ++sp) {
-        float4* pp = reinterpret_cast<float4*>(sk.partials) +
-                     (static_cast<int64_t>(sp) * ngr + grp) * (R * NT * 32) + lane;
+#pragma unroll
+          for (int b = 0; b < kB; ++b)
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+              for (int n = 0; n < NT; ++n) {
+                acc[r][n][0] += v[b][r][n].x; acc[r][n][1] += v[b][r][n].y;
+                acc[r][n][2] += v[b][r][n].z; acc[r][n][3] += v[b][r][n].w;
+              }
+        }
+        for (int sp = 0; sp < sk.splits; ++sp) {
+          float4* pp = reinterpret_cast<float4*>(sk.partials) +
+                       (static_cast<int64_t>(sp) * ngr + grp) * (R * NT * 32) + lane;
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int n = 0; n < NT; ++n) __stcg(pp + (r * NT + n) * 32, make_float4(0.f, 0.f, 0.f, 0.f));
+        }
+        emit(grp, acc);
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
-          for (int n = 0; n < NT; ++n) __stcg(pp + (r * NT + n) * 32, make_float4(0.f, 0.f, 0.f, 0.f));
+          for (int n = 0; n < NT; ++n) acc[r][n][0] = acc[r][n][1] = acc[r][n][2] = acc[r][n][3] = 0.f;
       }
-      emit(grp, acc);
-#pragma unroll
-      for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int n = 0; n < NT; ++n) acc[r][n][0] = acc[r][n][1] = acc[r][n][2] = acc[r][n][3] = 0.f;
     }
   }
 
