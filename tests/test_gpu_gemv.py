@@ -288,13 +288,25 @@ def _nf4_case(n, k, copy=0):
 
 
 @pytest.mark.parametrize("n,k", [(1, 64), (31, 1024), (100, 8192), (33, 1088), (257, 4096),
-                                 (70, 16384)])
-def test_gemv_nf4(n, k):
+                                 (70, 16384), (95, 2048), (1000, 8192)])
+def test_gemv_nf4(n, k, m1_path):
     cb, qs, am, x, ref, ad = _nf4_case(n, k)
     y, idx = wobs.wobs_gemv_nf4(qs, am, cb, x, want_argmax=True)
     yf = y.float().cpu().numpy()
     assert_within(yf, ref, ad, "bf16", f"nf4 {n}x{k}")
     assert int(idx.item()) == int(oracle.argmax_rows(yf)[0])
+
+
+def test_nf4_dispatch_coverage(monkeypatch, capfd):
+    monkeypatch.setenv("WOBS_DEBUG", "1")
+    monkeypatch.delenv("WOBS_M1", raising=False)
+    for k in (8192, 1088):
+        cb, qs, am, x, _, _ = _nf4_case(40, k)
+        wobs.wobs_gemv_nf4(qs, am, cb, x)
+    torch.cuda.synchronize()
+    err = capfd.readouterr().err
+    kernels = [ln.split("kernel=")[1].split()[0] for ln in err.splitlines() if ln.startswith("wobs: op=")]
+    assert kernels == ["nf4_m1_cp", "nf4_m1"], kernels
 
 
 def test_gemv_nf4_deterministic():

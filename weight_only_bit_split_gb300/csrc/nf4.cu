@@ -174,6 +174,200 @@ __global__ void __launch_bounds__(kThreads, 2) nf4_m1_kernel(const uint8_t* __re
   }
 }
 
+// ----------------------------------------------- cp.async staged variant
+//
+// Same decomposition (a warp owns a 1024-element K slice and keeps its 32
+// activations per lane in registers; rows in batches of 32), with the code
+// and scale stream staged through a per-warp ring of shared-memory stages
+// by 16-byte asynchronous copies, requested one stage ahead and, for the
+// first stage, before the programmatic-launch wait.  A stage holds 8 rows of
+// the warp's slice: 8 x 512 bytes of codes and 8 x 64 bytes of block scales.
+// When K has fewer than 8 slices, the CTA runs 8 / slices batches side by
+// side (one group of warps each, synchronised by its own named barrier).
+constexpr int kCpRows = 8;                      // rows per stage
+constexpr int kCpStage = kCpRows * 512 + kCpRows * 64;
+constexpr int kCpRing = 2;
+
+__device__ __forceinline__ void group_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void cp_async16_nf4(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+               :: "r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))), "l"(src),
+                  "r"(valid ? 16 : 0) : "memory");
+}
+
+template <bool kArgmax>
+__global__ void __launch_bounds__(kThreads, 2) nf4_m1_cp_kernel(const uint8_t* __restrict__ qs,
+                                                                const float* __restrict__ absmax,
+                                                                Codebook16 cb,
+                                                                const __nv_bfloat16* __restrict__ x,
+                                                                __nv_bfloat16* __restrict__ y,
+                                                                int N, int K, ArgmaxArgs am) {
+  extern __shared__ __align__(16) float smem_f[];
+  float2* lut = reinterpret_cast<float2*>(smem_f);                                   // [256][16]
+  uint8_t* rings = reinterpret_cast<uint8_t*>(smem_f + 2 * 256 * kLutCopies);         // [warps][ring][stage]
+  __shared__ float red[kWarps][kBatch];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nsl = K >> 10;                 // 1, 2, 4 or 8 slices
+  const int groups = kWarps / nsl;         // batches processed side by side
+  const int grp = warp / nsl, sl = warp - grp * nsl;
+  const int kh = K >> 1;
+  const int nab = K >> 6;
+  const int nbatch = (N + kBatch - 1) / kBatch;
+  const int bstride = gridDim.x * groups;
+  const int bfirst = blockIdx.x * groups + grp;
+  const int my_batches = bfirst < nbatch ? (nbatch - 1 - bfirst) / bstride + 1 : 0;
+  constexpr int kOct = kBatch / kCpRows;   // stages per batch
+  const int T = my_batches * kOct;
+  uint8_t* ring = rings + warp * (kCpRing * kCpStage);
+
+  int pb = bfirst, po = 0;                 // next stage: batch, row octet
+  auto issue = [&](int slot) {
+    uint8_t* st = ring + slot * kCpStage;
+    const int row0 = pb * kBatch + po * kCpRows;
+#pragma unroll
+    for (int r = 0; r < kCpRows; ++r) {
+      const int row = min(row0 + r, N - 1);
+      cp_async16_nf4(st + r * 512 + 16 * lane, qs + static_cast<int64_t>(row) * kh + sl * 512 + 16 * lane, true);
+    }
+    {
+      const int r = lane >> 2, q = lane & 3;
+      const int row = min(row0 + r, N - 1);
+      cp_async16_nf4(st + kCpRows * 512 + r * 64 + 16 * q,
+                     absmax + static_cast<int64_t>(row) * nab + sl * 16 + 4 * q, true);
+    }
+    if (++po == kOct) { po = 0; pb += bstride; }
+  };
+  if (T > 0) issue(0);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+
+  for (int i = threadIdx.x; i < 256 * kLutCopies; i += kThreads) {
+    const int e = i / kLutCopies;
+    lut[i] = make_float2(cb.v[e >> 4], cb.v[e & 15]);
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  // this lane's 32 activations: element sl*1024 + lane*32 + 4*j + t -> xr[2j], xr[2j+1]
+  float2 xr[16];
+  {
+    const uint4* xp = reinterpret_cast<const uint4*>(x + sl * 1024 + lane * 32);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint4 v = __ldg(xp + h);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xr[4 * h + i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+    }
+  }
+  __syncthreads();                         // the codebook table is complete
+
+  // byte offset of (code pair e, this lane's replica) in the table: e*128 + replica*8
+  const uint32_t lut_s = static_cast<uint32_t>(__cvta_generic_to_shared(lut));
+  const uint32_t rep8 = static_cast<uint32_t>(lane & (kLutCopies - 1)) * 8u;
+  uint64_t best = 0;
+  int cbt = bfirst;                        // batch being consumed
+  for (int t = 0; t < T; t += kOct, cbt += bstride) {
+    float p[kBatch];
+#pragma unroll
+    for (int r = 0; r < kBatch; ++r) p[r] = 0.f;
+#pragma unroll
+    for (int o = 0; o < kOct; ++o) {
+      if (t + o + 1 < T) issue((t + o + 1) % kCpRing);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      __syncwarp();
+      const uint8_t* st = ring + (o % kCpRing) * kCpStage;   // t is a multiple of kOct (even)
+#pragma unroll
+      for (int r = 0; r < kCpRows; ++r) {
+        const uint4 q = *reinterpret_cast<const uint4*>(st + r * 512 + 16 * lane);
+        const float a = *reinterpret_cast<const float*>(st + kCpRows * 512 + r * 64 + 4 * (lane >> 1));
+        float2 acc = make_float2(0.f, 0.f);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t off = (j == 0 ? (w[i] << 7) : (w[i] >> (8 * j - 7))) & 0x7F80u;
+            float2 v;
+            asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(lut_s + (off | rep8)));
+            acc = ffma2(v, xr[4 * i + j], acc);
+          }
+        }
+        p[o * kCpRows + r] = a * (acc.x + acc.y);
+      }
+      __syncwarp();
+    }
+    // batch complete: reduce-scatter, then combine the group's slices
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < off; ++i) {
+        const float send = upper ? p[i] : p[i + off];
+        const float keep = upper ? p[i + off] : p[i];
+        p[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    }
+    red[warp][lane] = p[0];
+    group_barrier(1 + grp, nsl * 32);
+    if (sl == 0) {
+      float tot = 0.f;
+      for (int w2 = 0; w2 < nsl; ++w2) tot += red[grp * nsl + w2][lane];
+      const int row = cbt * kBatch + lane;
+      if (row < N) {
+        const __nv_bfloat16 o = __float2bfloat16_rn(tot);
+        y[row] = o;
+        if (kArgmax) {
+          const uint64_t k = argmax_key(__bfloat162float(o), static_cast<uint32_t>(row));
+          best = k > best ? k : best;
+        }
+      }
+    }
+    group_barrier(1 + grp, nsl * 32);
+  }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  if (kArgmax) {
+    __shared__ uint64_t s_g[kWarps];
+    __shared__ uint64_t s_cta[1];
+    if (sl == 0) {
+      const uint64_t b = warp_max_u64(best);
+      if (lane == 0) s_g[grp] = b;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint64_t bk = 0;
+      for (int i = 0; i < groups; ++i) bk = s_g[i] > bk ? s_g[i] : bk;
+      s_cta[0] = bk;
+    }
+    __syncthreads();
+    argmax_publish(s_cta, 1, am, gridDim.x);
+  }
+}
+
+template <bool kArgmax>
+cudaError_t run_cp(const uint8_t* qs, const float* absmax, const Codebook16& cb, const void* x,
+                   void* y, int N, int K, const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
+  const int smem = 2 * 256 * kLutCopies * static_cast<int>(sizeof(float)) + kWarps * kCpRing * kCpStage;
+  cudaError_t e = cudaFuncSetAttribute(nf4_m1_cp_kernel<kArgmax>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int per_sm = max_resident_ctas(reinterpret_cast<const void*>(nf4_m1_cp_kernel<kArgmax>),
+                                       kThreads, smem);
+  const int groups = kWarps / (K / 1024);
+  int grid = device_sm_count() * (per_sm > 0 ? per_sm : 1);
+  const int need = ((N + kBatch - 1) / kBatch + groups - 1) / groups;
+  if (grid > need) grid = need;
+  info->grid_x = grid;
+  info->block = kThreads;
+  info->smem = smem;
+  info->kernel = "nf4_m1_cp";
+  return launch_k(nf4_m1_cp_kernel<kArgmax>, dim3(grid), dim3(kThreads), smem, st, true, qs, absmax,
+                  cb, static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, K,
+                  am);
+}
+
 template <bool kArgmax>
 cudaError_t run(const uint8_t* qs, const float* absmax, const Codebook16& cb, const void* x,
                 void* y, int N, int K, const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
@@ -201,6 +395,13 @@ cudaError_t run(const uint8_t* qs, const float* absmax, const Codebook16& cb, co
 cudaError_t launch_gemv_nf4(const uint8_t* qs, const float* absmax, const Codebook16& cb,
                             const void* x, void* y, int N, int K, const ArgmaxArgs& am,
                             cudaStream_t st, Launch* info) {
+  // staged variant: K of 1, 2, 4 or 8 whole 1024-element slices, 16-byte
+  // aligned scale rows and activations
+  const bool cp = (K == 1024 || K == 2048 || K == 4096 || K == 8192) &&
+                  reinterpret_cast<uintptr_t>(absmax) % 16 == 0 &&
+                  reinterpret_cast<uintptr_t>(x) % 16 == 0 && !m1_ldg_forced();
+  if (cp) return am.out ? run_cp<true>(qs, absmax, cb, x, y, N, K, am, st, info)
+                        : run_cp<false>(qs, absmax, cb, x, y, N, K, am, st, info);
   if (am.out) return run<true>(qs, absmax, cb, x, y, N, K, am, st, info);
   return run<false>(qs, absmax, cb, x, y, N, K, am, st, info);
 }
