@@ -72,6 +72,12 @@ WsLayout ws_layout(int op, int M, int N, int K) {
   L.partials = off;
   if (L.splits > 1) {
     size_t pb = 4ull * L.splits * M * N;
+    if ((op == WOBS_OP_GEMV_F16 || op == WOBS_OP_GEMV_BF16) && M >= 1) {
+      // fragment-ordered partials of the tensor-core kernel: 256-row tiles,
+      // columns padded to n8 tiles
+      const size_t tb = 4ull * L.splits * ((N + 255) / 256) * 256 * (8 * ((M + 7) / 8));
+      if (tb > pb) pb = tb;
+    }
     if (op == WOBS_OP_GEMV_Q4_0_Q8_1 && M >= 2 && K % 256 == 0) {
       const size_t tb = wobs::q4_mma_partial_bytes(M, N, K, env_splits());
       if (tb > pb) pb = tb;
@@ -173,7 +179,10 @@ int choose_splits(int op, int M, int N, int K) {
       const int kmax = K / 8 > 0 ? K / 8 : 1;
       if (forced) return forced < kmax ? forced : kmax;
       if (M == 1) return 1;
-      int s = (target + groups - 1) / groups;
+      // one CTA per SM: split K only when the 256-row tiles alone leave SMs
+      // idle, and never past one wave
+      const int ntiles = (N + 255) / 256;
+      int s = device_sm_count() / ntiles;
       const int cap = K / 512 > 0 ? K / 512 : 1;
       if (s > cap) s = cap;
       return s < 1 ? 1 : s;

@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kMThreads, 1) dense_mma_kernel(const T* __rest
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int kXBuf = NT * 8 * kXStride;
   uint8_t* xbuf = smem;                                  // [2][NT*8][kXStride]
-  uint8_t* wring = smem + 2 * kXBuf;                     // [kMThreads][kWS][32]
+  uint8_t* wring = smem + 2 * kXBuf;                     // [warps][kWS][2 rows][32 lanes][16 B]
   __shared__ __align__(8) uint64_t xbar[2];
   __shared__ uint64_t s_cta[NT * 8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -331,7 +331,9 @@ __global__ void __launch_bounds__(kMThreads, 1) dense_mma_kernel(const T* __rest
   const int nkt = (k1 - k0 + kKT - 1) / kKT;
   const int ntiles = (N + kMRows - 1) / kMRows;
   const int my_tiles = static_cast<int>(blockIdx.x) < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  uint8_t* myw = wring + tid * (kWS * 32);
+  // lane-contiguous 16-byte pieces: the copies and the 128-bit reads of a
+  // warp touch 512 contiguous bytes each, free of bank conflicts
+  uint8_t* myw = wring + warp * (kWS * 1024) + lane * 16;
 
   int ptile = blockIdx.x, pch = 0;        // weight chunk producer cursor
   auto wissue = [&](int slot) {
@@ -341,8 +343,8 @@ __global__ void __launch_bounds__(kMThreads, 1) dense_mma_kernel(const T* __rest
     const bool v = e < k1;
     const T* pa = W + static_cast<int64_t>(ra) * ldw + (v ? e : 0);
     const T* pb = W + static_cast<int64_t>(rb) * ldw + (v ? e : 0);
-    cp_async16_zfill(myw + slot * 32, pa, v);
-    cp_async16_zfill(myw + slot * 32 + 16, pb, v);
+    cp_async16_zfill(myw + slot * 1024, pa, v);
+    cp_async16_zfill(myw + slot * 1024 + 512, pb, v);
     if (++pch == nch) { pch = 0; ptile += gridDim.x; }
   };
   const int TW = my_tiles * nch;
@@ -393,9 +395,9 @@ __global__ void __launch_bounds__(kMThreads, 1) dense_mma_kernel(const T* __rest
         if (wi + kWS - 1 < TW) wissue((wi + kWS - 1) % kWS);
         cp_async_commit_group();
         cp_async_wait_group<kWS - 1>();
-        const uint8_t* wsl = myw + (wi % kWS) * 32;
+        const uint8_t* wsl = myw + (wi % kWS) * 1024;
         const uint4 a = *reinterpret_cast<const uint4*>(wsl);
-        const uint4 b = *reinterpret_cast<const uint4*>(wsl + 16);
+        const uint4 b = *reinterpret_cast<const uint4*>(wsl + 512);
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           const uint4 xv = *reinterpret_cast<const uint4*>(xs + n * 8 * kXStride + 64 * cc);
@@ -414,26 +416,37 @@ __global__ void __launch_bounds__(kMThreads, 1) dense_mma_kernel(const T* __rest
     const int rg = rbase + warp * 16 + g;
     bool finish = true;
     if (sk.splits > 1) {
+      // fragment order: one coalesced 512-byte store per n8 tile
+      const int64_t fbase = ((static_cast<int64_t>(s) * ntiles + tile) * kMW + warp) * (NT * 32) + lane;
+      float4* pp = reinterpret_cast<float4*>(sk.partials);
 #pragma unroll
-      for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int col = n * 8 + 2 * t + (h & 1), row = rg + 8 * (h >> 1);
-          if (col < M && row < N) sk.partials[(static_cast<int64_t>(s) * M + col) * N + row] = d[n][h];
-        }
+      for (int n = 0; n < NT; ++n) __stcg(pp + fbase + n * 32, make_float4(d[n][0], d[n][1], d[n][2], d[n][3]));
       finish = splitk_arrive_last(sk.counters, tile, sk.splits);
       if (finish) {
 #pragma unroll
-        for (int n = 0; n < NT; ++n)
+        for (int n = 0; n < NT; ++n) d[n][0] = d[n][1] = d[n][2] = d[n][3] = 0.f;
+        // splits added in order, several loaded together
+        constexpr int kB = 16 / NT;
+        const int64_t tstride = static_cast<int64_t>(ntiles) * kMW * NT * 32;
+        const int64_t f0 = (static_cast<int64_t>(tile) * kMW + warp) * (NT * 32) + lane;
+        for (int sp0 = 0; sp0 < sk.splits; sp0 += kB) {
+          float4 v[kB][NT];
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int col = n * 8 + 2 * t + (h & 1), row = rg + 8 * (h >> 1);
-            float acc = 0.f;
-            if (col < M && row < N)
-              for (int sp = 0; sp < sk.splits; ++sp)
-                acc += take_partial(sk.partials + (static_cast<int64_t>(sp) * M + col) * N + row);
-            d[n][h] = acc;
-          }
+          for (int b = 0; b < kB; ++b)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+              v[b][n] = sp0 + b < sk.splits ? __ldcg(pp + (sp0 + b) * tstride + f0 + n * 32)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int b = 0; b < kB; ++b)
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              d[n][0] += v[b][n].x; d[n][1] += v[b][n].y; d[n][2] += v[b][n].z; d[n][3] += v[b][n].w;
+            }
+        }
+        for (int sp = 0; sp < sk.splits; ++sp)
+#pragma unroll
+          for (int n = 0; n < NT; ++n) __stcg(pp + sp * tstride + f0 + n * 32, make_float4(0.f, 0.f, 0.f, 0.f));
       }
     }
     if (finish) {
