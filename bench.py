@@ -500,7 +500,7 @@ class DenseF16:
     name = "fp16_gemv_4096x4096"
     n, k = 4096, 4096
     dtype = "f32"
-    kernel = "dense_m1"
+    kernel = "dense_m1_cp"
     kernel_src = "dense.cu"
     workload_id = 1
     launches_per_step = 1
@@ -564,7 +564,7 @@ class NF4:
     name = "nf4_gemv_28672x8192"
     n, k = 28672, 8192
     dtype = "f32"
-    kernel = "nf4_m1"
+    kernel = "nf4_m1_cp"
     kernel_src = "nf4.cu"
     workload_id = 3
     launches_per_step = 1
@@ -639,7 +639,7 @@ class LmHead:
     n, k = 128000, 4096
     Ms = (1, 32)
     dtype = "f32"
-    kernel = "dense_m1 / dense_mn"
+    kernel = "dense_m1_cp / dense_mma"
     kernel_src = "dense.cu"
     workload_id = 5
     launches_per_step = 2
