@@ -23,6 +23,16 @@ def m1_path(request, monkeypatch):
     return request.param
 
 
+@pytest.fixture(params=["tc", "mma"])
+def mc_path(request, monkeypatch):
+    """Run a multi-column dense test through the tcgen05 kernel and the mma.sync one."""
+    if request.param == "mma":
+        monkeypatch.setenv("WOBS_TC", "0")
+    else:
+        monkeypatch.delenv("WOBS_TC", raising=False)
+    return request.param
+
+
 # ----------------------------------------------------------------- dense
 
 @pytest.mark.parametrize("n,k", [(1, 8), (37, 264), (300, 4096), (1000, 4104), (4096, 4096)])
@@ -35,7 +45,7 @@ def test_gemv_f16_m1(n, k, m1_path):
 
 
 @pytest.mark.parametrize("m,n,k", [(2, 300, 520), (3, 513, 1024), (8, 64, 4096)])
-def test_gemv_f16_multi_column_strided(m, n, k):
+def test_gemv_f16_multi_column_strided(m, n, k, mc_path):
     w = synth.weights(1, (n, k + 8), dtype=torch.float16)[:, :k]       # pitch k+8
     x = synth.activations(1, (m, k + 16), dtype=torch.float16)[:, :k]
     y = wobs.wobs_gemv_f16(w.to(dev()), x.to(dev())).cpu().float().numpy()
@@ -43,9 +53,30 @@ def test_gemv_f16_multi_column_strided(m, n, k):
     assert_within(y, oracle.gemv_dense(wn, xn), oracle.abs_dot_dense(wn, xn), "f16", "gemv_f16 M>1")
 
 
+@pytest.mark.parametrize("m,n,k", [(2, 1, 8), (9, 127, 72), (16, 129, 64), (17, 1000, 4104),
+                                   (31, 300, 520), (32, 4100, 1024), (1, 19600, 136), (3, 19500, 200)])
+def test_dense_multi_column_small_integers_exact(m, n, k, mc_path):
+    # small integers: every product and partial sum is exact in fp32, so the
+    # logits equal the integer result bit for bit whatever the summation order
+    # (pins the K tail, padded columns and rows, and the operand layouts)
+    rng = np.random.default_rng(m * 1000 + n)
+    w = rng.integers(-8, 9, size=(n, k)).astype(np.float32)
+    x = rng.integers(-8, 9, size=(m, k)).astype(np.float32)
+    exact = (x.astype(np.float64) @ w.astype(np.float64).T).astype(np.float32)
+    wt = torch.from_numpy(w).to(torch.bfloat16).to(dev())
+    xt = torch.from_numpy(x).to(torch.bfloat16).to(dev())
+    lg, am = wobs.wobs_gemv_bf16(wt, xt, want_argmax=True)
+    lgn = lg.cpu().numpy()
+    assert np.array_equal(lgn, exact)
+    assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(lgn))
+    y16 = wobs.wobs_gemv_f16(wt.to(torch.float16), xt.to(torch.float16)).cpu().float().numpy()
+    ref16 = exact.astype(np.float16).astype(np.float32)
+    assert np.array_equal(y16, ref16)
+
+
 @pytest.mark.parametrize("m,n,k", [(1, 1, 8), (1, 5000, 1024), (1, 3001, 4104), (2, 777, 512),
                                    (5, 1200, 2048), (32, 2000, 4096)])
-def test_gemv_bf16_logits_and_argmax(m, n, k, m1_path):
+def test_gemv_bf16_logits_and_argmax(m, n, k, m1_path, mc_path):
     w = synth.weights(5, (n, k), dtype=torch.bfloat16)
     x = synth.activations(5, (m, k), dtype=torch.bfloat16)
     logits, am = wobs.wobs_gemv_bf16(w.to(dev()), x.to(dev()), want_argmax=True)
@@ -72,7 +103,7 @@ def test_m1_dispatch_coverage(monkeypatch, capfd):
     err = capfd.readouterr().err
     lines = [ln for ln in err.splitlines() if ln.startswith("wobs: op=")]
     kernels = [ln.split("kernel=")[1].split()[0] for ln in lines]
-    assert kernels == ["q4_0_q8_1_m1_cp", "q4_0_q8_1_m1", "dense_m1_cp", "dense_mma",
+    assert kernels == ["q4_0_q8_1_m1_cp", "q4_0_q8_1_m1", "dense_m1_cp", "dense_tc",
                        "q4_0_q8_1_m1"], kernels
 
 

@@ -179,8 +179,10 @@ int choose_splits(int op, int M, int N, int K) {
       const int kmax = K / 8 > 0 ? K / 8 : 1;
       if (forced) return forced < kmax ? forced : kmax;
       if (M == 1) return 1;
-      // one CTA per SM: split K only when the 256-row tiles alone leave SMs
-      // idle, and never past one wave
+      // one CTA per SM: no split when the tensor-core kernel's 128-row tiles
+      // fill the GPU; otherwise split K for the 256-row mma.sync tiles, never
+      // past one wave
+      if ((N + 127) / 128 >= device_sm_count()) return 1;
       const int ntiles = (N + 255) / 256;
       int s = device_sm_count() / ntiles;
       const int cap = K / 512 > 0 ? K / 512 : 1;

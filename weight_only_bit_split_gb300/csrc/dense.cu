@@ -539,6 +539,13 @@ cudaError_t launch_gemv_dense(int dtype, const void* W, int64_t ldw, const void*
                               int M, void* Y, int out_f32, int N, int K, const SplitArgs& sk,
                               const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   const bool m1 = (M == 1 && sk.splits <= 1);
+  // tensor-core streaming kernel: any column count, as long as its 128-row
+  // tiles alone fill the GPU (it has no K split)
+  if (sk.splits <= 1 && dense_tc_enabled() && (M >= 2 || (N + 127) / 128 >= device_sm_count())) {
+    const cudaError_t e = launch_gemv_dense_tc(dtype, W, ldw, X, ldx, M, Y, N, K, am, st, info);
+    if (e != cudaErrorNotSupported) return e;
+    cudaGetLastError();
+  }
   // asynchronous copies: 16-byte aligned rows (checked by the caller), x in smem
   const bool cp = m1 && !m1_ldg_forced() && (kRingBytes + K * 2 <= 200 * 1024);
   if (dtype == 0) {

@@ -44,6 +44,13 @@ cudaError_t launch_gemv_dense(int dtype, const void* W, int64_t ldw, const void*
                               int M, void* Y, int out_f32, int N, int K, const SplitArgs& sk,
                               const ArgmaxArgs& am, cudaStream_t st, Launch* info);
 
+// Dense 2..32 columns on tcgen05 / TMA (no K split); cudaErrorNotSupported
+// when the driver offers no tensor-map encoder.  WOBS_TC=0 turns it off.
+cudaError_t launch_gemv_dense_tc(int dtype, const void* W, int64_t ldw, const void* X, int64_t ldx,
+                                 int M, void* Y, int N, int K, const ArgmaxArgs& am, cudaStream_t st,
+                                 Launch* info);
+bool dense_tc_enabled();
+
 cudaError_t launch_quantize_q8_1(const float* X, int64_t ldx, int M, int K, void* xq,
                                  cudaStream_t st, Launch* info);
 cudaError_t launch_quantize_q4_0(const float* W, int64_t ldw, int N, int K, uint8_t* qs,
