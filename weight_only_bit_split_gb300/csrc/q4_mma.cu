@@ -42,9 +42,6 @@
 namespace wobs {
 namespace {
 
-constexpr int kQW = 8;                  // warps per CTA
-constexpr int kQThreads = kQW * 32;
-constexpr int kQRing = 3;               // stages per warp ring
 constexpr int kQSB = 8;                 // blocks per stage
 constexpr int kQPitch = 144;            // bytes per row in a stage (128 codes + 16 scales)
 constexpr int kQStage = 16 * kQPitch;   // 2304 bytes
@@ -92,6 +89,18 @@ __device__ __forceinline__ void mma_f16(float& c0, float& c1, float& c2, float& 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D = A.B + {s0, s1, s0, s1}: the accumulator starts from two values (one
+// per output column of the lane) without copying them into four registers.
+__device__ __forceinline__ void mma_f16_init(float& d0, float& d1, float& d2, float& d3, uint32_t a0,
+                                             uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                             uint32_t b1, float s0, float s1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%10,%11};"
+      : "=f"(d0), "=f"(d1), "=f"(d2), "=f"(d3)
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(s0), "f"(s1));
+}
+
 // Warp-level split-K arrival: true in the warp that brings the count to
 // `splits` (it resets the counter, and then sees every split's partials).
 __device__ __forceinline__ bool splitk_arrive_last_warp(unsigned* counters, int group, int splits) {
@@ -110,15 +119,22 @@ __device__ __forceinline__ bool splitk_arrive_last_warp(unsigned* counters, int 
 
 // Rows one warp owns at a time: R m16 tiles share every activation fragment
 // read from shared memory.
+// With 9 or more columns a warp owns 32 rows, and the CTA runs 16 warps
+// with 2-stage rings (more warps to hide the tensor-core and shared-memory
+// latencies, the same bytes in flight); below that, 8 warps with 3-stage
+// rings and two CTAs per SM.
 template <int NT>
 struct Q4Shape {
   static constexpr int R = NT >= 2 ? 2 : 1;
   static constexpr int kRows = 16 * R;
   static constexpr int kStage = kRows * kQPitch;
+  static constexpr int kW = NT >= 2 ? 16 : 8;
+  static constexpr int kThreads = kW * 32;
+  static constexpr int kRing = NT >= 2 ? 2 : 3;
 };
 
 template <int NT, bool kArgmax>
-__global__ void __launch_bounds__(kQThreads, NT == 1 ? 2 : 1) q4_mma_kernel(const uint8_t* __restrict__ qs,
+__global__ void __launch_bounds__(Q4Shape<NT>::kThreads, NT == 1 ? 2 : 1) q4_mma_kernel(const uint8_t* __restrict__ qs,
                                                                const uint16_t* __restrict__ d4,
                                                                const uint8_t* __restrict__ xq, int M,
                                                                float* __restrict__ Y, int N, int K,
@@ -127,6 +143,9 @@ __global__ void __launch_bounds__(kQThreads, NT == 1 ? 2 : 1) q4_mma_kernel(cons
   constexpr int R = Q4Shape<NT>::R;
   constexpr int RW = Q4Shape<NT>::kRows;
   constexpr int STG = Q4Shape<NT>::kStage;
+  constexpr int kQW = Q4Shape<NT>::kW;
+  constexpr int kQThreads = Q4Shape<NT>::kThreads;
+  constexpr int kQRing = Q4Shape<NT>::kRing;
   extern __shared__ __align__(16) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -302,8 +321,8 @@ __global__ void __launch_bounds__(kQThreads, NT == 1 ? 2 : 1) q4_mma_kernel(cons
         const float dgb = (j & 1) ? half_hi(swb) : half_lo(swb);
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          float c0 = cd[n].x, c1 = cd[n].y, c2 = cd[n].x, c3 = cd[n].y;
-          mma_f16(c0, c1, c2, c3, a0, a1, a2, a3, xv[n].x, xv[n].y);
+          float c0, c1, c2, c3;
+          mma_f16_init(c0, c1, c2, c3, a0, a1, a2, a3, xv[n].x, xv[n].y, cd[n].x, cd[n].y);
           mma_f16(c0, c1, c2, c3, h0, h1, h2, h3, xv[n].z, xv[n].w);
           const float2 d8 = make_float2(cd[n].z, cd[n].w);
           const float2 sa2 = f32x2_mul(make_float2(dga, dga), d8);
@@ -469,7 +488,8 @@ cudaError_t run_t(const uint8_t* qs, const void* d, const void* xq, int M, float
                   Launch* info) {
   const int kpb = plan.kpb, splits = plan.splits;
   if (splits > 1 && splits > sk.splits) return cudaErrorInvalidValue;   // workspace too small
-  const int smem = kpb * NT * kQXBytes + kQW * kQRing * Q4Shape<NT>::kStage;
+  constexpr int kQW = Q4Shape<NT>::kW, kQThreads = Q4Shape<NT>::kThreads;
+  const int smem = kpb * NT * kQXBytes + kQW * Q4Shape<NT>::kRing * Q4Shape<NT>::kStage;
   auto kern = q4_mma_kernel<NT, kArgmax>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
