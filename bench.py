@@ -639,8 +639,8 @@ class LmHead:
     n, k = 128000, 4096
     Ms = (1, 32)
     dtype = "f32"
-    kernel = "dense_m1_cp / dense_mma"
-    kernel_src = "dense.cu"
+    kernel = "dense_tc"
+    kernel_src = "dense_tc.cu"
     workload_id = 5
     launches_per_step = 2
 
