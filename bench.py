@@ -219,6 +219,19 @@ def time_steps(cycle, singles, steps, stream):
     return e0.elapsed_time(e1)
 
 
+def packed(shapes, dtype, device):
+    """One flat device buffer and views of it with the given shapes (16-byte
+    aligned offsets), so a step's inputs or outputs move in one copy."""
+    esize = torch.empty(0, dtype=dtype).element_size()
+    align = max(1, 16 // esize)
+    offs, total = [], 0
+    for shp in shapes:
+        offs.append(total)
+        total += (math.prod(shp) + align - 1) // align * align
+    flat = torch.empty(total, dtype=dtype, device=device)
+    return flat, [flat[o:o + math.prod(shp)].view(shp) for o, shp in zip(offs, shapes)]
+
+
 def capture(fn, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -319,9 +332,11 @@ class Q4M1:
                 row.append(wobs.wobs_quantize_q4_0(w))
                 del w
             self.planes.append(row)
-        self.x = [synth.activations(self.workload_id, (1, k), device=device) for _, k in self.shapes]
+        self.x_all, self.x = packed([(1, k) for _, k in self.shapes], torch.float32, device)
+        for xv, (_, k) in zip(self.x, self.shapes):
+            xv.copy_(synth.activations(self.workload_id, (1, k), device=device))
         self.xq = [torch.empty(1, k // 32 * 36, dtype=torch.uint8, device=device) for _, k in self.shapes]
-        self.y = [torch.empty(1, n, dtype=torch.float32, device=device) for n, _ in self.shapes]
+        self.y_all, self.y = packed([(1, n) for n, _ in self.shapes], torch.float32, device)
         torch.cuda.synchronize(device)
 
     @staticmethod
@@ -355,18 +370,15 @@ class Q4M1:
         return out
 
     def e2e_setup(self):
-        self.xh = [x.cpu().pin_memory() for x in self.x]
-        self.yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in self.y]
-        return sum(x.numel() * 4 for x in self.xh), sum(y.numel() * 4 for y in self.yh)
+        # the step's activations and outputs each live in one packed buffer
+        self.xh = self.x_all.cpu().pin_memory()
+        self.yh = torch.empty(self.y_all.shape, dtype=self.y_all.dtype).pin_memory()
+        return self.xh.numel() * 4, self.yh.numel() * 4
 
     def e2e_step(self, c):
-        w = self.wobs
-        for s in range(len(self.shapes)):
-            self.x[s].copy_(self.xh[s], non_blocking=True)
-            w.wobs_quantize_q8_1(self.x[s], self.xq[s])
-            qs, d = self.planes[c][s]
-            w.wobs_gemv_q4_0_q8_1(qs, d, self.xq[s], y=self.y[s])
-            self.yh[s].copy_(self.y[s], non_blocking=True)
+        self.x_all.copy_(self.xh, non_blocking=True)
+        self.step(c)
+        self.yh.copy_(self.y_all, non_blocking=True)
 
     def config(self):
         return {"workload": self.name, "shapes_NxK": [f"{n}x{k}" for n, k in self.shapes], "M": 1,
@@ -412,10 +424,14 @@ class Q4Sweep(Q4M1):
         super().__init__(device)
         from weight_only_bit_split_gb300 import synth
         k = self.shapes[0][1]
-        self.X = {m: synth.activations(self.workload_id, (m, k), copy=m, device=device) for m in self.Ms}
+        self.X_all, xs = packed([(m, k) for m in self.Ms], torch.float32, device)
+        self.X = dict(zip(self.Ms, xs))
+        for m in self.Ms:
+            self.X[m].copy_(synth.activations(self.workload_id, (m, k), copy=m, device=device))
         self.XQ = {m: torch.empty(m, k // 32 * 36, dtype=torch.uint8, device=device) for m in self.Ms}
-        self.Y = {(m, s): torch.empty(m, n, dtype=torch.float32, device=device)
-                  for m in self.Ms for s, (n, _) in enumerate(self.shapes)}
+        keys = [(m, s) for m in self.Ms for s in range(len(self.shapes))]
+        self.Y_all, ys = packed([(m, self.shapes[s][0]) for m, s in keys], torch.float32, device)
+        self.Y = dict(zip(keys, ys))
         self.ws = {(m, s): self.wobs.workspace(self.wobs.OP_GEMV_Q4_0_Q8_1, m, n, k, device)
                    for m in self.Ms for s, (n, _) in enumerate(self.shapes)}
         self.ws = {key: (torch.zeros_like(v) if v is not None else None) for key, v in self.ws.items()}
@@ -451,17 +467,14 @@ class Q4Sweep(Q4M1):
         return out
 
     def e2e_setup(self):
-        self.xh = {m: x.cpu().pin_memory() for m, x in self.X.items()}
-        self.yh = {key: torch.empty(y.shape, dtype=y.dtype).pin_memory() for key, y in self.Y.items()}
-        return sum(x.numel() * 4 for x in self.xh.values()), sum(y.numel() * 4 for y in self.yh.values())
+        self.xh = self.X_all.cpu().pin_memory()
+        self.yh = torch.empty(self.Y_all.shape, dtype=self.Y_all.dtype).pin_memory()
+        return self.xh.numel() * 4, self.yh.numel() * 4
 
     def e2e_step(self, c):
-        for m in self.Ms:
-            self.X[m].copy_(self.xh[m], non_blocking=True)
-            self.wobs.wobs_quantize_q8_1(self.X[m], self.XQ[m])
-            for s in range(len(self.shapes)):
-                self._gemv(c, s, m)
-                self.yh[(m, s)].copy_(self.Y[(m, s)], non_blocking=True)
+        self.X_all.copy_(self.xh, non_blocking=True)
+        self.step(c)
+        self.yh.copy_(self.Y_all, non_blocking=True)
 
     def config(self):
         c = super().config()
@@ -846,18 +859,21 @@ def main(argv=None):
     peak, peak_kind = measured_peaks()
     traffic = traffic_record(cls.kernel if isinstance(cls.kernel, str) else None)
 
-    # end to end through the public API with pinned host buffers
+    # end to end through the public API with pinned host buffers: each
+    # step's calls (H2D of the inputs, quantise/GEMV launches, D2H of the
+    # outputs) captured once per weight copy in a StepGraph and replayed
     h2d, d2h = wl.e2e_setup()
     e2e_steps = max(3, min(args.steps, 200))
+    step_graphs = [wobs.StepGraph(lambda c=c: wl.e2e_step(c), stream) for c in range(wl.copies)]
     with torch.cuda.stream(stream):
         for i in range(3):
-            wl.e2e_step(i % wl.copies)
+            step_graphs[i % wl.copies].replay()
         stream.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for i in range(e2e_steps):
-            wl.e2e_step(i % wl.copies)
+            step_graphs[i % wl.copies].replay()
         e1.record(stream)
     e1.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -892,8 +908,9 @@ def main(argv=None):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
-                    "how": "public Python API per step: pinned H2D of the activations, the "
-                           "step's launches, D2H of the outputs"},
+                    "how": "public Python API calls of one step captured once per weight copy "
+                           "in a wobs.StepGraph and replayed every step: pinned H2D of the "
+                           "activations, the step's launches, D2H of the outputs"},
             "gpu_launches": wl.launches_per_step * args.steps,
             "clocks": clocks.report(),
         }

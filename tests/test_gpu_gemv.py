@@ -359,3 +359,39 @@ def test_bw_probe_reads_every_word(variant, nbytes):
         got = int(out.cpu().numpy().view(np.uint32)[0])
         assert got == int(oracle.xor_words(buf.cpu().numpy()))
     assert wobs.wobs_error_word() == 0
+
+
+# ------------------------------------------------------------ step graph
+
+def test_step_graph_replays_the_captured_calls():
+    (qs, d, xq), ref, ad, _ = _q4_case(777, 4096, 1)
+    n, k = 777, 4096
+    xh = torch.from_numpy(synth.activations(2, (1, k), copy=9).numpy()).pin_memory()
+    x = torch.empty(1, k, device=dev())
+    xq2 = torch.empty_like(xq)
+    y = torch.empty(1, n, device=dev())
+    yh = torch.empty(1, n).pin_memory()
+
+    def step():
+        x.copy_(xh, non_blocking=True)
+        wobs.wobs_quantize_q8_1(x, xq2)
+        wobs.wobs_gemv_q4_0_q8_1(qs, d, xq2, y=y)
+        yh.copy_(y, non_blocking=True)
+
+    g = wobs.StepGraph(step)
+    eager = yh.clone()
+    for _ in range(3):
+        yh.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(yh, eager)
+    # new inputs written into the pinned buffer are picked up by the next replay
+    xh.copy_(torch.from_numpy(synth.activations(2, (1, k), copy=10).numpy()))
+    g.replay()
+    torch.cuda.synchronize()
+    step()
+    torch.cuda.synchronize()
+    again = yh.clone()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(yh, again) and not torch.equal(again, eager)

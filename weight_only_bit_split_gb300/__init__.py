@@ -72,6 +72,33 @@ def _codebook(cb):
     return (ctypes.c_float * 16)(*vals)
 
 
+# ----------------------------------------------------------- step graph
+
+class StepGraph:
+    """A fixed sequence of library calls, replayed as one CUDA graph.
+
+    Decode loops make the same calls with the same shapes and buffers for
+    every token.  ``fn`` (any mix of ``wobs_*`` calls and tensor copies) runs
+    once eagerly on ``stream``, which also sizes the cached workspaces, and is
+    then captured; ``replay()`` launches the whole sequence with one graph
+    launch on the current stream.  Every buffer the calls touch must stay
+    alive and in place while the graph is used; host buffers of copies must
+    be pinned.
+    """
+
+    def __init__(self, fn, stream=None):
+        self.stream = stream if stream is not None else torch.cuda.Stream()
+        with torch.cuda.stream(self.stream):
+            fn()
+        self.stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            fn()
+
+    def replay(self):
+        self.graph.replay()
+
+
 # ------------------------------------------------------------ workspace
 
 _ws_cache = {}
