@@ -40,7 +40,9 @@
  *   - Environment: WOBS_DEBUG=1 logs every dispatch (op, shape, kernel,
  *     grid, split) to stderr; WOBS_SPLITK=<s> overrides the split-K factor
  *     of the dense and Q4_0 multi-column kernels (testing only; the
- *     workspace must be sized for it with the same variable set).
+ *     workspace must be sized for it with the same variable set);
+ *     WOBS_TC=0 keeps dense GEMVs off the tcgen05 kernel and WOBS_M1=ldg
+ *     selects the direct-load M = 1 kernels (both for testing).
  */
 #ifndef WOBS_H
 #define WOBS_H

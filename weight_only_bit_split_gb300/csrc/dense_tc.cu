@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
       pdl_wait();
       for (int i = 0; i < pre; ++i)
         tma_load_2d(base + i * S::kStage + kTcABytes, &tx, (i % nk) * kTcK, 0, &full[i]);
+      int issued = pre;
       for (int i = pre; i < total; ++i) {
         const int s = i % kTcStages;
         if (!mbar_wait(&empty[s], ((i / kTcStages) & 1) ^ 1)) { s_abort = 1; break; }
@@ -197,6 +198,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) dense_tc_kernel(const __grid_co
         mbar_expect_tx(&full[s], S::kStage);
         tma_load_2d(base + s * S::kStage, &tw, k0, tile * kTcRows, &full[s]);
         tma_load_2d(base + s * S::kStage + kTcABytes, &tx, k0, 0, &full[s]);
+        issued = i + 1;
+      }
+      if (s_abort) {
+        // copies still in flight must land before the CTA's shared memory is
+        // released: wait (bounded) for the last round of stages issued
+        const int first = issued > kTcStages ? issued - kTcStages : 0;
+        for (int i = first; i < issued; ++i) mbar_wait(&full[i % kTcStages], (i / kTcStages) & 1);
       }
     }
   } else if (warp == 1) {

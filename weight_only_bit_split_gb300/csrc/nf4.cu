@@ -263,9 +263,9 @@ __global__ void __launch_bounds__(kThreads, 2) nf4_m1_cp_kernel(const uint8_t* _
   }
   __syncthreads();                         // the codebook table is complete
 
-  // byte offset of (code pair e, this lane's replica) in the table: e*128 + replica*8
-  const uint32_t lut_s = static_cast<uint32_t>(__cvta_generic_to_shared(lut));
-  const uint32_t rep8 = static_cast<uint32_t>(lane & (kLutCopies - 1)) * 8u;
+  // this lane's replica of the table; entry e starts e * 128 bytes further
+  const uint32_t lut_b = static_cast<uint32_t>(__cvta_generic_to_shared(lut)) +
+                         static_cast<uint32_t>(lane & (kLutCopies - 1)) * 8u;
   uint64_t best = 0;
   int cbt = bfirst;                        // batch being consumed
   for (int t = 0; t < T; t += kOct, cbt += bstride) {
@@ -289,9 +289,10 @@ __global__ void __launch_bounds__(kThreads, 2) nf4_m1_cp_kernel(const uint8_t* _
         for (int i = 0; i < 4; ++i) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint32_t off = (j == 0 ? (w[i] << 7) : (w[i] >> (8 * j - 7))) & 0x7F80u;
+            // byte j of the word -> table entry (byte * 16 + replica) * 8
+            const uint32_t e = __byte_perm(w[i], 0u, 0x4440u | static_cast<uint32_t>(j));
             float2 v;
-            asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(lut_s + (off | rep8)));
+            asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(e * 128u + lut_b));
             acc = ffma2(v, xr[4 * i + j], acc);
           }
         }
