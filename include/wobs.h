@@ -262,6 +262,16 @@ WOBS_API int wobs_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, 
  */
 WOBS_API int wobs_error_word(void* stream, int* host_out);
 
+/*
+ * Test export for the failure path (no counterpart on the pages): launches
+ * one warp that waits on an mbarrier nothing arrives on, bounded by
+ * `limit_cycles` (1 ... 1e9 SM clock cycles), so the wait gives up, writes
+ * WOBS_DEVICE_WAIT_SELFTEST (3) to the device error word and the kernel
+ * returns; the context stays usable.  Codes the kernels write: 1 = a
+ * read-ceiling probe wait, 2 = a GEMV copy wait, 3 = this self test.
+ */
+WOBS_API int wobs_selftest_wait_timeout(long long limit_cycles, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -344,6 +344,13 @@ def wobs_q4_0_q8_1_blockdots(qs, xq):
     return out
 
 
+def wobs_selftest_wait_timeout(limit_cycles=1_000_000, device=None):
+    """Launch the failure-path self test (a wait that gives up); returns nothing."""
+    lib = _lib.get()
+    device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    _check(lib.wobs_selftest_wait_timeout(int(limit_cycles), _stream(device)), lib)
+
+
 def wobs_error_word(device=None):
     """Read and clear the device error word (synchronises the current stream)."""
     lib = _lib.get()

@@ -40,6 +40,7 @@ SIGNATURES = {
     "wobs_q4_0_q8_1_blockdots": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p,
                                          c_void_p]),
     "wobs_error_word": (c_int, [c_void_p, ctypes.POINTER(c_int)]),
+    "wobs_selftest_wait_timeout": (c_int, [ctypes.c_longlong, c_void_p]),
 }
 
 

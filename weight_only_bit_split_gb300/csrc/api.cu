@@ -417,6 +417,14 @@ int wobs_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, int N, in
   return finish_launch(e, "q4_0_q8_1_blockdots", M, N, K, L, 1);
 }
 
+int wobs_selftest_wait_timeout(long long limit_cycles, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > 1000000000ll)
+    return fail(WOBS_ERR_INVALID_ARG, "selftest_wait_timeout: limit %lld outside 1..1e9 cycles", limit_cycles);
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_wait_timeout(limit_cycles, static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "selftest_wait_timeout", 0, 0, 0, L, 1);
+}
+
 int wobs_error_word(void* stream, int* host_out) {
   if (!host_out) return fail(WOBS_ERR_INVALID_ARG, "error_word: null pointer");
   cudaError_t e = wobs::read_and_clear_error_word(static_cast<cudaStream_t>(stream), host_out);

@@ -82,12 +82,14 @@ cudaError_t launch_gemv_nf4(const uint8_t* qs, const float* absmax, const Codebo
                             cudaStream_t st, Launch* info);
 
 cudaError_t read_and_clear_error_word(cudaStream_t st, int* host_out);
+cudaError_t launch_wait_timeout(long long limit, cudaStream_t st, Launch* info);
 // Device address of the error word on the current device (null if unknown).
 int* error_word_ptr();
 
 // Device error codes written to the error word.
 constexpr int kErrProbeWait = 1;      // bw_probe bulk-copy wait gave up
 constexpr int kErrGemvWait = 2;       // a GEMV bulk-copy wait gave up
+constexpr int kErrSelfTestWait = 3;   // the failure-path self test's wait gave up (expected)
 
 // Which M = 1 kernel family to use: bulk-copy rings (default where the
 // shape allows) or direct 16-byte loads (WOBS_M1=ldg forces the latter).

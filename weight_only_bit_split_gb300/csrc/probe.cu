@@ -11,6 +11,7 @@
 #include <cstdio>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace wobs {
 
@@ -91,28 +92,7 @@ __global__ void __launch_bounds__(kProbeThreads) probe32_kernel(const uint4* buf
 // Variant 3: cp.async.bulk (TMA, 1-D) into a ring of shared-memory stages.
 constexpr int kBulkStages = 4;
 constexpr int kBulkChunk = 32768;  // bytes per stage
-constexpr long long kWaitCycles = 2000000000ll;  // ~1 s at GB300 clocks
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Bounded wait on an mbarrier phase; false if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  const uint32_t a = smem_u32(bar);
-  const long long t0 = clock64();
-  while (true) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (ok) return true;
-    if (clock64() - t0 > kWaitCycles) return false;
-  }
-}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return smem_addr(p); }
 
 __device__ __forceinline__ void bulk_issue(void* dst, const void* src, uint32_t bytes,
                                            uint64_t* bar) {
@@ -234,6 +214,30 @@ cudaError_t launch_bw_probe(const void* buf, size_t bytes, int grid, int variant
       probe_bulk_kernel<<<grid, kProbeThreads, smem, st>>>(static_cast<const uint8_t*>(buf), bytes, xor_out);
       break;
   }
+  return cudaGetLastError();
+}
+
+// Failure-path self test: one warp waits on an mbarrier that nothing
+// arrives on, with a short bound; the wait gives up, the error word gets
+// kErrSelfTestWait and the kernel returns normally (no trap, no hang).
+__global__ void wait_timeout_kernel(long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(&bar, 0, limit);
+  if (!__all_sync(0xffffffffu, ok) && threadIdx.x == 0) atomicExch(&g_error_word, kErrSelfTestWait);
+  // leave the barrier complete so nothing is pending at exit
+  if (threadIdx.x == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(&bar)) : "memory");
+}
+
+cudaError_t launch_wait_timeout(long long limit, cudaStream_t st, Launch* info) {
+  info->grid_x = 1;
+  info->block = 32;
+  info->kernel = "wait_timeout";
+  wait_timeout_kernel<<<1, 32, 0, st>>>(limit);
   return cudaGetLastError();
 }
 

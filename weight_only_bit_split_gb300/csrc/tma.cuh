@@ -32,8 +32,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
 
-// Wait for the phase with parity `parity` to complete; false after the limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with parity `parity` to complete; false after `limit`
+// clock cycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          long long limit = kWaitCycles) {
   const uint32_t a = smem_addr(bar);
   uint32_t ok;
   asm volatile(
@@ -48,7 +50,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok) : "r"(a), "r"(parity) : "memory");
     if (ok) return true;
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
 }
 
