@@ -155,7 +155,9 @@ __global__ void __launch_bounds__(kCpThreads) dense_m1_cp_kernel(const T* __rest
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int total_warps = gridDim.x * kCpWarps;
-  const int wg = blockIdx.x * kCpWarps + warp;
+  // rows spread round-robin over the CTAs first, so every SM gets an
+  // equal share even when there are fewer rows than warps
+  const int wg = warp * gridDim.x + blockIdx.x;
   const int row_bytes = K * 2;
   const int nseg = (row_bytes + kSeg - 1) / kSeg;
   const int rows_w = wg < N ? (N - 1 - wg) / total_warps + 1 : 0;
@@ -244,8 +246,7 @@ cudaError_t run_m1_cp_t(const void* W, int64_t ldw, const void* x, void* y, int 
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int grid = 2 * device_sm_count();
-  const int need = (N + kCpWarps - 1) / kCpWarps;
-  if (grid > need) grid = need;
+  if (grid > N) grid = N;
   info->grid_x = grid;
   info->block = kCpThreads;
   info->smem = smem;

@@ -232,7 +232,9 @@ __global__ void __launch_bounds__(kCpThreads) q4_m1_cp_kernel(const uint8_t* __r
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int total_warps = gridDim.x * kCpWarps;
-  const int wg = blockIdx.x * kCpWarps + warp;
+  // rows spread round-robin over the CTAs first, so every SM gets an
+  // equal share even when there are fewer rows than warps
+  const int wg = warp * gridDim.x + blockIdx.x;
   const int nseg = (nb + kSegBlocks - 1) / kSegBlocks;
   const int rows_w = wg < N ? (N - 1 - wg) / total_warps + 1 : 0;
   const int T = rows_w * nseg;
@@ -336,8 +338,7 @@ cudaError_t run_m1_cp_t(const uint8_t* qs, const void* d, const void* xq, float*
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int grid = 2 * device_sm_count();
-  const int need = (N + kCpWarps - 1) / kCpWarps;
-  if (grid > need) grid = need;
+  if (grid > N) grid = N;
   info->grid_x = grid;
   info->block = kCpThreads;
   info->smem = smem;
