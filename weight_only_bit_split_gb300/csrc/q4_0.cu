@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc_cp_kernel(
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int total_warps = gridDim.x * W;
-  const int wg = blockIdx.x * W + warp;
+  const int wg = warp * gridDim.x + blockIdx.x;   // rows round-robin over the CTAs first
   const int nseg = (nb + kSegBlocks - 1) / kSegBlocks;
   const int rows_w = wg < N ? (N - 1 - wg) / total_warps + 1 : 0;
   const int T = rows_w * nseg;
@@ -513,8 +513,7 @@ cudaError_t run_mc_t(const uint8_t* qs, const void* d, const void* xq, int M, fl
   if (e != cudaSuccess) return e;
   const int per_sm = max_resident_ctas(reinterpret_cast<const void*>(kern), W * 32, smem);
   int grid = device_sm_count() * (per_sm > 0 ? per_sm : 1);
-  const int need = (N + W - 1) / W;
-  if (grid > need) grid = need;
+  if (grid > N) grid = N;
   info->grid_x = grid;
   info->block = W * 32;
   info->smem = smem;
