@@ -113,7 +113,7 @@ def test_dense_f16_output_stays_in_bounds(m, n, k):
     check_guards(gy, f"f16 M={m}")
 
 
-@pytest.mark.parametrize("n,k", [(100, 8192), (33, 1088), (95, 2048)])
+@pytest.mark.parametrize("n,k", [(100, 8192), (33, 1088), (95, 2048), (5003, 8192)])
 def test_nf4_output_stays_in_bounds(n, k):
     cb = nf4_codebook_fixture()
     w = synth.weights(3, (n, k), dtype=torch.bfloat16).float().numpy()

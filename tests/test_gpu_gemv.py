@@ -318,9 +318,23 @@ def _nf4_case(n, k, copy=0):
     return cb, to_dev(qs), to_dev(absmax), x.to(dev()).reshape(-1), ref, ad
 
 
+@pytest.fixture(params=["mma", "cp", "ldg"])
+def nf4_path(request, monkeypatch):
+    """Run an NF4 test through the tensor-core kernel, the staged CUDA-core one
+    and the plain-load one (shapes a kernel does not take fall through to the
+    next)."""
+    monkeypatch.delenv("WOBS_NF4", raising=False)
+    monkeypatch.delenv("WOBS_M1", raising=False)
+    if request.param == "cp":
+        monkeypatch.setenv("WOBS_NF4", "cp")
+    elif request.param == "ldg":
+        monkeypatch.setenv("WOBS_M1", "ldg")
+    return request.param
+
+
 @pytest.mark.parametrize("n,k", [(1, 64), (31, 1024), (100, 8192), (33, 1088), (257, 4096),
-                                 (70, 16384), (95, 2048), (1000, 8192)])
-def test_gemv_nf4(n, k, m1_path):
+                                 (70, 16384), (95, 2048), (1000, 8192), (3, 8192), (129, 6144)])
+def test_gemv_nf4(n, k, nf4_path):
     cb, qs, am, x, ref, ad = _nf4_case(n, k)
     y, idx = wobs.wobs_gemv_nf4(qs, am, cb, x, want_argmax=True)
     yf = y.float().cpu().numpy()
@@ -328,16 +342,52 @@ def test_gemv_nf4(n, k, m1_path):
     assert int(idx.item()) == int(oracle.argmax_rows(yf)[0])
 
 
+# more row tiles than the ring has stages in every CTA, and a ragged last tile
+@pytest.mark.parametrize("n,k", [(5003, 8192), (60013, 1024)])
+def test_gemv_nf4_stage_ring_wraps(n, k):
+    cb, qs, am, x, ref, ad = _nf4_case(n, k, copy=1)
+    y, idx = wobs.wobs_gemv_nf4(qs, am, cb, x, want_argmax=True)
+    yf = y.float().cpu().numpy()
+    assert_within(yf, ref, ad, "bf16", f"nf4 {n}x{k}")
+    assert int(idx.item()) == int(oracle.argmax_rows(yf)[0])
+
+
+# activation and codebook magnitudes far from 1: the tensor-core kernel's
+# power-of-two scalings must come back out exactly
+@pytest.mark.parametrize("xmul,cbmul", [(2.0 ** 40, 1.0), (2.0 ** -40, 1.0), (1.0, 1000.0),
+                                        (3.0e-3, 2.0 ** -30)])
+def test_gemv_nf4_scaled_inputs(xmul, cbmul):
+    n, k = 300, 4096
+    cb = (np.asarray(nf4_codebook_fixture(), np.float32) * np.float32(cbmul)).astype(np.float32)
+    w = synth.weights(4, (n, k), dtype=torch.bfloat16).float().numpy()
+    x = (synth.activations(4, (1, k)) * xmul).to(torch.bfloat16)
+    codes, absmax = oracle.quantize_nf4(w, np.asarray(nf4_codebook_fixture(), np.float32))
+    qs = oracle.pack_nf4(codes)
+    xf = x.float().numpy()
+    ref = oracle.gemv_nf4(qs, absmax, cb, xf)[0]
+    ad = oracle.abs_dot_nf4(qs, absmax, cb, xf)[0]
+    y, _ = wobs.wobs_gemv_nf4(to_dev(qs), to_dev(absmax), cb, x.to(dev()).reshape(-1))
+    assert_within(y.float().cpu().numpy(), ref, ad, "bf16", f"nf4 x*{xmul} cb*{cbmul}")
+
+
 def test_nf4_dispatch_coverage(monkeypatch, capfd):
     monkeypatch.setenv("WOBS_DEBUG", "1")
     monkeypatch.delenv("WOBS_M1", raising=False)
+    monkeypatch.delenv("WOBS_NF4", raising=False)
     for k in (8192, 1088):
         cb, qs, am, x, _, _ = _nf4_case(40, k)
         wobs.wobs_gemv_nf4(qs, am, cb, x)
+    # a codebook entry too small for f16 beside the others takes the float kernel
+    cb, qs, am, x, ref, ad = _nf4_case(40, 8192)
+    cb2 = np.asarray(cb, np.float32).copy()
+    cb2[8] = np.float32(1e-12)
+    wobs.wobs_gemv_nf4(qs, am, cb2, x)
+    monkeypatch.setenv("WOBS_NF4", "cp")
+    wobs.wobs_gemv_nf4(qs, am, cb, x)
     torch.cuda.synchronize()
     err = capfd.readouterr().err
     kernels = [ln.split("kernel=")[1].split()[0] for ln in err.splitlines() if ln.startswith("wobs: op=")]
-    assert kernels == ["nf4_m1_cp", "nf4_m1"], kernels
+    assert kernels == ["nf4_mma", "nf4_m1", "nf4_m1_cp", "nf4_m1_cp"], kernels
 
 
 def test_gemv_nf4_deterministic():

@@ -162,6 +162,11 @@ int max_resident_ctas(const void* kernel, int block, int smem) {
 
 int forced_splits() { return env_splits(); }
 
+bool nf4_cp_forced() {
+  const char* v = std::getenv("WOBS_NF4");
+  return v && std::strcmp(v, "cp") == 0;
+}
+
 bool m1_ldg_forced() {
   const char* v = std::getenv("WOBS_M1");
   return v && std::strcmp(v, "ldg") == 0;

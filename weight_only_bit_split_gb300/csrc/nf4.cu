@@ -396,6 +396,14 @@ cudaError_t run(const uint8_t* qs, const float* absmax, const Codebook16& cb, co
 cudaError_t launch_gemv_nf4(const uint8_t* qs, const float* absmax, const Codebook16& cb,
                             const void* x, void* y, int N, int K, const ArgmaxArgs& am,
                             cudaStream_t st, Launch* info) {
+  // tensor-core variant first (K of 1, 2, 4 or 8 thousand, an f16-exact
+  // scaled codebook, 16-byte aligned planes); WOBS_NF4=cp selects the
+  // CUDA-core staged variant instead
+  if (!m1_ldg_forced() && !nf4_cp_forced()) {
+    cudaError_t e = launch_nf4_mma(qs, absmax, cb, x, y, N, K, am, st, info);
+    if (e != cudaErrorNotSupported) return e;
+    cudaGetLastError();
+  }
   // staged variant: K of 1, 2, 4 or 8 whole 1024-element slices, 16-byte
   // aligned scale rows and activations
   const bool cp = (K == 1024 || K == 2048 || K == 4096 || K == 8192) &&

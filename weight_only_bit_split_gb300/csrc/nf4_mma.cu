@@ -1,0 +1,561 @@
+// NF4 blockwise 4-bit decode GEMV, M = 1, with the products on the tensor
+// cores.
+//
+// bitsandbytes issue #1842 ("70B 4-bit LLM decode bottlenecked by HIP kernel
+// (kgemm_4bit_inference_naive) efficiency"): the fused 4-bit inference GEMV
+// for one decode token, 64-element blocks with a float absmax each, codes
+// looked up in a 16-entry codebook.  On this GPU the CUDA-core form of that
+// kernel is bound by its codebook lookups, not by DRAM: one shared-memory
+// table read per code pair, and the float FMAs behind it, for each half
+// byte of weight stream.  This variant moves the multiply-adds to mma.sync
+// and splits the lookups between two pipes:
+//
+//   * codes decode to f16 pairs.  The codebook is scaled by a power of two
+//     (so its largest entry lies in [2^14, 2^15)) and rounded to f16 once:
+//     each weight carries a relative rounding error of at most 2^-11 and the
+//     scale comes back out exactly in f32.  The activations are scaled the
+//     same way per warp slice and are exact in f16;
+//   * half of the code words go through a 256-entry byte -> f16-pair table in
+//     shared memory, laid out so lane l always reads bank l (one wavefront
+//     per warp lookup, whatever the codes); the other half go through
+//     byte-permute lookups in four registers of low bytes and four of high
+//     bytes (21 integer instructions per 8 codes, no memory traffic);
+//   * a decoded byte is already an A-fragment register (two consecutive
+//     codes of one row), so one m16n8k16 MMA covers 16 rows x 16 codes.  The
+//     four MMAs of a 64-element block accumulate in f32 and the block sum is
+//     scaled by its absmax in f32, as in the format's definition;
+//   * a CTA takes blocks of 64 rows and streams each through a ring of
+//     shared-memory stages of 64 rows x 1024 codes plus their absmax, each
+//     filled by five 2-D tensor copies (128-byte x 64-row code boxes in the
+//     128-byte swizzle) that one producer warp issues.  Each of the 16
+//     compute warps owns 32 rows and two 64-code blocks of every stage; the
+//     activation fragments, converted once, sit in the unused halves of the
+//     table's 256-byte entry strides.  When the last stage of a row block is
+//     released, the producer adds the 8 K-group partials of each row in a
+//     fixed order and writes the outputs;
+//   * MMA row i of a row tile is box row 2i (i < 8) or 2(i - 8) + 1, so the
+//     8-byte code reads of a half warp meet four distinct swizzle phases and
+//     no bank twice;
+//   * the table lives at shared-window address 0x20000, so the lookup
+//     address of a byte is one byte permute of the code word and a constant
+//     (0x20000 | lane * 4), with no add.
+#include <cmath>
+#include <cstdlib>
+
+#include "common.cuh"
+#include "tcgen05.cuh"
+
+namespace wobs {
+namespace {
+
+constexpr int kCW = 16;                      // compute warps: 2 row halves x 8 K groups
+constexpr int kThreads = (kCW + 1) * 32;     // + the producer warp
+constexpr int kRB = 64;                      // rows per row block
+constexpr int kKG = 8;                       // K groups (two 64-code blocks each per stage)
+constexpr uint32_t kTabAddr = 0x20000;       // shared-window address of the table
+constexpr int kTabBytes = 256 * 256;         // entry e: 64 words at e * 256, lane l reads word l;
+                                             // bytes 128..255 of entry c hold activation block c
+constexpr int kMaxStages = 4;
+constexpr int kMiscBytes = 512;              // barriers, counters, codebook, argmax keys
+constexpr int kRedBytes = kMaxStages * kKG * kRB * 4;
+// A stage: 64 rows x 1024 codes (four 128-byte x 64-row code boxes in the
+// 128-byte swizzle, 8 KB each) and their 16 absmax per row (4 KB).
+constexpr int kKS = 1024;                    // codes per row per stage
+constexpr int kStage = 4 * 8192 + kRB * 64;  // 36864 bytes, a multiple of 1024
+constexpr uint32_t kStageTx = kStage;
+
+// PTX prmt, default mode: selector nibble bits 0-2 pick one of the eight
+// source bytes, bit 3 replicates that byte's sign bit over the result byte.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+               :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Codebook held as byte planes: lo/hi bytes of the f16 entries 0..7 (A) and
+// 8..15 (B), two registers each.
+struct Planes {
+  uint32_t la0, la1, lb0, lb1, ha0, ha1, hb0, hb1;
+};
+
+// One code word (4 bytes, 8 codes; byte j = element 2j in its high nibble,
+// element 2j + 1 in its low nibble) -> four f16 pairs, low half = the even
+// element.  Table variant: one lookup per byte.
+// `tl` = kTabAddr | lane * 4: byte e of the word addresses table word
+// e * 64 + lane, i.e. kTabAddr | e << 8 | lane << 2.
+__device__ __forceinline__ void decode_table(uint32_t w, uint32_t tl, uint32_t (&r)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) r[j] = lds32(prmt(w, tl, 0x7604u | (j << 4)));
+}
+
+// Register variant: the low 3 bits of each code select a byte in the A and B
+// planes, the high bit (spread to a byte mask by sign replication) picks A or
+// B, and byte permutes pair the low and high bytes into f16 values.
+__device__ __forceinline__ void decode_planes(uint32_t w, const Planes& p, uint32_t (&r)[4]) {
+  const uint32_t s = w & 0x77777777u;
+  const uint32_t w4 = w << 4;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t sel = h ? (s >> 16) : s;
+    const uint32_t m = prmt(w4, w, h ? 0xFBEAu : 0xD9C8u);   // byte i = 0xFF where code i >= 8
+    const uint32_t la = prmt(p.la0, p.la1, sel), lb = prmt(p.lb0, p.lb1, sel);
+    const uint32_t ha = prmt(p.ha0, p.ha1, sel), hb = prmt(p.hb0, p.hb1, sel);
+    const uint32_t lo = (la & ~m) | (lb & m);
+    const uint32_t hi = (ha & ~m) | (hb & m);
+    r[2 * h] = prmt(lo, hi, 0x4051u);
+    r[2 * h + 1] = prmt(lo, hi, 0x6273u);
+  }
+}
+
+// Power-of-two scale 2^(141 - E) for a positive float with biased exponent E
+// (clamped to [15, 254]): brings the value into [2^14, 2^15); `inv` is its
+// exact inverse.
+__device__ __forceinline__ void pow2_scale(float m, float& scale, float& inv) {
+  int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu);
+  e = e < 15 ? 15 : e;
+  scale = __uint_as_float(static_cast<uint32_t>(268 - e) << 23);
+  inv = __uint_as_float(static_cast<uint32_t>(e - 14) << 23);
+}
+
+// Shared-memory layout, from the dynamic base `base` (same in every CTA):
+// [base, +512) misc, [+512, +512 + kRedBytes) warp partials, then 1024-byte
+// aligned stage slots up to the table at 0x20000, the table [0x20000,
+// 0x30000), then more stage slots up to the end of the allocation.
+struct Layout {
+  uint32_t base, red, a0, b0;
+  int na, S;
+};
+__device__ __forceinline__ Layout make_layout(uint32_t base, uint32_t bytes) {
+  Layout L;
+  L.base = base;
+  L.red = base + kMiscBytes;
+  L.a0 = (L.red + kRedBytes + 1023u) & ~1023u;
+  L.b0 = kTabAddr + kTabBytes;
+  const uint32_t end = base + bytes;
+  L.na = L.a0 <= kTabAddr ? static_cast<int>((kTabAddr - L.a0) / kStage) : -1;
+  const int nb = end >= L.b0 ? static_cast<int>((end - L.b0) / kStage) : -1;
+  L.S = (L.na < 0 || nb < 0) ? 0 : (L.na + nb < kMaxStages ? L.na + nb : kMaxStages);
+  return L;
+}
+__device__ __forceinline__ uint32_t slot_addr(const Layout& L, int s) {
+  return s < L.na ? L.a0 + s * kStage : L.b0 + (s - L.na) * kStage;
+}
+
+// Warps 0..15 compute (row half warp & 1, K group warp >> 1), warp 16
+// produces.  A CTA takes row blocks blockIdx.x, + gridDim.x, ...; each row
+// block streams K in stages of 1024 codes.
+template <int P, bool kArgmax>
+__global__ void __launch_bounds__(kThreads, 1) nf4_mma_kernel(const __grid_constant__ CUtensorMap tq,
+                                                             const __grid_constant__ CUtensorMap ta,
+                                                             Codebook16 cb, float cb_scale,
+                                                             float cb_inv,
+                                                             const __nv_bfloat16* __restrict__ x,
+                                                             __nv_bfloat16* __restrict__ y, int N,
+                                                             int K, uint32_t smem_bytes,
+                                                             ArgmaxArgs am, int* err) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t base = smem_addr(smem);
+  const Layout L = make_layout(base, smem_bytes);
+  auto gen = [&](uint32_t a) { return smem + (a - base); };
+  uint64_t* full = reinterpret_cast<uint64_t*>(gen(base));              // [8]
+  uint64_t* empty = full + kMaxStages;                                   // [8]
+  unsigned* nissue = reinterpret_cast<unsigned*>(gen(base + 128));       // [8]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gen(base + 160));
+  uint16_t* cbh = reinterpret_cast<uint16_t*>(gen(base + 192));          // [16]
+  float* wmax = reinterpret_cast<float*>(gen(base + 224));               // [8] (16 halves)
+  uint64_t* keys = reinterpret_cast<uint64_t*>(gen(base + 288));         // [17], to base + 424
+  float* red = reinterpret_cast<float*>(gen(L.red));                     // [S][8 K groups][64 rows]
+  const int S = L.S;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int spb = K / kKS;                  // stages per row block
+  const int nblk = (N + kRB - 1) / kRB;
+  const int T = static_cast<int>(blockIdx.x) < nblk
+                    ? (nblk - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                    : 0;
+  const int total = T * spb;                // stages this CTA streams
+  if (S < 2) {                              // the table cannot sit at 0x20000: refuse, touch nothing
+    if (tid == 0 && err) atomicExch(err, kErrGemvWait);
+    return;
+  }
+
+  // stage j (row block j / spb, K part j % spb) -> slot j % S; lane 0 of the
+  // producer warp calls it
+  auto issue = [&](int j) {
+    const int s = j % S;
+    const uint32_t st = slot_addr(L, s);
+    const int row0 = (static_cast<int>(blockIdx.x) + (j / spb) * static_cast<int>(gridDim.x)) * kRB;
+    const int k0 = (j % spb) * (kKS / 2);   // byte column of the codes
+    nissue[s] += 1u;
+    mbar_expect_tx(full + s, kStageTx);
+#pragma unroll
+    for (int bx = 0; bx < 4; ++bx) tma_load_2d(st + bx * 8192, &tq, k0 + bx * 128, row0, full + s);
+    tma_load_2d(st + 4 * 8192, &ta, (j % spb) * (kKS / 64), row0, full + s);
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, kCW);
+    }
+    mbar_fence_init();
+    *abort_flag = 0;
+  }
+  if (tid < kMaxStages) nissue[tid] = 0u;
+  if (tid < 16) {
+    float v = cb.v[0];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) v = tid == i ? cb.v[i] : v;
+    cbh[tid] = __half_as_ushort(__float2half_rn(v * cb_scale));
+  }
+  __syncthreads();
+  if (tid == kCW * 32)
+    for (int j = 0; j < S && j < total; ++j) issue(j);
+  pdl_launch_dependents();
+
+  Planes pl;
+  if (warp < kCW) {
+    // the codebook as the shared table (every entry's 32 lane words) and as
+    // byte planes
+    for (int i = tid; i < 256 * 32; i += kCW * 32) {
+      const int e = i >> 5, l = i & 31;
+      sts32(kTabAddr + e * 256 + l * 4,
+            static_cast<uint32_t>(cbh[e >> 4]) | (static_cast<uint32_t>(cbh[e & 15]) << 16));
+    }
+    auto lob = [&](int i) { return static_cast<uint32_t>(cbh[i] & 0xFFu); };
+    auto hib = [&](int i) { return static_cast<uint32_t>(cbh[i] >> 8); };
+    pl.la0 = lob(0) | lob(1) << 8 | lob(2) << 16 | lob(3) << 24;
+    pl.la1 = lob(4) | lob(5) << 8 | lob(6) << 16 | lob(7) << 24;
+    pl.lb0 = lob(8) | lob(9) << 8 | lob(10) << 16 | lob(11) << 24;
+    pl.lb1 = lob(12) | lob(13) << 8 | lob(14) << 16 | lob(15) << 24;
+    pl.ha0 = hib(0) | hib(1) << 8 | hib(2) << 16 | hib(3) << 24;
+    pl.ha1 = hib(4) | hib(5) << 8 | hib(6) << 16 | hib(7) << 24;
+    pl.hb0 = hib(8) | hib(9) << 8 | hib(10) << 16 | hib(11) << 24;
+    pl.hb1 = hib(12) | hib(13) << 8 | hib(14) << 16 | hib(15) << 24;
+  }
+  pdl_wait();
+  // activations -> f16 in the table's gaps, block c at kTabAddr + c * 256 +
+  // 128 (elements in order), all scaled by one power of two that puts max|x|
+  // in [2^14, 2^15): the maximum first (warp w takes blocks w, w + 16, ...),
+  // then the conversion
+  const int nbk = K / 64;
+  if (warp < kCW) {
+    float mx = 0.f;
+    for (int c = warp; c < nbk; c += kCW) {
+      const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(x + c * 64) + lane);
+      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(v << 16)), fabsf(__uint_as_float(v & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) wmax[warp] = mx;
+  }
+  __syncthreads();
+  float xs, xinv;
+  {
+    float mx = 0.f;
+#pragma unroll
+    for (int w2 = 0; w2 < kCW; ++w2) mx = fmaxf(mx, wmax[w2]);
+    pow2_scale(mx, xs, xinv);
+  }
+  if (warp < kCW) {
+    for (int c = warp; c < nbk; c += kCW) {
+      const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(x + c * 64) + lane);
+      const __half2 h2 = __floats2half2_rn(__uint_as_float(v << 16) * xs,
+                                           __uint_as_float(v & 0xFFFF0000u) * xs);
+      sts32(kTabAddr + c * 256 + 128 + 4 * lane, *reinterpret_cast<const uint32_t*>(&h2));
+    }
+  }
+  __syncthreads();                          // table and activation blocks complete
+
+  uint64_t best = 0;
+  bool ok = true;
+  if (warp < kCW) {
+    // ------------------------------------------------------------ compute
+    const int rh = warp & 1, q = warp >> 1;
+    const uint32_t tl = kTabAddr | (static_cast<uint32_t>(lane) << 2);
+    const float out_mul = xinv * cb_inv;
+    // rows of MMA row g in row tile u: 32 rh + 16 u + 2g, and + 1 for MMA
+    // row g + 8.  This lane's 8 code bytes of block b of a row: logical
+    // 16-byte chunk 4 (q & 1) + 2b + t / 2 of box q / 2, stored at chunk ^
+    // (row & 7); the odd row's chunk differs by one in bit 0.
+    const int r0 = 32 * rh + 2 * g;
+    const uint32_t swz = (2 * g) & 7;
+    uint32_t co[2][2];                      // [block][row parity] byte offsets in the stage
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const uint32_t c = 4 * (q & 1) + 2 * b + (t >> 1);
+      co[b][0] = (q >> 1) * 8192 + r0 * 128 + ((c ^ swz) << 4) + 8 * (t & 1);
+      co[b][1] = (q >> 1) * 8192 + (r0 + 1) * 128 + ((c ^ swz ^ 1u) << 4) + 8 * (t & 1);
+    }
+    const uint32_t abs_off = 4 * 8192 + r0 * 64 + 8 * q;
+    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};   // [row tile][row parity]
+    int s = 0, ks = 0;
+    uint32_t ph = 0;
+    uint32_t st = slot_addr(L, 0);
+    for (int j = 0; j < total; ++j) {
+      if (*abort_flag) break;
+      if (!mbar_wait(full + s, ph)) {
+        ok = false;
+        *abort_flag = 1;
+        break;
+      }
+      float am[2][2][2];                    // [row tile][row parity][block]
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int p2 = 0; p2 < 2; ++p2) {
+          const uint2 a = lds64(st + abs_off + (16 * u + p2) * 64);
+          am[u][p2][0] = __uint_as_float(a.x);
+          am[u][p2][1] = __uint_as_float(a.y);
+        }
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t xa = kTabAddr + (ks * 16 + 2 * q + b) * 256 + 128 + 32 * t;
+        const uint4 xv0 = lds128(xa), xv1 = lds128(xa + 16);
+        const uint32_t xf[8] = {xv0.x, xv0.y, xv0.z, xv0.w, xv1.x, xv1.y, xv1.z, xv1.w};
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint2 wg = lds64(st + co[b][0] + u * 16 * 128);
+          const uint2 wh = lds64(st + co[b][1] + u * 16 * 128);
+          const uint32_t words[4] = {wg.x, wg.y, wh.x, wh.y};
+          uint32_t r[4][4];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            if (qq >= 4 - P) decode_planes(words[qq], pl, r[qq]);
+            else decode_table(words[qq], tl, r[qq]);
+          }
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            // MMA m: bytes 2m, 2m + 1 of the lane's 8 bytes of both rows
+            const int wq = m >> 1, jj = 2 * (m & 1);
+            const uint32_t a[4] = {r[wq][jj], r[2 + wq][jj], r[wq][jj + 1], r[2 + wq][jj + 1]};
+            mma16816(d, a, xf[2 * m], xf[2 * m + 1]);
+          }
+          acc[u][0] = fmaf(am[u][0][b], d[0], acc[u][0]);
+          acc[u][1] = fmaf(am[u][1][b], d[2], acc[u][1]);
+        }
+      }
+      if (ks == spb - 1) {
+        // row block complete for this warp: its row partials, then a fresh start
+        if (t == 0) {
+          float* rs = red + (s * kKG + q) * kRB + r0;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            rs[16 * u] = acc[u][0] * out_mul;
+            rs[16 * u + 1] = acc[u][1] * out_mul;
+            acc[u][0] = acc[u][1] = 0.f;
+          }
+        } else {
+          acc[0][0] = acc[0][1] = acc[1][0] = acc[1][1] = 0.f;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(empty + s);
+      if (++ks == spb) ks = 0;
+      if (++s == S) { s = 0; ph ^= 1u; }
+      st = slot_addr(L, s);
+    }
+  } else {
+    // ----------------------------------------------------------- produce
+    int s = 0;
+    uint32_t ph = 0;
+    for (int j = 0; j < total; ++j) {
+      if (*abort_flag) break;
+      if (!mbar_wait(empty + s, ph)) {
+        ok = false;
+        *abort_flag = 1;
+        break;
+      }
+      if (j % spb == spb - 1) {
+        // every compute warp has left its partials of this row block in slot s:
+        // rows lane and lane + 32, K groups added in order
+        const int row0 = (static_cast<int>(blockIdx.x) + (j / spb) * static_cast<int>(gridDim.x)) * kRB;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int rr = lane + 32 * hh, row = row0 + rr;
+          if (row < N) {
+            const float* rs = red + s * kKG * kRB + rr;
+            float v = rs[0];
+#pragma unroll
+            for (int q2 = 1; q2 < kKG; ++q2) v += rs[q2 * kRB];
+            const __nv_bfloat16 o = __float2bfloat16_rn(v);
+            y[row] = o;
+            if (kArgmax) {
+              const uint64_t k = argmax_key(__bfloat162float(o), static_cast<uint32_t>(row));
+              best = k > best ? k : best;
+            }
+          }
+        }
+        __syncwarp();
+      }
+      if (j + S < total && lane == 0) issue(j + S);
+      __syncwarp();
+      if (++s == S) { s = 0; ph ^= 1u; }
+    }
+  }
+  if (!ok && lane == 0 && err) atomicExch(err, kErrGemvWait);
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    // let every issued copy land before the CTA's shared memory is released
+    for (int s2 = 0; s2 < S; ++s2)
+      if (nissue[s2] > 0u) mbar_wait(full + s2, (nissue[s2] - 1u) & 1u);
+  }
+  if (kArgmax) {
+    best = warp_max_u64(best);
+    if (lane == 0) keys[warp] = best;
+    __syncthreads();
+    if (tid == 0) {
+      uint64_t k = 0;
+      for (int w2 = 0; w2 <= kCW; ++w2) k = keys[w2] > k ? keys[w2] : k;
+      keys[0] = k;
+    }
+    __syncthreads();
+    argmax_publish(keys, 1, am, gridDim.x);
+  }
+}
+
+// 2-D tensor map over a row-major [rows][cols] matrix (row pitch `ld`
+// bytes), no fill beyond the edges other than zeros.
+bool make_map(CUtensorMap* map, CUtensorMapDataType type, int esize, const void* ptr, int64_t cols,
+              int64_t rows, int64_t ld, int box_cols, int box_rows, CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  (void)esize;
+  return fn(map, type, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int P, bool kArgmax>
+cudaError_t run_p(const uint8_t* qs, const float* absmax, const Codebook16& cb, float cb_scale,
+                  float cb_inv, const void* x, void* y, int N, int K, const ArgmaxArgs& am,
+                  cudaStream_t st, Launch* info) {
+  auto kern = nf4_mma_kernel<P, kArgmax>;
+  // all the opt-in shared memory the static part leaves, set up once (-1 if
+  // the attribute calls fail)
+  static const int smem = [&] {
+    cudaFuncAttributes fa;
+    int dev = 0, optin = 0;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return -1;
+    const int bytes = optin - static_cast<int>(fa.sharedSizeBytes);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+      return -1;
+    return bytes;
+  }();
+  // the allocation must reach past the table at 0x20000 (two stages fit below it)
+  if (smem < static_cast<int>(kTabAddr + kTabBytes)) {
+    cudaGetLastError();
+    return cudaErrorNotSupported;
+  }
+  CUtensorMap tq, ta;
+  if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qs, K / 2, N, K / 2, 128, kRB,
+                CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, absmax, K / 64, N, K / 16, 16, kRB,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorNotSupported;
+  const int nblk = (N + kRB - 1) / kRB;
+  int grid = device_sm_count();
+  if (grid > nblk) grid = nblk;
+  info->grid_x = grid;
+  info->block = kThreads;
+  info->smem = smem;
+  info->kernel = "nf4_mma";
+  return launch_k(kern, dim3(grid), dim3(kThreads), smem, st, true, tq, ta, cb, cb_scale, cb_inv,
+                  static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, K,
+                  static_cast<uint32_t>(smem), am, error_word_ptr());
+}
+
+template <bool kArgmax>
+cudaError_t run(const uint8_t* qs, const float* absmax, const Codebook16& cb, float cb_scale,
+                float cb_inv, const void* x, void* y, int N, int K, const ArgmaxArgs& am,
+                cudaStream_t st, Launch* info) {
+  // one code word in four through the register planes balances the table's
+  // shared-memory reads against the integer pipe (WOBS_NF4_P=0..2 overrides)
+  const char* v = std::getenv("WOBS_NF4_P");
+  const int p = v ? std::atoi(v) : 1;
+  if (p == 0) return run_p<0, kArgmax>(qs, absmax, cb, cb_scale, cb_inv, x, y, N, K, am, st, info);
+  if (p == 2) return run_p<2, kArgmax>(qs, absmax, cb, cb_scale, cb_inv, x, y, N, K, am, st, info);
+  return run_p<1, kArgmax>(qs, absmax, cb, cb_scale, cb_inv, x, y, N, K, am, st, info);
+}
+
+}  // namespace
+
+// The f16 codebook is usable when every entry is finite and every nonzero
+// entry, after the power-of-two scale that puts the largest magnitude in
+// [2^14, 2^15), is an f16 normal number (relative rounding error <= 2^-11).
+bool nf4_codebook_scale(const Codebook16& cb, float* scale, float* inv) {
+  float mx = 0.f;
+  for (float v : cb.v) {
+    if (!std::isfinite(v)) return false;
+    mx = std::fmax(mx, std::fabs(v));
+  }
+  if (mx == 0.f) { *scale = 1.f; *inv = 1.f; return true; }
+  int ex;
+  std::frexp(mx, &ex);                    // mx in [2^(ex-1), 2^ex)
+  if (ex < -100 || ex > 100) return false;
+  const float sc = std::ldexp(1.f, 15 - ex);
+  for (float v : cb.v)
+    if (v != 0.f && std::fabs(v) * sc < std::ldexp(1.f, -14)) return false;
+  *scale = sc;
+  *inv = std::ldexp(1.f, ex - 15);
+  return true;
+}
+
+cudaError_t launch_nf4_mma(const uint8_t* qs, const float* absmax, const Codebook16& cb,
+                           const void* x, void* y, int N, int K, const ArgmaxArgs& am,
+                           cudaStream_t st, Launch* info) {
+  float sc, inv;
+  if (!nf4_codebook_scale(cb, &sc, &inv)) return cudaErrorNotSupported;
+  if (reinterpret_cast<uintptr_t>(qs) % 16 || reinterpret_cast<uintptr_t>(absmax) % 16 ||
+      reinterpret_cast<uintptr_t>(x) % 16)
+    return cudaErrorNotSupported;
+  // stages of 1024 codes per row; at most 128 blocks of 64, the activation
+  // blocks the table's gaps hold
+  if (K % kKS != 0 || K > 8192) return cudaErrorNotSupported;
+  return am.out ? run<true>(qs, absmax, cb, sc, inv, x, y, N, K, am, st, info)
+                : run<false>(qs, absmax, cb, sc, inv, x, y, N, K, am, st, info);
+}
+
+}  // namespace wobs
