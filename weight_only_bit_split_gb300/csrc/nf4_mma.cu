@@ -71,21 +71,31 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
+// Shared loads as pure functions of their address, so the compiler may
+// interleave them with the MMAs.  Stage reads stay between the stage's full
+// wait and its release because their addresses come from a value produced
+// after the wait (`launder`) and the release takes the accumulators they
+// feed as inputs.
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  asm("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  asm("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
+}
+__device__ __forceinline__ uint32_t launder(uint32_t v) {
+  uint32_t r;
+  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v) : "memory");
+  return r;
 }
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
@@ -99,11 +109,25 @@ __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
 }
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D = A.B (accumulator from zero)
+__device__ __forceinline__ void mma16816_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                           uint32_t b1) {
+  const float z = 0.f;
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+}
+// Release of a stage once `dep` (the accumulators its reads feed) exists.
+__device__ __forceinline__ void mbar_arrive_after(uint64_t* bar, float d0, float d1, float d2,
+                                                  float d3) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];"
+               :: "r"(smem_addr(bar)), "f"(d0), "f"(d1), "f"(d2), "f"(d3) : "memory");
 }
 
 // Codebook held as byte planes: lo/hi bytes of the f16 entries 0..7 (A) and
@@ -322,7 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_kernel(const __grid_const
       co[b][0] = (q >> 1) * 8192 + r0 * 128 + ((c ^ swz) << 4) + 8 * (t & 1);
       co[b][1] = (q >> 1) * 8192 + (r0 + 1) * 128 + ((c ^ swz ^ 1u) << 4) + 8 * (t & 1);
     }
-    const uint32_t abs_off = 4 * 8192 + r0 * 64 + 8 * q;
+    // absmax box: 64-byte rows in the 64-byte swizzle (16-byte chunk index ^=
+    // (row >> 1) & 3); this lane's pair of K group q is chunk q / 2, half q & 1
+    const uint32_t abs_off = 4 * 8192 + r0 * 64 + ((((q >> 1) ^ g) & 3) << 4) + 8 * (q & 1);
     float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};   // [row tile][row parity]
     int s = 0, ks = 0;
     uint32_t ph = 0;
@@ -334,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_kernel(const __grid_const
         *abort_flag = 1;
         break;
       }
+      st = launder(st);
       float am[2][2][2];                    // [row tile][row parity][block]
 #pragma unroll
       for (int u = 0; u < 2; ++u)
@@ -356,16 +383,18 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_kernel(const __grid_const
           uint32_t r[4][4];
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) {
-            if (qq >= 4 - P) decode_planes(words[qq], pl, r[qq]);
+            // P of every 8 code words (two blocks) through the register planes
+            if (4 * b + qq >= 8 - P) decode_planes(words[qq], pl, r[qq]);
             else decode_table(words[qq], tl, r[qq]);
           }
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          float d[4];
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             // MMA m: bytes 2m, 2m + 1 of the lane's 8 bytes of both rows
             const int wq = m >> 1, jj = 2 * (m & 1);
             const uint32_t a[4] = {r[wq][jj], r[2 + wq][jj], r[wq][jj + 1], r[2 + wq][jj + 1]};
-            mma16816(d, a, xf[2 * m], xf[2 * m + 1]);
+            if (m == 0) mma16816_z(d, a, xf[0], xf[1]);
+            else mma16816(d, a, xf[2 * m], xf[2 * m + 1]);
           }
           acc[u][0] = fmaf(am[u][0][b], d[0], acc[u][0]);
           acc[u][1] = fmaf(am[u][1][b], d[2], acc[u][1]);
@@ -386,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_kernel(const __grid_const
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_cta(empty + s);
+      if (lane == 0) mbar_arrive_after(empty + s, acc[0][0], acc[0][1], acc[1][0], acc[1][1]);
       if (++ks == spb) ks = 0;
       if (++s == S) { s = 0; ph ^= 1u; }
       st = slot_addr(L, s);
@@ -493,7 +522,7 @@ cudaError_t run_p(const uint8_t* qs, const float* absmax, const Codebook16& cb, 
   if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, qs, K / 2, N, K / 2, 128, kRB,
                 CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, absmax, K / 64, N, K / 16, 16, kRB,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
+                CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorNotSupported;
   const int nblk = (N + kRB - 1) / kRB;
   int grid = device_sm_count();
@@ -511,12 +540,13 @@ template <bool kArgmax>
 cudaError_t run(const uint8_t* qs, const float* absmax, const Codebook16& cb, float cb_scale,
                 float cb_inv, const void* x, void* y, int N, int K, const ArgmaxArgs& am,
                 cudaStream_t st, Launch* info) {
-  // one code word in four through the register planes balances the table's
-  // shared-memory reads against the integer pipe (WOBS_NF4_P=0..2 overrides)
+  // code words per 8 decoded through the register planes instead of the
+  // shared table (WOBS_NF4_P = 0..3 overrides the default)
   const char* v = std::getenv("WOBS_NF4_P");
   const int p = v ? std::atoi(v) : 1;
   if (p == 0) return run_p<0, kArgmax>(qs, absmax, cb, cb_scale, cb_inv, x, y, N, K, am, st, info);
   if (p == 2) return run_p<2, kArgmax>(qs, absmax, cb, cb_scale, cb_inv, x, y, N, K, am, st, info);
+  if (p == 3) return run_p<3, kArgmax>(qs, absmax, cb, cb_scale, cb_inv, x, y, N, K, am, st, info);
   return run_p<1, kArgmax>(qs, absmax, cb, cb_scale, cb_inv, x, y, N, K, am, st, info);
 }
 
