@@ -577,8 +577,8 @@ class NF4:
     name = "nf4_gemv_28672x8192"
     n, k = 28672, 8192
     dtype = "f32"
-    kernel = "nf4_m1_cp"
-    kernel_src = "nf4.cu"
+    kernel = "nf4_mma"
+    kernel_src = "nf4_mma.cu"
     workload_id = 3
     launches_per_step = 1
 
