@@ -17,7 +17,8 @@ numerics  exact conversions (fp16/bf16 round-to-nearest-even), rounding,
           units in the last place.
 formats   Q8_1 activation blocks, Q4_0 weight blocks, NF4 blockwise codes and
           the NormalFloat codebook: quantise, pack, unpack, dequantise.
-gemv      the dot products themselves (dense, Q4_0 x Q8_1, NF4), greedy argmax,
+gemv      the dot products themselves (dense, Q4_0 x Q8_1, NF4), greedy argmax
+          and argmin,
           the streaming-read checksum, and the parity bound.
 
 Every function with no independent pin would say "parity unpinned" here; at
@@ -37,6 +38,6 @@ from .formats import (  # noqa: F401
 )
 from .gemv import (  # noqa: F401
     gemv_dense, abs_dot_dense, q4_0_q8_1_blockdots, gemv_q4_0_q8_1,
-    abs_dot_q4_0_q8_1, gemv_nf4, abs_dot_nf4, argmax_rows, xor_words,
+    abs_dot_q4_0_q8_1, gemv_nf4, abs_dot_nf4, argmax_rows, argmin_rows, xor_words,
     parity_bound,
 )

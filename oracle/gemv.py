@@ -136,14 +136,33 @@ def argmax_rows(logits):
     index wins -- the reduction of the ArgCompare discussion ("[WIP]
     ArgCompare Benchmark Results and Performance Analysis", section
     "ArgMax/ArgMin Operations Analysis in real-world AI models": argmax over
-    the vocabulary axis, f32/bf16 in, i64 out).  Inputs must be finite.
+    the vocabulary axis, f16/bf16/f32 in, i64 out).  Infinities are ordered
+    like any other value (a masked logit is -inf); NaN is not allowed.
     """
     lg = _as_cols(np.asarray(logits))
-    assert np.all(np.isfinite(lg)), "argmax_rows: non-finite logits"
+    assert not np.any(np.isnan(lg)), "argmax_rows: NaN input"
     out = np.empty(lg.shape[0], dtype=np.int64)
     for m in range(lg.shape[0]):
         best = lg[m].max()
         out[m] = np.flatnonzero(lg[m] == best)[0]
+    return out
+
+
+def argmin_rows(values):
+    """Argmin of each row of ``values`` (M, N): int64 (M,).
+
+    The ArgCompare discussion covers argmin beside argmax (same page, the
+    "Vector Quantization" and "Image Retrieval" rows: argmin over the last
+    axis, f32 in, i64 out).  The smallest value wins; among equal values
+    (-0.0 equals +0.0) the lowest index wins; infinities are ordered, NaN is
+    not allowed.
+    """
+    v = _as_cols(np.asarray(values))
+    assert not np.any(np.isnan(v)), "argmin_rows: NaN input"
+    out = np.empty(v.shape[0], dtype=np.int64)
+    for m in range(v.shape[0]):
+        least = v[m].min()
+        out[m] = np.flatnonzero(v[m] == least)[0]
     return out
 
 

@@ -150,3 +150,48 @@ def test_xor_words_is_order_free_and_self_inverse():
         acc ^= int(wv)
     assert acc == x
     assert int(oracle.xor_words(np.concatenate([b, b]))) == 0
+
+
+def _row(vals):
+    return np.asarray([float(v) for v in vals], dtype=np.float32)
+
+
+def test_argmin_hand_cases():
+    for case in load("argmin_cases.json")["cases"]:
+        assert oracle.argmin_rows(_row(case["row"]))[0] == case["argmin"], case["why"]
+
+
+def test_argmax_infinities():
+    for case in load("argmin_cases.json")["argmax_inf_cases"]:
+        assert oracle.argmax_rows(_row(case["row"]))[0] == case["argmax"], case["why"]
+
+
+def _scan(row, better):
+    # a first-principles scan: keep the first element, replace it only by a
+    # strictly better one, so the lowest index of the best value survives
+    bi = 0
+    for i in range(1, len(row)):
+        if better(float(row[i]), float(row[bi])):
+            bi = i
+    return bi
+
+
+def test_argmax_argmin_brute_force_with_many_ties():
+    rng = np.random.default_rng(11)
+    for n in (1, 2, 3, 7, 33, 100):
+        # few distinct values (ties everywhere), signed zeros and infinities mixed in
+        pool = np.asarray([-np.inf, -2.0, -0.0, 0.0, 1.5, 3.0, np.inf], np.float32)
+        rows = pool[rng.integers(0, len(pool), size=(20, n))]
+        amax, amin = oracle.argmax_rows(rows), oracle.argmin_rows(rows)
+        for m in range(rows.shape[0]):
+            assert amax[m] == _scan(rows[m], lambda a, b: a > b)
+            assert amin[m] == _scan(rows[m], lambda a, b: a < b)
+
+
+def test_argmin_is_argmax_of_the_negation():
+    rng = np.random.default_rng(12)
+    v = rng.integers(-5, 6, size=(64, 257)).astype(np.float32)   # many ties
+    v[3, :] = 0.0
+    v[3, 100] = -0.0                                               # -0 and +0 tie
+    assert np.array_equal(oracle.argmin_rows(v), oracle.argmax_rows(-v))
+    assert oracle.argmin_rows(v)[3] == 0
