@@ -724,11 +724,102 @@ class LmHead:
         return nbytes
 
 
+class ArgCmp:
+    """Standalone argmax / argmin over rows of the ArgCompare discussion's
+    model table: LLaMA-3-8B vocabulary rows at batch 1 and 32 (bf16), a
+    256000-entry Gemma row (bf16) and the Image Retrieval argmin over
+    [32, 1M] f32."""
+    name = "argcompare_rows"
+    cases = (("llama3_b1", 1, 128000, torch.bfloat16, False),
+             ("llama3_b32", 32, 128000, torch.bfloat16, False),
+             ("gemma_b1", 1, 256000, torch.bfloat16, False),
+             ("retrieval_argmin", 32, 1048576, torch.float32, True))
+    dtype = "f32"
+    kernel = "argcmp_cta"
+    kernel_src = "argcmp.cu"
+    workload_id = 6
+    launches_per_step = 4
+
+    def __init__(self, device):
+        import weight_only_bit_split_gb300 as wobs
+        from weight_only_bit_split_gb300 import synth
+        self.wobs = wobs
+        self.copies = max(1, math.ceil(ROTATE_BYTES / self.bytes_per_step()))
+        self.X = [[synth.normal((m, n), 1.0, synth.seed_of(self.workload_id, 2, c), device=device,
+                                dtype=dt) for _, m, n, dt, _ in self.cases] for c in range(self.copies)]
+        self.out = [torch.empty(m, dtype=torch.int64, device=device) for _, m, _, _, _ in self.cases]
+        self.ws = [torch.zeros(max(16, wobs.wobs_workspace_size(wobs.OP_ARGCMP, m, n,
+                                                                torch.empty(0, dtype=dt).element_size())),
+                               dtype=torch.uint8, device=device) for _, m, n, dt, _ in self.cases]
+
+    @classmethod
+    def call_bytes(cls, i):
+        _, m, n, dt, _ = cls.cases[i]
+        return m * n * torch.empty(0, dtype=dt).element_size() + 8 * m
+
+    @classmethod
+    def bytes_per_step(cls):
+        return sum(cls.call_bytes(i) for i in range(len(cls.cases)))
+
+    def _call(self, c, i):
+        f = self.wobs.wobs_argmin if self.cases[i][4] else self.wobs.wobs_argmax
+        f(self.X[c][i], out=self.out[i], ws=self.ws[i])
+
+    def step(self, c):
+        for i in range(len(self.cases)):
+            self._call(c, i)
+
+    def kernel_calls(self):
+        return [(self.cases[i][0], self.call_bytes(i), lambda c, i=i: self._call(c, i))
+                for i in range(len(self.cases))]
+
+    def e2e_setup(self):
+        # the rows come from the host (pinned) and the indices go back each step
+        self.xh = [x.cpu().pin_memory() for x in self.X[0]]
+        self.oh = [torch.empty(o.shape, dtype=torch.int64).pin_memory() for o in self.out]
+        return (sum(x.numel() * x.element_size() for x in self.xh),
+                sum(o.numel() * 8 for o in self.oh))
+
+    def e2e_step(self, c):
+        for i in range(len(self.cases)):
+            self.X[c][i].copy_(self.xh[i], non_blocking=True)
+            self._call(c, i)
+            self.oh[i].copy_(self.out[i], non_blocking=True)
+
+    def config(self):
+        return {"workload": self.name,
+                "rows": [f"{name} [{m}, {n}] {str(dt).replace('torch.', '')} "
+                         f"{'argmin' if mn else 'argmax'}" for name, m, n, dt, mn in self.cases],
+                "row_copies": self.copies,
+                "working_set_gb": round(self.copies * self.bytes_per_step() / 1e9, 3),
+                "l2": "inputs larger than L2: rotated copies of the rows, working set above 1 GB"}
+
+    @classmethod
+    def oracle_prepare(cls, frac):
+        from weight_only_bit_split_gb300 import synth
+        prep = []
+        for _, m, n, dt, mn in cls.cases:
+            rows = max(1, int(round(m * frac))) if m > 1 else 1
+            cols = n if m > 1 else max(1, int(round(n * frac)))
+            x = synth.normal((rows, cols), 1.0, synth.seed_of(cls.workload_id, 2, 0), dtype=dt)
+            prep.append((x.float().numpy(), mn, dt))
+        return prep
+
+    @classmethod
+    def oracle_step(cls, prep):
+        import oracle
+        nbytes = 0
+        for x, mn, dt in prep:
+            (oracle.argmin_rows if mn else oracle.argmax_rows)(x)
+            nbytes += x.size * torch.empty(0, dtype=dt).element_size() + 8 * x.shape[0]
+        return nbytes
+
+
 WORKLOADS = {"q4_m1": Q4M1, "q4_m_sweep": Q4Sweep, "fp16_4096": DenseF16, "nf4": NF4,
-             "lm_head": LmHead}
+             "lm_head": LmHead, "argcmp": ArgCmp}
 # oracle row fraction per step (bounds the CPU time of one oracle step)
 ORACLE_FRACTION = {"q4_m1": 0.125, "q4_m_sweep": 1 / 64, "fp16_4096": 0.5, "nf4": 1 / 32,
-                   "lm_head": 1 / 256}
+                   "lm_head": 1 / 256, "argcmp": 1 / 4}
 
 
 def oracle_rate(cls, frac, min_seconds, max_steps=None):

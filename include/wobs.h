@@ -43,6 +43,8 @@
  *     workspace must be sized for it with the same variable set);
  *     WOBS_TC=0 keeps dense GEMVs off the tcgen05 kernel and WOBS_M1=ldg
  *     selects the direct-load M = 1 kernels (both for testing).
+ *     WOBS_SPLITK=<s> also forces <s> slices per row on wobs_argmax /
+ *     wobs_argmin.
  */
 #ifndef WOBS_H
 #define WOBS_H
@@ -74,6 +76,12 @@ extern "C" {
 #define WOBS_OP_GEMV_BF16 2
 #define WOBS_OP_GEMV_Q4_0_Q8_1 3
 #define WOBS_OP_GEMV_NF4 4
+#define WOBS_OP_ARGCMP 5     /* wobs_argmax / wobs_argmin; K = element bytes */
+
+/* ---- element types of wobs_argmax / wobs_argmin ---- */
+#define WOBS_DTYPE_F16 1
+#define WOBS_DTYPE_BF16 2
+#define WOBS_DTYPE_F32 3
 
 /* Largest activation-column count of the multi-column entry points. */
 #define WOBS_MAX_M 32
@@ -240,9 +248,42 @@ WOBS_API int wobs_gemv_nf4(const uint8_t* qs, const float* absmax, const float* 
                            size_t ws_bytes, void* stream);
 
 /*
+ * Standalone ArgCompare over the rows of a matrix ("[WIP] ArgCompare
+ * Benchmark Results and Performance Analysis", IREE discussion #23609:
+ * argmax over the vocabulary axis, [1..32, 32K..256K] f16/bf16/f32 -> i64,
+ * batched rows up to [4096, 32768], and argmin over [32, 1M] f32, section
+ * "ArgMax/ArgMin Operations Analysis in real-world AI models").
+ *
+ *   wobs_argmax: out[m] = the n of the largest X[m][n]; wobs_argmin: of the
+ *   smallest.  Among equal values the lowest n wins; -0.0 equals +0.0;
+ *   infinities are ordered like other values; a row holding NaN gives an
+ *   unspecified index in 0..N-1.
+ *
+ *   dtype  WOBS_DTYPE_F16, _BF16 or _F32
+ *   X      [M][ldx] elements of dtype, 16-byte aligned, ldx >= N with
+ *          ldx * element size a multiple of 16 bytes (ldx is ignored when
+ *          M == 1); N any value in 1..WOBS_ARGCMP_MAX_N (ragged tails
+ *          included); 1 <= M <= WOBS_ARGCMP_MAX_M
+ *   out    int64 [M], 8-byte aligned
+ *   ws     workspace of wobs_workspace_size(WOBS_OP_ARGCMP, M, N, element
+ *          bytes): zero when one CTA or one warp covers a row (ws may then
+ *          be NULL), else 12 bytes a row (per-row keys and arrival counters,
+ *          zero-filled, left zero-filled after the call).
+ * Errors: INVALID_ARG (null, dtype, M, ldx), UNSUPPORTED_SHAPE (N),
+ * MISALIGNED, WORKSPACE_TOO_SMALL, LAUNCH_FAILED.
+ */
+#define WOBS_ARGCMP_MAX_M (1 << 24)
+#define WOBS_ARGCMP_MAX_N (1 << 30)
+WOBS_API int wobs_argmax(int dtype, const void* X, int64_t ldx, int M, int N, int64_t* out,
+                         void* ws, size_t ws_bytes, void* stream);
+WOBS_API int wobs_argmin(int dtype, const void* X, int64_t ldx, int M, int N, int64_t* out,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Workspace bytes needed by one call of `op` with this shape on the current
  * device (split-K partials and counters, argmax keys and counter).  Returns
- * 0 for an unknown op or a shape that needs none.
+ * 0 for an unknown op or a shape that needs none.  For WOBS_OP_ARGCMP, M
+ * and N are the matrix shape and K the element size in bytes (2 or 4).
  */
 WOBS_API size_t wobs_workspace_size(int op, int M, int N, int K);
 

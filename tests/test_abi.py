@@ -124,3 +124,42 @@ def test_product_codebook_equals_oracle_fixture():
     a = normal_float_levels().numpy()
     b = nf4_codebook_fixture()
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_argcmp_argument_checks():
+    out = FAKE16
+    for name in ("wobs_argmax", "wobs_argmin"):
+        rc, _ = _status(name, 2, None, 64, 1, 64, out, None, 0, None)
+        assert rc == -1                   # null X
+        rc, _ = _status(name, 7, FAKE16, 64, 1, 64, out, None, 0, None)
+        assert rc == -1                   # unknown dtype
+        rc, _ = _status(name, 2, FAKE16, 64, 0, 64, out, None, 0, None)
+        assert rc == -1                   # M = 0
+        rc, _ = _status(name, 2, FAKE16, 64, 1, 0, out, None, 0, None)
+        assert rc == -3                   # N = 0
+        rc, _ = _status(name, 2, FAKE16, 32, 2, 64, out, None, 0, None)
+        assert rc == -1                   # ldx < N
+        rc, _ = _status(name, 2, FAKE_ODD, 64, 1, 64, out, None, 0, None)
+        assert rc == -2                   # X misaligned
+        rc, _ = _status(name, 2, FAKE16, 68, 2, 64, out, None, 0, None)
+        assert rc == -2                   # 68 bf16 = 136-byte pitch breaks 16-byte rows
+        rc, _ = _status(name, 3, FAKE16, 64, 1, 64, ctypes.c_void_p(0x10004), None, 0, None)
+        assert rc == -2                   # out not 8-byte aligned
+
+
+def test_argcmp_workspace_rules(monkeypatch):
+    lib = _lib.get()
+    assert lib.wobs_workspace_size(5, 1, 1000, 3) == 0        # element size must be 2 or 4
+    assert lib.wobs_workspace_size(5, 0, 1000, 2) == 0
+    # a single long row is split, so it needs its key and counter
+    assert lib.wobs_workspace_size(5, 1, 131072, 2) == 16
+    # forcing one slice a row removes the workspace; forcing several adds it
+    monkeypatch.setenv("WOBS_SPLITK", "1")
+    assert lib.wobs_workspace_size(5, 1, 131072, 2) == 0
+    monkeypatch.setenv("WOBS_SPLITK", "3")
+    assert lib.wobs_workspace_size(5, 10, 1000, 4) == (12 * 10 + 15) // 16 * 16
+    # and the call refuses a missing or short workspace before any launch
+    rc, msg = _status("wobs_argmax", 3, FAKE16, 1000, 10, 1000, FAKE16, None, 0, None)
+    assert rc == -1 and "workspace" in msg
+    rc, _ = _status("wobs_argmax", 3, FAKE16, 1000, 10, 1000, FAKE16, FAKE16, 64, None)
+    assert rc == -4

@@ -19,6 +19,8 @@ OP_GEMV_F16 = 1
 OP_GEMV_BF16 = 2
 OP_GEMV_Q4_0_Q8_1 = 3
 OP_GEMV_NF4 = 4
+OP_ARGCMP = 5
+DTYPE_CODES = {torch.float16: 1, torch.bfloat16: 2, torch.float32: 3}
 MAX_M = 32
 Q8_1_BLOCK_BYTES = 36
 
@@ -328,6 +330,35 @@ def wobs_gemv_nf4(qs, absmax, codebook, x, y=None, argmax=None, want_argmax=Fals
                            _stream(qs.device))
     _check(rc, lib)
     return y, argmax
+
+
+def _argcmp(name, X, out, ws):
+    lib = _lib.get()
+    X2 = X if X.dim() == 2 else X.view(1, -1)
+    _need(X2, "X", None, 2)
+    if X2.dtype not in DTYPE_CODES:
+        raise TypeError(f"X: dtype {X2.dtype}, expected float16, bfloat16 or float32")
+    M, N = X2.shape
+    if out is None:
+        out = torch.empty(M, dtype=torch.int64, device=X2.device)
+    _need(out, "out", torch.int64, None, X2.device)
+    if ws is None:
+        need = wobs_workspace_size(OP_ARGCMP, M, N, X2.element_size())
+        ws = workspace(OP_ARGCMP, M, N, X2.element_size(), X2.device) if need else None
+    rc = getattr(lib, name)(DTYPE_CODES[X2.dtype], _ptr(X2), _rows(X2), M, N, _ptr(out), _ptr(ws),
+                            ws.numel() if ws is not None else 0, _stream(X2.device))
+    _check(rc, lib)
+    return out
+
+
+def wobs_argmax(X, out=None, ws=None):
+    """int64 [M]: index of the largest element of each row of X [M, N] (lowest on ties)."""
+    return _argcmp("wobs_argmax", X, out, ws)
+
+
+def wobs_argmin(X, out=None, ws=None):
+    """int64 [M]: index of the smallest element of each row of X [M, N] (lowest on ties)."""
+    return _argcmp("wobs_argmin", X, out, ws)
 
 
 def wobs_q4_0_q8_1_blockdots(qs, xq):

@@ -36,6 +36,10 @@ SIGNATURES = {
                                     c_int, c_void_p, c_size_t, c_void_p]),
     "wobs_gemv_nf4": (c_int, [c_void_p, c_void_p, c_float_p, c_void_p, c_void_p, c_void_p, c_int,
                               c_int, c_void_p, c_size_t, c_void_p]),
+    "wobs_argmax": (c_int, [c_int, c_void_p, c_int64, c_int, c_int, c_void_p, c_void_p, c_size_t,
+                            c_void_p]),
+    "wobs_argmin": (c_int, [c_int, c_void_p, c_int64, c_int, c_int, c_void_p, c_void_p, c_size_t,
+                            c_void_p]),
     "wobs_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
     "wobs_q4_0_q8_1_blockdots": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p,
                                          c_void_p]),

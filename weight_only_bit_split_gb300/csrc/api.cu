@@ -262,6 +262,14 @@ const char* wobs_last_error(void) { return g_err; }
 int wobs_version(void) { return 1; }
 
 size_t wobs_workspace_size(int op, int M, int N, int K) {
+  if (op == WOBS_OP_ARGCMP) {
+    // K carries the element size in bytes (2 or 4)
+    if (M < 1 || M > WOBS_ARGCMP_MAX_M || N < 1 || N > WOBS_ARGCMP_MAX_N || (K != 2 && K != 4))
+      return 0;
+    const wobs::ArgcmpPlan p = wobs::plan_argcmp(K, M, N, env_splits());
+    if (p.warp_rows || p.splits == 1) return 0;
+    return (12ull * M + 15ull) & ~15ull;   // keys [M] (8 bytes), then counters [M] (4 bytes)
+  }
   if (op < WOBS_OP_GEMV_F16 || op > WOBS_OP_GEMV_NF4 || M < 1 || M > WOBS_MAX_M || N < 1 || K < 1)
     return 0;
   return ws_layout(op, M, N, K).total;
@@ -408,6 +416,48 @@ int wobs_gemv_nf4(const uint8_t* qs, const float* absmax, const float* codebook,
   cudaError_t e = wobs::launch_gemv_nf4(qs, absmax, cb, x, y, N, K, p.am,
                                         static_cast<cudaStream_t>(stream), &L);
   return finish_launch(e, "gemv_nf4", 1, N, K, L, 1);
+}
+
+static int argcmp(const char* op, bool is_min, int dtype, const void* X, int64_t ldx, int M, int N,
+                  int64_t* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!X || !out) return fail(WOBS_ERR_INVALID_ARG, "%s: null pointer", op);
+  if (dtype < WOBS_DTYPE_F16 || dtype > WOBS_DTYPE_F32)
+    return fail(WOBS_ERR_INVALID_ARG, "%s: dtype %d (1 fp16, 2 bf16, 3 fp32)", op, dtype);
+  if (M < 1 || M > WOBS_ARGCMP_MAX_M) return fail(WOBS_ERR_INVALID_ARG, "%s: M=%d outside 1..%d", op, M, WOBS_ARGCMP_MAX_M);
+  if (N < 1 || N > WOBS_ARGCMP_MAX_N) return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "%s: N=%d outside 1..%d", op, N, WOBS_ARGCMP_MAX_N);
+  const int es = dtype == WOBS_DTYPE_F32 ? 4 : 2;
+  if (M > 1 && ldx < N) return fail(WOBS_ERR_INVALID_ARG, "%s: ldx < N", op);
+  if (!aligned16(X) || (M > 1 && (ldx * es) % 16))
+    return fail(WOBS_ERR_MISALIGNED, "%s: X rows must be 16-byte aligned", op);
+  if (reinterpret_cast<uintptr_t>(out) & 7u) return fail(WOBS_ERR_MISALIGNED, "%s: out not 8-byte aligned", op);
+  const wobs::ArgcmpPlan p = wobs::plan_argcmp(es, M, N, env_splits());
+  if (!p.warp_rows && static_cast<int64_t>(M) * p.splits > 0x7FFFFFFFll)
+    return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "%s: M x slices exceeds the grid", op);
+  uint64_t* keys = nullptr;
+  unsigned* counters = nullptr;
+  if (!p.warp_rows && p.splits > 1) {
+    const size_t need = (12ull * M + 15ull) & ~15ull;
+    if (!ws) return fail(WOBS_ERR_INVALID_ARG, "%s: workspace required (%zu bytes) but ws is NULL", op, need);
+    if (!aligned16(ws)) return fail(WOBS_ERR_MISALIGNED, "%s: workspace must be 16-byte aligned", op);
+    if (ws_bytes < need)
+      return fail(WOBS_ERR_WORKSPACE_TOO_SMALL, "%s: workspace %zu bytes < %zu needed", op, ws_bytes, need);
+    keys = static_cast<uint64_t*>(ws);
+    counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + 8ull * M);
+  }
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_argcmp(dtype, is_min, X, M > 1 ? ldx : N, M, N, p, out, keys, counters,
+                                      static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, op, M, N, 0, L, p.warp_rows ? 1 : p.splits);
+}
+
+int wobs_argmax(int dtype, const void* X, int64_t ldx, int M, int N, int64_t* out, void* ws,
+                size_t ws_bytes, void* stream) {
+  return argcmp("argmax", false, dtype, X, ldx, M, N, out, ws, ws_bytes, stream);
+}
+
+int wobs_argmin(int dtype, const void* X, int64_t ldx, int M, int N, int64_t* out, void* ws,
+                size_t ws_bytes, void* stream) {
+  return argcmp("argmin", true, dtype, X, ldx, M, N, out, ws, ws_bytes, stream);
 }
 
 int wobs_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, int N, int K, int32_t* out,

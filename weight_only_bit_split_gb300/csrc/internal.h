@@ -81,6 +81,21 @@ cudaError_t launch_gemv_nf4(const uint8_t* qs, const float* absmax, const Codebo
                             const void* x, void* y, int N, int K, const ArgmaxArgs& am,
                             cudaStream_t st, Launch* info);
 
+// Standalone argmax / argmin over the rows of [M][N] (dtype 1 fp16, 2 bf16,
+// 3 fp32).  warp_rows: one warp per row, no workspace; otherwise one CTA per
+// (row, slice of `chunk` elements), `splits` slices a row, and with more than
+// one slice the rows' keys [M] and arrival counters [M] live in the caller's
+// workspace.
+struct ArgcmpPlan {
+  bool warp_rows = false;
+  int splits = 1;
+  int chunk = 0;
+};
+ArgcmpPlan plan_argcmp(int esize, int M, int N, int forced_splits);
+cudaError_t launch_argcmp(int dtype, bool is_min, const void* X, int64_t ldx, int M, int N,
+                          const ArgcmpPlan& p, int64_t* out, uint64_t* keys, unsigned* counters,
+                          cudaStream_t st, Launch* info);
+
 cudaError_t read_and_clear_error_word(cudaStream_t st, int* host_out);
 cudaError_t launch_wait_timeout(long long limit, cudaStream_t st, Launch* info);
 // Device address of the error word on the current device (null if unknown).

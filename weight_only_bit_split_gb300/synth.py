@@ -12,8 +12,10 @@ Recipe: ``torch.Generator(device).manual_seed(seed)`` and ``torch.randn``
 
 The workloads are the decode shapes of the pages: an 8B model's
 projections (4096x4096 q/o, 1024x4096 k/v, 14336x4096 gate/up, 4096x14336
-down), a 70B model's MLP matrix (28672x8192) and a 128000-token vocabulary
-head.  Weights ~ N(0, 0.02^2), activations ~ N(0, 1).
+down), a 70B model's MLP matrix (28672x8192), a 128000-token vocabulary
+head, and the rows of the standalone argmax / argmin (logit rows of 32K to
+262K entries, batched rows, a 1M-entry distance row).  Weights ~ N(0,
+0.02^2), activations and logit rows ~ N(0, 1).
 """
 import torch
 
@@ -32,6 +34,11 @@ WORKLOADS = {
             M=(1, 2, 4, 8, 12, 16, 24, 32)),
     5: dict(name="bf16_lm_head_argmax_128000x4096", fmt="bf16", shapes=[(128000, 4096)],
             M=(1, 32)),
+    # standalone argmax / argmin rows (M, N): vocabulary heads of the ArgCompare
+    # discussion's model table, values ~ N(0, 1) stand in for logits
+    6: dict(name="argcompare_rows", fmt="argcmp",
+            shapes=[(1, 128000), (32, 128000), (1, 262144), (8, 32768), (4096, 8192),
+                    (64, 1048576)], M=()),
 }
 
 
