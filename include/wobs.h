@@ -260,10 +260,10 @@ WOBS_API int wobs_gemv_nf4(const uint8_t* qs, const float* absmax, const float* 
  *   unspecified index in 0..N-1.
  *
  *   dtype  WOBS_DTYPE_F16, _BF16 or _F32
- *   X      [M][ldx] elements of dtype, 16-byte aligned, ldx >= N with
- *          ldx * element size a multiple of 16 bytes (ldx is ignored when
- *          M == 1); N any value in 1..WOBS_ARGCMP_MAX_N (ragged tails
- *          included); 1 <= M <= WOBS_ARGCMP_MAX_M
+ *   X      [M][ldx] elements of dtype, aligned to the element size, any
+ *          pitch ldx >= N (ignored when M == 1): rows need not start on a
+ *          16-byte boundary (the exception to the library's alignment rule);
+ *          N any value in 1..WOBS_ARGCMP_MAX_N; 1 <= M <= WOBS_ARGCMP_MAX_M
  *   out    int64 [M], 8-byte aligned
  *   ws     workspace of wobs_workspace_size(WOBS_OP_ARGCMP, M, N, element
  *          bytes): zero when one CTA or one warp covers a row (ws may then

@@ -140,9 +140,9 @@ def test_argcmp_argument_checks():
         rc, _ = _status(name, 2, FAKE16, 32, 2, 64, out, None, 0, None)
         assert rc == -1                   # ldx < N
         rc, _ = _status(name, 2, FAKE_ODD, 64, 1, 64, out, None, 0, None)
-        assert rc == -2                   # X misaligned
-        rc, _ = _status(name, 2, FAKE16, 68, 2, 64, out, None, 0, None)
-        assert rc == -2                   # 68 bf16 = 136-byte pitch breaks 16-byte rows
+        assert rc == -2                   # bf16 X at an odd address
+        rc, _ = _status(name, 3, ctypes.c_void_p(0x10002), 64, 1, 64, out, None, 0, None)
+        assert rc == -2                   # fp32 X not 4-byte aligned
         rc, _ = _status(name, 3, FAKE16, 64, 1, 64, ctypes.c_void_p(0x10004), None, 0, None)
         assert rc == -2                   # out not 8-byte aligned
 

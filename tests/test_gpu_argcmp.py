@@ -88,6 +88,22 @@ def test_padded_pitch(dtype):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("offset", [1, 3, 5])
+@pytest.mark.parametrize("splits", ["", "7"])
+def test_rows_off_the_16_byte_grid(dtype, offset, splits, monkeypatch):
+    # a row that starts `offset` elements past a 16-byte boundary, odd pitch
+    if splits:
+        monkeypatch.setenv("WOBS_SPLITK", splits)
+    m, n, ld = 6, 3001, 3003
+    flat = rows((m * ld + offset,), 10, dtype, levels=5)
+    view = flat[offset:].view(m, ld)[:, :n]
+    got = wobs.wobs_argmax(flat.to(dev())[offset:].view(m, ld)[:, :n]).cpu().numpy()
+    assert np.array_equal(got, ref(view.contiguous(), False))
+    got = wobs.wobs_argmin(flat.to(dev())[offset:].view(m, ld)[:, :n]).cpu().numpy()
+    assert np.array_equal(got, ref(view.contiguous(), True))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
 def test_signed_zeros_infinities_and_constant_rows(dtype):
     n = 20000
     t = torch.full((6, n), -1.0, dtype=dtype)
@@ -127,6 +143,7 @@ FULL = [((1, 128000), torch.bfloat16, False), ((32, 128000), torch.bfloat16, Fal
         ((1, 262144), torch.bfloat16, False), ((1, 256000), torch.bfloat16, False),
         ((8, 32768), torch.float16, False), ((1, 50257), torch.float32, False),
         ((32, 1024), torch.float32, False), ((4096, 8192), torch.float32, True),
+        ((512, 30522), torch.float32, False),
         ((256, 131072), torch.float32, False), ((64, 1048576), torch.float32, False),
         ((32, 1048576), torch.float32, True)]
 

@@ -427,8 +427,8 @@ static int argcmp(const char* op, bool is_min, int dtype, const void* X, int64_t
   if (N < 1 || N > WOBS_ARGCMP_MAX_N) return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "%s: N=%d outside 1..%d", op, N, WOBS_ARGCMP_MAX_N);
   const int es = dtype == WOBS_DTYPE_F32 ? 4 : 2;
   if (M > 1 && ldx < N) return fail(WOBS_ERR_INVALID_ARG, "%s: ldx < N", op);
-  if (!aligned16(X) || (M > 1 && (ldx * es) % 16))
-    return fail(WOBS_ERR_MISALIGNED, "%s: X rows must be 16-byte aligned", op);
+  if (reinterpret_cast<uintptr_t>(X) % es)
+    return fail(WOBS_ERR_MISALIGNED, "%s: X not aligned to its element size", op);
   if (reinterpret_cast<uintptr_t>(out) & 7u) return fail(WOBS_ERR_MISALIGNED, "%s: out not 8-byte aligned", op);
   const wobs::ArgcmpPlan p = wobs::plan_argcmp(es, M, N, env_splits());
   if (!p.warp_rows && static_cast<int64_t>(M) * p.splits > 0x7FFFFFFFll)

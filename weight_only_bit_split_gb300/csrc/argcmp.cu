@@ -16,7 +16,8 @@
 //     4096 elements a slice); with many short rows, a warp takes a whole
 //     row instead;
 //   * 16-byte read-only loads with an evict-first L2 policy, four in flight
-//     per thread before any compare;
+//     per thread before any compare (rows of any pitch: a scalar head up to
+//     the first 16-byte boundary, a scalar ragged tail);
 //   * each thread keeps its best (value, index) in registers with a strict
 //     compare, so among equal values the first one it met -- its lowest
 //     index -- survives; -0.0 == +0.0 under the IEEE compare;
@@ -77,23 +78,33 @@ __device__ __forceinline__ uint64_t make_key(float best, uint32_t idx) {
   return (static_cast<uint64_t>(~static_cast<uint32_t>(k >> 32)) << 32) | (k & 0xFFFFFFFFull);
 }
 
-// Scan elements [lo, hi) of `row` with `nt` threads (this one is `lt`).
-// lo is a multiple of the vector width; the row start is 16-byte aligned.
+// Scan elements [lo, hi) of `row` with `nt` threads (this one is `lt`), each
+// thread in increasing index order: a scalar head up to the first 16-byte
+// boundary, whole 16-byte vectors, a scalar tail.  `row` is aligned to its
+// element size; any pitch works.
 template <typename T, bool kMin>
 __device__ __forceinline__ void scan(const T* __restrict__ row, int lo, int hi, int lt, int nt,
                                      uint64_t pol, float& best, uint32_t& bi) {
   constexpr int E = Elem<T>::kPerVec;
-  const int v0 = lo / E, v1 = hi / E;     // whole vectors
-  const uint4* rv = reinterpret_cast<const uint4*>(row);
-  for (int v = v0 + lt; v < v1; v += nt * kUnroll) {
+  const int a0 = static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) /
+                                  sizeof(T));   // first element on a 16-byte boundary
+  int vs = lo <= a0 ? a0 : a0 + (lo - a0 + E - 1) / E * E;
+  if (vs > hi) vs = hi;
+  for (int i = lo + lt; i < vs; i += nt) {
+    const float x = Elem<T>::get1(row + i);
+    if (better<kMin>(x, best)) { best = x; bi = static_cast<uint32_t>(i); }
+  }
+  const int nv = (hi - vs) / E;           // whole vectors from vs
+  const uint4* rv = reinterpret_cast<const uint4*>(row + vs);
+  for (int v = lt; v < nv; v += nt * kUnroll) {
     uint4 buf[kUnroll];
 #pragma unroll
     for (int j = 0; j < kUnroll; ++j)
-      if (v + j * nt < v1) buf[j] = ld_stream16(rv + v + j * nt, pol);
+      if (v + j * nt < nv) buf[j] = ld_stream16(rv + v + j * nt, pol);
 #pragma unroll
     for (int j = 0; j < kUnroll; ++j) {
-      if (v + j * nt < v1) {
-        const uint32_t base = static_cast<uint32_t>((v + j * nt) * E);
+      if (v + j * nt < nv) {
+        const uint32_t base = static_cast<uint32_t>(vs + (v + j * nt) * E);
 #pragma unroll
         for (int i = 0; i < E; ++i) {
           const float x = Elem<T>::get(buf[j], i);
@@ -102,8 +113,7 @@ __device__ __forceinline__ void scan(const T* __restrict__ row, int lo, int hi, 
       }
     }
   }
-  // ragged tail of the row (fewer than one vector), in index order
-  for (int i = v1 * E + lt; i < hi; i += nt) {
+  for (int i = vs + nv * E + lt; i < hi; i += nt) {
     const float x = Elem<T>::get1(row + i);
     if (better<kMin>(x, best)) { best = x; bi = static_cast<uint32_t>(i); }
   }
