@@ -15,9 +15,9 @@
 //     that the grid covers every SM at least four times over, never below
 //     4096 elements a slice); with many short rows, a warp takes a whole
 //     row instead;
-//   * 16-byte read-only loads with an evict-first L2 policy, four in flight
+//   * 32-byte read-only loads with an evict-first L2 policy, four in flight
 //     per thread before any compare (rows of any pitch: a scalar head up to
-//     the first 16-byte boundary, a scalar ragged tail);
+//     the first 32-byte boundary, a scalar ragged tail);
 //   * each thread keeps its best (value, index) in registers with a strict
 //     compare, so among equal values the first one it met -- its lowest
 //     index -- survives; -0.0 == +0.0 under the IEEE compare;
@@ -79,15 +79,15 @@ __device__ __forceinline__ uint64_t make_key(float best, uint32_t idx) {
 }
 
 // Scan elements [lo, hi) of `row` with `nt` threads (this one is `lt`), each
-// thread in increasing index order: a scalar head up to the first 16-byte
-// boundary, whole 16-byte vectors, a scalar tail.  `row` is aligned to its
+// thread in increasing index order: a scalar head up to the first 32-byte
+// boundary, whole 32-byte vectors, a scalar tail.  `row` is aligned to its
 // element size; any pitch works.
 template <typename T, bool kMin>
 __device__ __forceinline__ void scan(const T* __restrict__ row, int lo, int hi, int lt, int nt,
                                      uint64_t pol, float& best, uint32_t& bi) {
-  constexpr int E = Elem<T>::kPerVec;
-  const int a0 = static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(row) & 15u)) & 15u) /
-                                  sizeof(T));   // first element on a 16-byte boundary
+  constexpr int E = 2 * Elem<T>::kPerVec;  // elements per 32-byte vector
+  const int a0 = static_cast<int>(((32u - (reinterpret_cast<uintptr_t>(row) & 31u)) & 31u) /
+                                  sizeof(T));   // first element on a 32-byte boundary
   int vs = lo <= a0 ? a0 : a0 + (lo - a0 + E - 1) / E * E;
   if (vs > hi) vs = hi;
   for (int i = lo + lt; i < vs; i += nt) {
@@ -97,19 +97,21 @@ __device__ __forceinline__ void scan(const T* __restrict__ row, int lo, int hi, 
   const int nv = (hi - vs) / E;           // whole vectors from vs
   const uint4* rv = reinterpret_cast<const uint4*>(row + vs);
   for (int v = lt; v < nv; v += nt * kUnroll) {
-    uint4 buf[kUnroll];
+    uint4 buf[kUnroll][2];
 #pragma unroll
     for (int j = 0; j < kUnroll; ++j)
-      if (v + j * nt < nv) buf[j] = ld_stream16(rv + v + j * nt, pol);
+      if (v + j * nt < nv) ld_stream32(rv + 2 * (v + j * nt), pol, buf[j][0], buf[j][1]);
 #pragma unroll
     for (int j = 0; j < kUnroll; ++j) {
       if (v + j * nt < nv) {
         const uint32_t base = static_cast<uint32_t>(vs + (v + j * nt) * E);
 #pragma unroll
-        for (int i = 0; i < E; ++i) {
-          const float x = Elem<T>::get(buf[j], i);
-          if (better<kMin>(x, best)) { best = x; bi = base + i; }
-        }
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int i = 0; i < E / 2; ++i) {
+            const float x = Elem<T>::get(buf[j][h], i);
+            if (better<kMin>(x, best)) { best = x; bi = base + h * (E / 2) + i; }
+          }
       }
     }
   }

@@ -73,6 +73,13 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p, uint64_t pol) {
   return r;
 }
 
+// 32-byte (256-bit) form of ld_stream16; the address must be 32-byte aligned.
+__device__ __forceinline__ void ld_stream32(const void* p, uint64_t pol, uint4& a, uint4& b) {
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+      : "l"(p), "l"(pol));
+}
+
 // 16-byte read-only load through L1 (activations, re-read by many warps).
 __device__ __forceinline__ uint4 ld_nc16(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));

@@ -57,13 +57,7 @@ __global__ void __launch_bounds__(kProbeThreads) probe16_kernel(const uint4* buf
   publish_xor(acc, out);
 }
 
-// Variant 2: 32 bytes per thread-iteration (one 256-bit load).
-__device__ __forceinline__ void ld_stream32(const void* p, uint64_t pol, uint4& a, uint4& b) {
-  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
-      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
-      : "l"(p), "l"(pol));
-}
-
+// Variant 2: 32 bytes per thread-iteration (one 256-bit load, ld_stream32).
 __global__ void __launch_bounds__(kProbeThreads) probe32_kernel(const uint4* buf, size_t n16,
                                                                  uint32_t* out) {
   const uint64_t pol = l2_evict_first_policy();
