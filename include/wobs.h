@@ -44,7 +44,10 @@
  *     WOBS_TC=0 keeps dense GEMVs off the tcgen05 kernel and WOBS_M1=ldg
  *     selects the direct-load M = 1 kernels (both for testing).
  *     WOBS_SPLITK=<s> also forces <s> slices per row on wobs_argmax /
- *     wobs_argmin.
+ *     wobs_argmin.  WOBS_NF4=cp selects the CUDA-core NF4 kernel,
+ *     WOBS_NF4_P=0..3 sets how many code words in eight the tensor-core NF4
+ *     kernel decodes in registers, and WOBS_NF4_STAGES=2..4 caps its copy
+ *     ring (all three for measurements).
  */
 #ifndef WOBS_H
 #define WOBS_H

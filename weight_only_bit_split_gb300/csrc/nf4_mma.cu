@@ -210,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_kernel(const __grid_const
                                                              const __nv_bfloat16* __restrict__ x,
                                                              __nv_bfloat16* __restrict__ y, int N,
                                                              int K, uint32_t smem_bytes,
-                                                             ArgmaxArgs am, int* err) {
+                                                             int max_stages, ArgmaxArgs am,
+                                                             int* err) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = smem_addr(smem);
   const Layout L = make_layout(base, smem_bytes);
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_kernel(const __grid_const
   float* wmax = reinterpret_cast<float*>(gen(base + 224));               // [8] (16 halves)
   uint64_t* keys = reinterpret_cast<uint64_t*>(gen(base + 288));         // [17], to base + 424
   float* red = reinterpret_cast<float*>(gen(L.red));                     // [S][8 K groups][64 rows]
-  const int S = L.S;
+  const int S = L.S < max_stages ? L.S : max_stages;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -531,9 +532,14 @@ cudaError_t run_p(const uint8_t* qs, const float* absmax, const Codebook16& cb, 
   info->block = kThreads;
   info->smem = smem;
   info->kernel = "nf4_mma";
+  // ring depth: every stage the shared memory holds (WOBS_NF4_STAGES = 2..4
+  // caps it, for measurements)
+  const char* sv = std::getenv("WOBS_NF4_STAGES");
+  const int max_stages = sv ? std::atoi(sv) : kMaxStages;
   return launch_k(kern, dim3(grid), dim3(kThreads), smem, st, true, tq, ta, cb, cb_scale, cb_inv,
                   static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, K,
-                  static_cast<uint32_t>(smem), am, error_word_ptr());
+                  static_cast<uint32_t>(smem), max_stages < 2 ? 2 : max_stages, am,
+                  error_word_ptr());
 }
 
 template <bool kArgmax>
