@@ -15,9 +15,9 @@ Modules
 -------
 numerics  exact conversions (fp16/bf16 round-to-nearest-even), rounding,
           units in the last place.
-formats   Q8_1 activation blocks, Q4_0 weight blocks, NF4 blockwise codes and
+formats   Q8_1 activation blocks, Q4_0 and Q8_0 weight blocks, NF4 blockwise codes and
           the NormalFloat codebook: quantise, pack, unpack, dequantise.
-gemv      the dot products themselves (dense, Q4_0 x Q8_1, NF4), greedy argmax
+gemv      the dot products themselves (dense, Q4_0 x Q8_1, Q8_0 x Q8_1, NF4), greedy argmax
           and argmin,
           the streaming-read checksum, and the parity bound.
 
@@ -34,10 +34,12 @@ from .numerics import (  # noqa: F401
 from .formats import (  # noqa: F401
     quantize_q8_1, pack_q8_1, unpack_q8_1,
     quantize_q4_0, pack_q4_0, unpack_q4_0, dequantize_q4_0,
+    quantize_q8_0, dequantize_q8_0,
     nf4_codebook, quantize_nf4, pack_nf4, unpack_nf4, dequantize_nf4,
 )
 from .gemv import (  # noqa: F401
     gemv_dense, abs_dot_dense, q4_0_q8_1_blockdots, gemv_q4_0_q8_1,
-    abs_dot_q4_0_q8_1, gemv_nf4, abs_dot_nf4, argmax_rows, argmin_rows, xor_words,
+    abs_dot_q4_0_q8_1, q8_0_q8_1_blockdots, gemv_q8_0_q8_1, abs_dot_q8_0_q8_1,
+    gemv_nf4, abs_dot_nf4, argmax_rows, argmin_rows, xor_words,
     parity_bound,
 )

@@ -1,4 +1,5 @@
-"""Quantised formats: Q8_1 activations, Q4_0 weights, NF4 blockwise weights.
+"""Quantised formats: Q8_1 activations, Q4_0 and Q8_0 weights, NF4 blockwise
+weights.
 
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
@@ -31,6 +32,19 @@ element j in its low nibble and element j + 16 in its high nibble.
 Dequantised value: fp16(d) * (q - 8).  In memory the library keeps two
 planes per matrix: ``qs[N][K/2]`` (the nibble bytes, block after block) and
 ``d[N][K/32]`` (fp16 scales).
+
+Q8_0 (weights), named in the same case study, section "What correctness
+was measured against": the new matrix path is tested on Q4_0 and Q8_0
+weights.  Per block of 32 consecutive elements of one weight row, in IEEE
+float32 (the Q8_1 recipe without the sum field):
+
+    amax = max_i |w_i|
+    d    = amax / 127
+    q_i  = round_half_away(w_i / d)        (q_i = 0 when d == 0)
+
+and the block stores fp16(d) and the 32 int8 codes.  Planes: ``qs[N][K]``
+(int8 codes, element order) and ``d[N][K/32]`` (fp16).  Dequantised value:
+fp16(d) * q.
 
 NF4 (weights), named in bitsandbytes issue #1842 "70B 4-bit LLM decode
 bottlenecked by HIP kernel (kgemm_4bit_inference_naive) efficiency",
@@ -107,6 +121,43 @@ def unpack_q8_1(blocks, k):
     s16 = np.ascontiguousarray(b[:, :, 2:4]).view(np.float16).reshape(m, nb)
     q = np.ascontiguousarray(b[:, :, 4:36]).view(np.int8).reshape(m, k)
     return q, d16, s16
+
+
+# --------------------------------------------------------------------- Q8_0
+
+QK8_0 = 32
+
+
+def quantize_q8_0(w):
+    """Quantise weights ``w`` (N, K) float32 to Q8_0.
+
+    Returns ``(q, d16)``: int8 codes (N, K), element order, and fp16 scales
+    (N, K/32).  Both are the two planes the library stores.
+    """
+    w = np.asarray(w, dtype=np.float32)
+    assert w.ndim == 2 and w.shape[1] % QK8_0 == 0
+    n, k = w.shape
+    nb = k // QK8_0
+    q = np.zeros((n, k), dtype=np.int8)
+    d16 = np.zeros((n, nb), dtype=np.float16)
+    for b in range(nb):
+        blk = w[:, QK8_0 * b:QK8_0 * (b + 1)]
+        amax = np.max(np.abs(blk), axis=1)                      # exact
+        d = (amax / np.float32(127.0)).astype(np.float32)       # IEEE fp32 div
+        zero = d == 0
+        quot = (blk / np.where(zero, np.float32(1.0), d)[:, None]).astype(np.float32)
+        qb = np.where(zero[:, None], 0.0, round_half_away(quot))
+        assert np.all(np.abs(qb) <= 127)
+        q[:, QK8_0 * b:QK8_0 * (b + 1)] = qb.astype(np.int8)
+        d16[:, b] = f16_rn(d)
+    return q, d16
+
+
+def dequantize_q8_0(q, d16):
+    """fp16(d) * q as float64, (N, K)."""
+    q = np.asarray(q, dtype=np.int8).astype(np.float64)
+    d = np.repeat(np.asarray(d16, np.float16).astype(np.float64), QK8_0, axis=1)
+    return q * d
 
 
 # --------------------------------------------------------------------- Q4_0

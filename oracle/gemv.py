@@ -12,7 +12,7 @@ double precision), over exactly the operand values the device sees.
 
 import numpy as np
 
-from .formats import QK4_0, QK_NF4, unpack_nf4, unpack_q4_0
+from .formats import QK4_0, QK8_0, QK_NF4, unpack_nf4, unpack_q4_0
 from .numerics import ulp
 
 _ROWS_PER_CHUNK = 1024
@@ -98,6 +98,47 @@ def abs_dot_q4_0_q8_1(qs, d4, q8, d8):
             s = (q4b * q8b[mm]).sum(axis=2).astype(np.float64)
             out[mm, r0:r0 + q4b.shape[0]] = (s * ac * b[mm]).sum(axis=1)
     return out
+
+
+def q8_0_q8_1_blockdots(qw, q8):
+    """Exact integer block dots sum_i qw_i * q8_{m,i}, (M, N, K/32) int32.
+
+    ``qw``: Q8_0 codes (N, K) int8; ``q8``: Q8_1 codes (M, K) int8.
+    |sum| <= 32 * 127 * 127 = 516128, so int32 holds it exactly.
+    """
+    qw = np.asarray(qw, dtype=np.int8).astype(np.int64)
+    q8 = _as_cols(q8).astype(np.int64)
+    n, k = qw.shape
+    m = q8.shape[0]
+    nb = k // QK8_0
+    out = np.empty((m, n, nb), dtype=np.int64)
+    q8b = q8.reshape(m, nb, QK8_0)
+    for r0 in range(0, n, _ROWS_PER_CHUNK):
+        qb = qw[r0:r0 + _ROWS_PER_CHUNK].reshape(-1, nb, QK8_0)
+        for mm in range(m):
+            out[mm, r0:r0 + qb.shape[0]] = (qb * q8b[mm]).sum(axis=2)
+    assert np.all(np.abs(out) <= 516128)
+    return out.astype(np.int32)
+
+
+def gemv_q8_0_q8_1(qw, dw, q8, d8):
+    """y[m, n] = sum_b dw[n, b] * d8[m, b] * sumi[m, n, b] in float64.
+
+    ``dw``: fp16 Q8_0 weight scales (N, K/32); ``d8``: fp16 Q8_1 activation
+    scales (M, K/32); ``sumi``: the exact block dots above.
+    """
+    sumi = q8_0_q8_1_blockdots(qw, q8).astype(np.float64)
+    a = np.asarray(dw, np.float16).astype(np.float64)
+    b = _as_cols(np.asarray(d8, np.float16)).astype(np.float64)
+    return (sumi * a[None, :, :] * b[:, None, :]).sum(axis=2)
+
+
+def abs_dot_q8_0_q8_1(qw, dw, q8, d8):
+    """sum_i |dw qw_i| * |d8 q8_i| in float64, (M, N)."""
+    return gemv_q8_0_q8_1(np.abs(np.asarray(qw, np.int8).astype(np.int16)).astype(np.int8),
+                          np.abs(np.asarray(dw, np.float16)),
+                          np.abs(_as_cols(np.asarray(q8, np.int8)).astype(np.int16)).astype(np.int8),
+                          np.abs(_as_cols(np.asarray(d8, np.float16))))
 
 
 def gemv_nf4(qs, absmax, cb, x):

@@ -217,3 +217,47 @@ def test_nf4_nearest_tie_goes_to_lower_level():
     w[0, 2] = -0.75          # exactly between levels 0 and 1
     codes, _ = oracle.quantize_nf4(w, cb)
     assert codes[0, 1] == 2 and codes[0, 2] == 0
+
+
+# ------------------------------------------------------------------ Q8_0
+
+def test_q8_0_h7_worked_block():
+    h = load("q8_0_h7_h8.json")["h7"]
+    q, d16 = oracle.quantize_q8_0(np.asarray([h["w"]], dtype=np.float32))
+    assert q[0].tolist() == h["q"]
+    assert float(d16[0, 0]) == h["d16"]
+
+
+def test_q8_0_invariants_on_random_rows():
+    rng = np.random.default_rng(21)
+    w = (rng.standard_normal((40, 256)) * 0.02).astype(np.float32)
+    w[3, :32] = 0.0                                   # a zero block
+    q, d16 = oracle.quantize_q8_0(w)
+    assert q.dtype == np.int8 and np.all(np.abs(q.astype(np.int32)) <= 127)
+    wb = w.reshape(40, 8, 32)
+    qb = q.reshape(40, 8, 32).astype(np.float64)
+    amax = np.abs(wb).max(axis=2)
+    for n in range(40):
+        for b in range(8):
+            if amax[n, b] == 0:
+                assert np.all(qb[n, b] == 0) and float(d16[n, b]) == 0.0
+                continue
+            i = int(np.argmax(np.abs(wb[n, b])))
+            assert abs(qb[n, b, i]) == 127 and np.sign(qb[n, b, i]) == np.sign(wb[n, b, i])
+            d = float(np.float32(amax[n, b]) / np.float32(127.0))
+            # each code is the nearest multiple of d, up to float32 rounding of the quotient
+            assert np.all(np.abs(wb[n, b].astype(np.float64) - d * qb[n, b]) <= d / 2 * (1 + 2 ** -20))
+    # dequantised weights stay within half an fp16 step plus the fp16 rounding of d
+    deq = oracle.dequantize_q8_0(q, d16)
+    dd = np.repeat(d16.astype(np.float64), 32, axis=1)
+    assert np.all(np.abs(deq - w) <= dd * 0.5 + 127 * dd * 2 ** -11 + 1e-12)
+
+
+def test_q8_0_codes_equal_q8_1_codes():
+    # Q8_1 is Q8_0 plus a sum field: on the same numbers the codes and
+    # scales agree (two oracle functions written separately)
+    rng = np.random.default_rng(22)
+    v = rng.standard_normal((5, 320)).astype(np.float32)
+    q0, d0 = oracle.quantize_q8_0(v)
+    q1, d1, _ = oracle.quantize_q8_1(v)
+    assert np.array_equal(q0, q1) and np.array_equal(d0.view(np.uint16), d1.view(np.uint16))

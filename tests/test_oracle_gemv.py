@@ -195,3 +195,60 @@ def test_argmin_is_argmax_of_the_negation():
     v[3, 100] = -0.0                                               # -0 and +0 tie
     assert np.array_equal(oracle.argmin_rows(v), oracle.argmax_rows(-v))
     assert oracle.argmin_rows(v)[3] == 0
+
+
+# ------------------------------------------------------------ Q8_0 x Q8_1
+
+def _h8_inputs():
+    h7 = load("q8_0_h7_h8.json")["h7"]["w"]
+    w = np.zeros((2, 64), np.float32)
+    w[0, :32] = h7
+    w[0, 32:] = 1.0
+    w[1, 32] = -1.0
+    w[1, 33:] = 0.25
+    return w
+
+
+def test_q8_0_q8_1_h8_worked_example():
+    from fractions import Fraction
+    h = load("q8_0_h7_h8.json")["h8"]
+    qw, dw = oracle.quantize_q8_0(_h8_inputs())
+    q8, d8, _ = oracle.quantize_q8_1(np.ones((1, 64), np.float32))
+    assert np.array_equal(oracle.q8_0_q8_1_blockdots(qw, q8)[0], np.asarray(h["sumi"]))
+    assert dw.astype(np.float64).tolist() == h["dw"]
+    y = oracle.gemv_q8_0_q8_1(qw, dw, q8, d8)[0]
+    for n in range(2):
+        num, den = h["y_num_den"][n]
+        assert y[n] == float(Fraction(num, den))
+
+
+def test_q8_0_q8_1_blockdots_brute_force():
+    rng = np.random.default_rng(23)
+    qw = rng.integers(-127, 128, size=(3, 96)).astype(np.int8)
+    q8 = rng.integers(-127, 128, size=(2, 96)).astype(np.int8)
+    got = oracle.q8_0_q8_1_blockdots(qw, q8)
+    for m in range(2):
+        for n in range(3):
+            for b in range(3):
+                s = 0
+                for i in range(32):
+                    s += int(qw[n, 32 * b + i]) * int(q8[m, 32 * b + i])
+                assert got[m, n, b] == s
+
+
+def test_q8_0_q8_1_closed_forms():
+    # constant positive rows quantise to all-127 codes: against x = ones each
+    # block dot is 32 * 127 * 127, and a transposed operand would break the
+    # row-index pattern of the second check
+    w = np.full((4, 128), 0.3, np.float32)
+    qw, dw = oracle.quantize_q8_0(w)
+    q8, d8, _ = oracle.quantize_q8_1(np.ones((1, 128), np.float32))
+    assert np.all(oracle.q8_0_q8_1_blockdots(qw, q8) == 32 * 127 * 127)
+    # unit scales: weights n * e_0 per row (amax n, d = n/127 exactly only for
+    # n = 127) -- use codes directly: y = sum of row codes times x codes
+    qw2 = np.zeros((5, 32), np.int8)
+    for n in range(5):
+        qw2[n, n] = n + 1
+    x8 = np.arange(1, 33, dtype=np.int8)[None, :]
+    y = oracle.gemv_q8_0_q8_1(qw2, np.ones((5, 1), np.float16), x8, np.ones((1, 1), np.float16))[0]
+    assert y.tolist() == [float((n + 1) * (n + 1)) for n in range(5)]
