@@ -724,6 +724,85 @@ class LmHead:
         return nbytes
 
 
+class Q8M1(Q4M1):
+    """Q8_0 x Q8_1, M = 1, the four 8B projection shapes (the case study's
+    other tested weight format)."""
+    name = "q8_0_q8_1_m1_8b_shapes"
+    kernel = "q8_0_q8_1_mc_cp"
+    kernel_src = "q8_0.cu"
+    wbpw = 1.0625                                   # bytes per weight
+
+    def __init__(self, device):
+        import weight_only_bit_split_gb300 as wobs
+        from weight_only_bit_split_gb300 import synth
+        self.wobs = wobs
+        wbytes = sum(self.wbpw * n * k for n, k in self.shapes)
+        self.copies = max(1, math.ceil(ROTATE_BYTES / wbytes))
+        self.planes = []
+        for c in range(self.copies):
+            row = []
+            for n, k in self.shapes:
+                w = synth.weights(self.workload_id, (n, k), copy=c, device=device)
+                row.append(wobs.wobs_quantize_q8_0(w))
+                del w
+            self.planes.append(row)
+        self.x_all, self.x = packed([(1, k) for _, k in self.shapes], torch.float32, device)
+        for xv, (_, k) in zip(self.x, self.shapes):
+            xv.copy_(synth.activations(self.workload_id, (1, k), device=device))
+        self.xq = [torch.empty(1, k // 32 * 36, dtype=torch.uint8, device=device) for _, k in self.shapes]
+        self.y_all, self.y = packed([(1, n) for n, _ in self.shapes], torch.float32, device)
+        torch.cuda.synchronize(device)
+
+    @staticmethod
+    def gemv_bytes(n, k):
+        return n * k + 2 * (n * k // 32) + 36 * k // 32 + 4 * n
+
+    def step(self, c):
+        w = self.wobs
+        for s in range(len(self.shapes)):
+            w.wobs_quantize_q8_1(self.x[s], self.xq[s])
+            qs, d = self.planes[c][s]
+            w.wobs_gemv_q8_0_q8_1(qs, d, self.xq[s], y=self.y[s])
+
+    def kernel_calls(self):
+        out = []
+        for s, (n, k) in enumerate(self.shapes):
+            def fn(c, s=s):
+                qs, d = self.planes[c][s]
+                self.wobs.wobs_gemv_q8_0_q8_1(qs, d, self.xq[s], y=self.y[s])
+            out.append((f"{n}x{k}", self.gemv_bytes(n, k), fn))
+        return out
+
+    def config(self):
+        cfg = super().config()
+        cfg["step"] = "per shape: quantize_q8_1(x) then gemv_q8_0_q8_1"
+        cfg["working_set_gb"] = round(self.copies * sum(self.wbpw * n * k for n, k in self.shapes) / 1e9, 3)
+        return cfg
+
+    @classmethod
+    def oracle_prepare(cls, frac):
+        import oracle
+        from weight_only_bit_split_gb300 import synth
+        prep = []
+        for n, k in cls.shapes:
+            rows = max(1, int(round(n * frac)))
+            w = synth.weights(cls.workload_id, (rows, k)).numpy()
+            qw, dw = oracle.quantize_q8_0(w)
+            x = synth.activations(cls.workload_id, (1, k)).numpy()
+            prep.append((qw, dw, x, rows, k))
+        return prep
+
+    @classmethod
+    def oracle_step(cls, prep):
+        import oracle
+        nbytes = 0
+        for qw, dw, x, rows, k in prep:
+            q8, d8, _ = oracle.quantize_q8_1(x)
+            oracle.gemv_q8_0_q8_1(qw, dw, q8, d8)
+            nbytes += cls.gemv_bytes(rows, k) + cls.quant_bytes(k)
+        return nbytes
+
+
 class ArgCmp:
     """Standalone argmax / argmin over rows of the ArgCompare discussion's
     model table: LLaMA-3-8B vocabulary rows at batch 1 and 32 (bf16), a
@@ -816,10 +895,10 @@ class ArgCmp:
 
 
 WORKLOADS = {"q4_m1": Q4M1, "q4_m_sweep": Q4Sweep, "fp16_4096": DenseF16, "nf4": NF4,
-             "lm_head": LmHead, "argcmp": ArgCmp}
+             "lm_head": LmHead, "argcmp": ArgCmp, "q8_m1": Q8M1}
 # oracle row fraction per step (bounds the CPU time of one oracle step)
 ORACLE_FRACTION = {"q4_m1": 0.125, "q4_m_sweep": 1 / 64, "fp16_4096": 0.5, "nf4": 1 / 32,
-                   "lm_head": 1 / 256, "argcmp": 1 / 4}
+                   "lm_head": 1 / 256, "argcmp": 1 / 4, "q8_m1": 1 / 16}
 
 
 def oracle_rate(cls, frac, min_seconds, max_steps=None):

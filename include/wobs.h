@@ -9,7 +9,8 @@
  *   - dense fp16 / bf16 (batch1-cdna README, "02-gemv");
  *   - Q4_0 weights x Q8_1 activations with integer block dots ("The kernel
  *     that waited for itself", m12-db-gemm case study, section "Seven
- *     variants, one microbenchmark, many mistakes");
+ *     variants, one microbenchmark, many mistakes"), and Q8_0 weights x
+ *     Q8_1 activations (same page, "What correctness was measured against");
  *   - NF4 blockwise 4-bit codebook weights (bitsandbytes issue #1842,
  *     "Benchmark Data" and "Minimal Repro");
  * plus an optional fused greedy argmax over the outputs ("[WIP] ArgCompare
@@ -80,6 +81,7 @@ extern "C" {
 #define WOBS_OP_GEMV_Q4_0_Q8_1 3
 #define WOBS_OP_GEMV_NF4 4
 #define WOBS_OP_ARGCMP 5     /* wobs_argmax / wobs_argmin; K = element bytes */
+#define WOBS_OP_GEMV_Q8_0_Q8_1 6
 
 /* ---- element types of wobs_argmax / wobs_argmin ---- */
 #define WOBS_DTYPE_F16 1
@@ -233,6 +235,38 @@ WOBS_API int wobs_quantize_nf4(const void* W, int64_t ldw, int N, int K,
  *   ws  workspace (op WOBS_OP_GEMV_Q4_0_Q8_1).
  */
 WOBS_API int wobs_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* xq, int M,
+                                 float* y, int64_t* argmax, int N, int K, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/*
+ * Q8_0 weight quantisation ("The kernel that waited for itself", section
+ * "What correctness was measured against": the matrix path is tested on
+ * Q4_0 and Q8_0 weights).  Per block of 32 consecutive elements of a row,
+ * IEEE float32: d = max|w| / 127, q = round-half-away(w / d) (0 when
+ * d == 0).  Outputs the two planes the GEMV reads: qs int8 [N][K] (codes in
+ * element order) and d fp16 [N][K/32].  Bit-exact with the definition.
+ *
+ *   W fp32 [N][ldw] (ldw >= K, 4-byte aligned); K multiple of 32.
+ */
+WOBS_API int wobs_quantize_q8_0(const float* W, int64_t ldw, int N, int K, int8_t* qs, void* d,
+                                void* stream);
+
+/*
+ * Q8_0 x Q8_1 GEMV (same page and section), 1 to 32 columns: per weight
+ * block b and column m the exact integer block dot
+ * sumi = sum_i qw_i * q8_{m,i} (signed 4-way byte dot products), then
+ * y[m][n] += dw[n][b] * d8[m][b] * sumi in fp32.
+ *
+ *   qs int8 [N][K] and d fp16 [N][K/32] (both 16-byte aligned, from
+ *   wobs_quantize_q8_0 or repacked llama.cpp blocks); xq [M][K/32] Q8_1
+ *   blocks; y fp32 [M][N]; argmax int64 [M] or NULL; 1 <= M <= WOBS_MAX_M;
+ *   K a multiple of 256 (UNSUPPORTED_SHAPE otherwise, also when K is so long
+ *   that one column's activation blocks no longer fit in shared memory).
+ *   Columns are processed eight at a time (fewer for very long rows), one
+ *   kernel launch each, so the weights are read once per eight columns.
+ *   ws  workspace (op WOBS_OP_GEMV_Q8_0_Q8_1), needed only for the argmax.
+ */
+WOBS_API int wobs_gemv_q8_0_q8_1(const int8_t* qs, const void* d, const void* xq, int M,
                                  float* y, int64_t* argmax, int N, int K, void* ws,
                                  size_t ws_bytes, void* stream);
 

@@ -163,3 +163,26 @@ def test_argcmp_workspace_rules(monkeypatch):
     assert rc == -1 and "workspace" in msg
     rc, _ = _status("wobs_argmax", 3, FAKE16, 1000, 10, 1000, FAKE16, FAKE16, 64, None)
     assert rc == -4
+
+
+def test_q8_0_argument_checks():
+    rc, _ = _status("wobs_quantize_q8_0", None, 64, 1, 64, FAKE16, FAKE16, None)
+    assert rc == -1
+    rc, _ = _status("wobs_quantize_q8_0", FAKE16, 64, 1, 48, FAKE16, FAKE16, None)
+    assert rc == -3                        # K not a multiple of 32
+    rc, _ = _status("wobs_quantize_q8_0", FAKE16, 64, 1, 64, FAKE16, FAKE_ODD, None)
+    assert rc == -2                        # fp16 scales at an odd address
+    g = "wobs_gemv_q8_0_q8_1"
+    rc, _ = _status(g, FAKE16, None, FAKE16, 1, FAKE16, None, 8, 256, None, 0, None)
+    assert rc == -1
+    rc, _ = _status(g, FAKE16, FAKE16, FAKE16, 33, FAKE16, None, 8, 256, None, 0, None)
+    assert rc == -1                        # M above 32
+    rc, _ = _status(g, FAKE16, FAKE16, FAKE16, 1, FAKE16, None, 8, 96, None, 0, None)
+    assert rc == -3                        # K not a multiple of 256
+    rc, _ = _status(g, FAKE16, ctypes.c_void_p(0x10008), FAKE16, 1, FAKE16, None, 8, 256, None, 0, None)
+    assert rc == -2                        # scale plane not 16-byte aligned
+    rc, msg = _status(g, FAKE16, FAKE16, FAKE16, 1, FAKE16, FAKE16, 8, 256, None, 0, None)
+    assert rc == -1 and "workspace" in msg  # argmax without a workspace
+    lib = _lib.get()
+    assert lib.wobs_workspace_size(6, 1, 4096, 4096) >= 8 + 8 * 32
+    assert lib.wobs_workspace_size(6, 33, 4096, 4096) == 0

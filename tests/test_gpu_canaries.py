@@ -143,3 +143,42 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     assert wobs.wobs_error_word() == 0
     with pytest.raises(wobs.WobsError):
         wobs.wobs_selftest_wait_timeout(0)
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 1000, 4096), (3, 333, 2304), (8, 700, 1024), (13, 77, 512)])
+def test_q8_0_outputs_and_workspace_stay_in_bounds(m, n, k):
+    w, x = w_x_fp32(2, n, k, m)
+    qw, dw = oracle.quantize_q8_0(w)
+    q8, d8, s8 = oracle.quantize_q8_1(x)
+    gy = guarded((m, n), torch.float32)
+    ga = guarded((m,), torch.int64)
+    wsz = wobs.wobs_workspace_size(wobs.OP_GEMV_Q8_0_Q8_1, m, n, k)
+    gw = guarded((max(wsz, 1),), torch.uint8)
+    gw[4].zero_()
+    y, am = wobs.wobs_gemv_q8_0_q8_1(to_dev(qw), f16_to_dev(dw), to_dev(oracle.pack_q8_1(q8, d8, s8)),
+                                     y=gy[4], argmax=ga[4], ws=gw[4])
+    torch.cuda.synchronize()
+    for g, what in ((gy, "y"), (ga, "argmax"), (gw, "workspace")):
+        check_guards(g, f"q8_0 M={m} {n}x{k} {what}")
+    yn = y.cpu().numpy()
+    assert_within(yn, oracle.gemv_q8_0_q8_1(qw, dw, q8, d8), oracle.abs_dot_q8_0_q8_1(qw, dw, q8, d8),
+                  "f32", "guarded q8_0")
+    assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
+    assert int(gw[4].count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("m,n,splits", [(1, 131077, None), (5, 1000, "3"), (400, 300, None)])
+def test_argcmp_output_and_workspace_stay_in_bounds(m, n, splits, monkeypatch):
+    if splits:
+        monkeypatch.setenv("WOBS_SPLITK", splits)
+    x = synth.normal((m, n), 1.0, synth.seed_of(6, 2, 3))
+    go = guarded((m,), torch.int64)
+    wsz = wobs.wobs_workspace_size(wobs.OP_ARGCMP, m, n, 4)
+    gw = guarded((max(wsz, 1),), torch.uint8)
+    gw[4].zero_()
+    out = wobs.wobs_argmax(x.to(dev()), out=go[4], ws=gw[4] if wsz else None)
+    torch.cuda.synchronize()
+    check_guards(go, "argmax out")
+    check_guards(gw, "argmax workspace")
+    assert np.array_equal(out.cpu().numpy(), oracle.argmax_rows(x.numpy()))
+    assert int(gw[4].count_nonzero()) == 0

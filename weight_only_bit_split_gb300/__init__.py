@@ -20,6 +20,7 @@ OP_GEMV_BF16 = 2
 OP_GEMV_Q4_0_Q8_1 = 3
 OP_GEMV_NF4 = 4
 OP_ARGCMP = 5
+OP_GEMV_Q8_0_Q8_1 = 6
 DTYPE_CODES = {torch.float16: 1, torch.bfloat16: 2, torch.float32: 3}
 MAX_M = 32
 Q8_1_BLOCK_BYTES = 36
@@ -302,6 +303,49 @@ def wobs_gemv_q4_0_q8_1(qs, d, xq, y=None, argmax=None, want_argmax=False, ws=No
     if ws is None:
         ws = _auto_ws(OP_GEMV_Q4_0_Q8_1, M, N, K, qs.device, argmax)
     rc = lib.wobs_gemv_q4_0_q8_1(_ptr(qs), _ptr(d), _ptr(xq2), M, _ptr(y), _ptr(argmax), N, K,
+                                 _ptr(ws), ws.numel() if ws is not None else 0,
+                                 _stream(qs.device))
+    _check(rc, lib)
+    return y, argmax
+
+
+def wobs_quantize_q8_0(W, qs=None, d=None):
+    """Q8_0 planes of fp32 weights W[N, K]: (qs int8 [N, K], d fp16 [N, K/32])."""
+    lib = _lib.get()
+    _need(W, "W", torch.float32, 2)
+    N, K = W.shape
+    if qs is None:
+        qs = torch.empty(N, K, dtype=torch.int8, device=W.device)
+    if d is None:
+        d = torch.empty(N, K // 32, dtype=torch.float16, device=W.device)
+    _need(qs, "qs", torch.int8, 2, W.device)
+    _need(d, "d", torch.float16, 2, W.device)
+    rc = lib.wobs_quantize_q8_0(_ptr(W), _rows(W), N, K, _ptr(qs), _ptr(d), _stream(W.device))
+    _check(rc, lib)
+    return qs, d
+
+
+def wobs_gemv_q8_0_q8_1(qs, d, xq, y=None, argmax=None, want_argmax=False, ws=None):
+    """y[M, N] (fp32) from Q8_0 planes (qs int8 [N, K], d [N, K/32]) and Q8_1 blocks xq [M, ...]."""
+    lib = _lib.get()
+    _need(qs, "qs", torch.int8, 2)
+    _need(d, "d", torch.float16, 2, qs.device)
+    xq2 = xq if xq.dim() == 2 else xq.view(1, -1)
+    _need(xq2, "xq", torch.uint8, 2, qs.device)
+    N, K = qs.shape
+    M = xq2.shape[0]
+    if xq2.shape[1] != (K // 32) * Q8_1_BLOCK_BYTES or not xq2.is_contiguous():
+        raise ValueError("xq must be contiguous [M, K/32*36]")
+    if not (qs.is_contiguous() and d.is_contiguous()) or d.shape != (N, K // 32):
+        raise ValueError("qs/d must be contiguous planes [N, K] and [N, K/32]")
+    if y is None:
+        y = torch.empty(M, N, dtype=torch.float32, device=qs.device)
+    _need(y, "y", torch.float32, None, qs.device)
+    if argmax is None and want_argmax:
+        argmax = torch.empty(M, dtype=torch.int64, device=qs.device)
+    if ws is None:
+        ws = _auto_ws(OP_GEMV_Q8_0_Q8_1, M, N, K, qs.device, argmax)
+    rc = lib.wobs_gemv_q8_0_q8_1(_ptr(qs), _ptr(d), _ptr(xq2), M, _ptr(y), _ptr(argmax), N, K,
                                  _ptr(ws), ws.numel() if ws is not None else 0,
                                  _stream(qs.device))
     _check(rc, lib)

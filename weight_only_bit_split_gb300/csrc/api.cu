@@ -270,8 +270,8 @@ size_t wobs_workspace_size(int op, int M, int N, int K) {
     if (p.warp_rows || p.splits == 1) return 0;
     return (12ull * M + 15ull) & ~15ull;   // keys [M] (8 bytes), then counters [M] (4 bytes)
   }
-  if (op < WOBS_OP_GEMV_F16 || op > WOBS_OP_GEMV_NF4 || M < 1 || M > WOBS_MAX_M || N < 1 || K < 1)
-    return 0;
+  const bool known = (op >= WOBS_OP_GEMV_F16 && op <= WOBS_OP_GEMV_NF4) || op == WOBS_OP_GEMV_Q8_0_Q8_1;
+  if (!known || M < 1 || M > WOBS_MAX_M || N < 1 || K < 1) return 0;
   return ws_layout(op, M, N, K).total;
 }
 
@@ -394,6 +394,39 @@ int wobs_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* xq, int M,
   cudaError_t e = wobs::launch_gemv_q4_0_q8_1(qs, d, xq, M, y, N, K, p.sk, p.am,
                                               static_cast<cudaStream_t>(stream), &L);
   return finish_launch(e, "gemv_q4_0_q8_1", M, N, K, L, p.sk.splits);
+}
+
+int wobs_quantize_q8_0(const float* W, int64_t ldw, int N, int K, int8_t* qs, void* d,
+                       void* stream) {
+  if (!W || !qs || !d) return fail(WOBS_ERR_INVALID_ARG, "quantize_q8_0: null pointer");
+  if (N < 1 || K < 32 || (K % 32)) return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "quantize_q8_0: N=%d K=%d", N, K);
+  if (ldw < K) return fail(WOBS_ERR_INVALID_ARG, "quantize_q8_0: ldw < K");
+  if (!aligned4(W) || (reinterpret_cast<uintptr_t>(d) & 1u))
+    return fail(WOBS_ERR_MISALIGNED, "quantize_q8_0: misaligned pointer");
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_quantize_q8_0(W, ldw, N, K, qs, d, static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "quantize_q8_0", 0, N, K, L, 1);
+}
+
+int wobs_gemv_q8_0_q8_1(const int8_t* qs, const void* d, const void* xq, int M, float* y,
+                        int64_t* argmax, int N, int K, void* ws, size_t ws_bytes, void* stream) {
+  if (!qs || !d || !xq || !y) return fail(WOBS_ERR_INVALID_ARG, "gemv_q8_0_q8_1: null pointer");
+  if (M < 1 || M > WOBS_MAX_M) return fail(WOBS_ERR_INVALID_ARG, "gemv_q8_0_q8_1: M=%d outside 1..%d", M, WOBS_MAX_M);
+  if (N < 1 || K < 256 || (K % 256))
+    return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "gemv_q8_0_q8_1: N=%d K=%d (K must be a positive multiple of 256)", N, K);
+  if (!aligned16(qs) || !aligned16(d) || !aligned4(xq) || !aligned4(y))
+    return fail(WOBS_ERR_MISALIGNED, "gemv_q8_0_q8_1: misaligned pointer");
+  if (argmax && (reinterpret_cast<uintptr_t>(argmax) & 7u))
+    return fail(WOBS_ERR_MISALIGNED, "gemv_q8_0_q8_1: argmax not 8-byte aligned");
+  Prepared p;
+  int rc = prepare_ws(WOBS_OP_GEMV_Q8_0_Q8_1, M, N, K, argmax, ws, ws_bytes, &p);
+  if (rc) return rc;
+  if (wobs::q8_0_columns_per_launch(K) == 0)
+    return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "gemv_q8_0_q8_1: K=%d: one column's activation blocks do not fit in shared memory", K);
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_gemv_q8_0_q8_1(qs, d, xq, M, y, N, K, p.am,
+                                              static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "gemv_q8_0_q8_1", M, N, K, L, 1);
 }
 
 int wobs_gemv_nf4(const uint8_t* qs, const float* absmax, const float* codebook, const void* x,

@@ -77,6 +77,15 @@ int forced_splits();
 cudaError_t launch_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, int N, int K,
                                        int32_t* out, cudaStream_t st, Launch* info);
 
+// Q8_0 weights: quantiser, and the GEMV (K % 256 == 0, 16-byte aligned
+// planes; columns taken q8_0_columns_per_launch(K) at a time, 0 = K too long)
+cudaError_t launch_quantize_q8_0(const float* W, int64_t ldw, int N, int K, int8_t* qs, void* d,
+                                 cudaStream_t st, Launch* info);
+cudaError_t launch_gemv_q8_0_q8_1(const int8_t* qs, const void* d, const void* xq, int M, float* Y,
+                                  int N, int K, const ArgmaxArgs& am, cudaStream_t st,
+                                  Launch* info);
+int q8_0_columns_per_launch(int K);
+
 cudaError_t launch_gemv_nf4(const uint8_t* qs, const float* absmax, const Codebook16& cb,
                             const void* x, void* y, int N, int K, const ArgmaxArgs& am,
                             cudaStream_t st, Launch* info);
