@@ -11,12 +11,16 @@
 //
 // GEMV design (sm_103a): one warp per weight row, lanes along K, rows
 // round-robin over every CTA; each warp streams its rows through its own
-// two-slot ring of 2176-byte segments (64 blocks: the first 16 code bytes of
-// every block, then the second 16, then the 64 scales) filled by 16-byte
-// cp.async, so every shared-memory read of the ring is lane-contiguous.  The
-// Q8_1 activation blocks of up to eight columns are re-laid out once per CTA
-// into conflict-free planes, and each weight block, read once, is dotted
-// with all of them.  More than eight columns are taken eight at a time.
+// two-slot ring of 2176-byte segments (64 blocks: their 2048 code bytes as
+// in memory, then their 64 scales) filled by 16-byte cp.async.  Shared and
+// global addresses of every copy are both lane-contiguous: a copy whose
+// shared side is scattered makes the L1 fetch each sector once per pass
+// (measured on GB300: twice the DRAM bytes over the crossbar and half the
+// streaming rate).  A lane takes 16-byte chunks, half a block each, dots
+// the 16 codes with the matching half of the Q8_1 activation block (staged
+// once per CTA in the same chunk order, so those reads are lane-contiguous
+// too) and scales the exact half-block sum by dw * d8.  Up to eight columns
+// share each weight chunk, read once; more are taken eight at a time.
 #include "common.cuh"
 
 namespace wobs {
@@ -51,8 +55,8 @@ __global__ void __launch_bounds__(kQThreads) q8_0_quant_kernel(const float* __re
 // -------------------------------------------------------------------- GEMV
 
 constexpr int kSegBlocks = 64;                  // blocks per ring segment
-constexpr int kHalfBytes = kSegBlocks * 16;     // one 16-byte half of every block
-constexpr int kSegBytes = 2 * kHalfBytes + kSegBlocks * 2;
+constexpr int kScaleOff = kSegBlocks * 32;      // codes, then the segment's scales
+constexpr int kSegBytes = kScaleOff + kSegBlocks * 2;
 constexpr int kRing = 2;
 
 template <int MC>
@@ -75,17 +79,13 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
-// Signed 32-element block dot from the two 16-byte halves of each side.
-__device__ __forceinline__ int q8_dot(uint4 wl, uint4 wh, int4 xl, int4 xh) {
+// Signed dot of 16 weight codes with 16 activation codes (exact).
+__device__ __forceinline__ int q8_dot16(uint4 w, int4 x) {
   int s = 0;
-  s = __dp4a(static_cast<int>(wl.x), xl.x, s);
-  s = __dp4a(static_cast<int>(wl.y), xl.y, s);
-  s = __dp4a(static_cast<int>(wl.z), xl.z, s);
-  s = __dp4a(static_cast<int>(wl.w), xl.w, s);
-  s = __dp4a(static_cast<int>(wh.x), xh.x, s);
-  s = __dp4a(static_cast<int>(wh.y), xh.y, s);
-  s = __dp4a(static_cast<int>(wh.z), xh.z, s);
-  s = __dp4a(static_cast<int>(wh.w), xh.w, s);
+  s = __dp4a(static_cast<int>(w.x), x.x, s);
+  s = __dp4a(static_cast<int>(w.y), x.y, s);
+  s = __dp4a(static_cast<int>(w.z), x.z, s);
+  s = __dp4a(static_cast<int>(w.w), x.w, s);
   return s;
 }
 
@@ -106,9 +106,8 @@ __global__ void __launch_bounds__(Q8Shape<MC>::kThreads) q8_mc_cp_kernel(
   const int rows_w = wg < N ? (N - 1 - wg) / total_warps + 1 : 0;
   const int T = rows_w * nseg;
   uint8_t* myring = smem + warp * (kRing * kSegBytes);
-  int4* x_lo = reinterpret_cast<int4*>(smem + Q8Shape<MC>::kRingBytes);   // [MC][nb]
-  int4* x_hi = x_lo + MC * nb;
-  float* x_d = reinterpret_cast<float*>(x_hi + MC * nb);
+  int4* x_c = reinterpret_cast<int4*>(smem + Q8Shape<MC>::kRingBytes);    // [MC][2 nb] code chunks
+  float* x_d = reinterpret_cast<float*>(x_c + 2 * MC * nb);                 // [MC][nb] scales
 
   int prow = wg, pseg = 0;   // next segment to request
   auto issue = [&](int slot) {
@@ -117,15 +116,12 @@ __global__ void __launch_bounds__(Q8Shape<MC>::kThreads) q8_mc_cp_kernel(
     const int n = min(kSegBlocks, nb - b0);
     const int8_t* qr = qs + static_cast<int64_t>(prow) * K + 32 * b0;
 #pragma unroll
-    for (int u = 0; u < kSegBlocks / 32; ++u) {
-      const int bl = 32 * u + lane;
-      if (bl < n) {
-        cp_async16(st + 16 * bl, qr + 32 * bl);
-        cp_async16(st + kHalfBytes + 16 * bl, qr + 32 * bl + 16);
-      }
+    for (int u = 0; u < 2 * kSegBlocks / 32; ++u) {
+      const int c = 32 * u + lane;                 // 16-byte chunk of the segment's codes
+      if (c < 2 * n) cp_async16(st + 16 * c, qr + 16 * c);
     }
     const uint16_t* dr = dw + static_cast<int64_t>(prow) * nb + b0;
-    if (lane < n / 8) cp_async16(st + 2 * kHalfBytes + 16 * lane, dr + 8 * lane);
+    if (lane < n / 8) cp_async16(st + kScaleOff + 16 * lane, dr + 8 * lane);
     if (++pseg == nseg) { pseg = 0; prow += total_warps; }
   };
   // the first kRing-1 segments are requested before waiting for the
@@ -142,12 +138,12 @@ __global__ void __launch_bounds__(Q8Shape<MC>::kThreads) q8_mc_cp_kernel(
     if (m < M) {
       const uint32_t* blk = reinterpret_cast<const uint32_t*>(xq + 36 * (static_cast<int64_t>(m) * nb + b));
       x_d[i] = __half2float(__ushort_as_half(static_cast<unsigned short>(__ldg(blk) & 0xFFFFu)));
-      x_lo[i] = make_int4(__ldg(blk + 1), __ldg(blk + 2), __ldg(blk + 3), __ldg(blk + 4));
-      x_hi[i] = make_int4(__ldg(blk + 5), __ldg(blk + 6), __ldg(blk + 7), __ldg(blk + 8));
+      x_c[2 * i] = make_int4(__ldg(blk + 1), __ldg(blk + 2), __ldg(blk + 3), __ldg(blk + 4));
+      x_c[2 * i + 1] = make_int4(__ldg(blk + 5), __ldg(blk + 6), __ldg(blk + 7), __ldg(blk + 8));
     } else {
       x_d[i] = 0.f;
-      x_lo[i] = make_int4(0, 0, 0, 0);
-      x_hi[i] = make_int4(0, 0, 0, 0);
+      x_c[2 * i] = make_int4(0, 0, 0, 0);
+      x_c[2 * i + 1] = make_int4(0, 0, 0, 0);
     }
   }
   __syncthreads();
@@ -169,17 +165,16 @@ __global__ void __launch_bounds__(Q8Shape<MC>::kThreads) q8_mc_cp_kernel(
     const int b0 = cseg * kSegBlocks;
     const int n = min(kSegBlocks, nb - b0);
 #pragma unroll
-    for (int u = 0; u < kSegBlocks / 32; ++u) {
-      const int bl = 32 * u + lane;
-      if (bl < n) {
-        const uint4 wl = *reinterpret_cast<const uint4*>(st + 16 * bl);
-        const uint4 wh = *reinterpret_cast<const uint4*>(st + kHalfBytes + 16 * bl);
+    for (int u = 0; u < 2 * kSegBlocks / 32; ++u) {
+      const int c = 32 * u + lane;              // chunk: half (c & 1) of block b0 + (c >> 1)
+      if (c < 2 * n) {
+        const uint4 wc = *reinterpret_cast<const uint4*>(st + 16 * c);
         const float dwf = __half2float(__ushort_as_half(
-            *reinterpret_cast<const unsigned short*>(st + 2 * kHalfBytes + 2 * bl)));
-        const int b = b0 + bl;
+            *reinterpret_cast<const unsigned short*>(st + kScaleOff + 2 * (c >> 1))));
+        const int b = b0 + (c >> 1);
 #pragma unroll
         for (int m = 0; m < MC; ++m) {
-          const int dot = q8_dot(wl, wh, x_lo[m * nb + b], x_hi[m * nb + b]);
+          const int dot = q8_dot16(wc, x_c[2 * (m * nb + b0) + c]);
           acc[m] = fmaf(static_cast<float>(dot), dwf * x_d[m * nb + b], acc[m]);
         }
       }
