@@ -6,12 +6,15 @@
 A step is one pass of the decode path over one batch of synthetic input.
 The default workload is the Q4_0 x Q8_1 M = 1 decode of an 8B model's four
 projection shapes (4096x4096, 1024x4096, 14336x4096, 4096x14336): per
-shape, quantise the fp32 activation vector to Q8_1 and run the GEMV.  The
-weights are rotated over enough seeded copies that the working set exceeds
+shape, one wobs_gemv_q4_0_f32 launch quantises the fp32 activation vector
+to Q8_1 (writing the blocks) and runs the GEMV on it.  The weights are rotated over enough seeded copies that the working set exceeds
 1.07 GB (the batch1-cdna README rotates 32 copies of a 4096^2 fp16 matrix
 for the same reason), so every step reads its weights from HBM, not L2.
 
-Other workloads (``--workload``): fp16_4096 (dense fp16 4096x4096), nf4
+Other workloads (``--workload``): q4_m1_2call (the same decode as two
+launches per shape, quantize_q8_1 then gemv_q4_0_q8_1), q8_m1 (Q8_0
+weights, same shapes), argcmp (standalone argmax / argmin rows),
+fp16_4096 (dense fp16 4096x4096), nf4
 (NF4 28672x8192), q4_m_sweep (Q4_0 x Q8_1 for M in {1,..,32} on 4096x4096
 and 14336x4096), lm_head (bf16 128000x4096 with fused argmax, M = 1 and 32).
 
@@ -310,8 +313,9 @@ def traffic_record(kernel):
 
 
 class Q4M1:
-    """Q4_0 x Q8_1, M = 1, the four 8B projection shapes."""
-    name = "q4_0_q8_1_m1_8b_shapes"
+    """Q4_0 x Q8_1, M = 1, the four 8B projection shapes: quantise then GEMV
+    as two launches per shape."""
+    name = "q4_0_q8_1_m1_8b_shapes_two_launch"
     shapes = [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)]
     dtype = "int8"
     kernel = "q4_0_q8_1_m1_cp"
@@ -409,6 +413,54 @@ class Q4M1:
             q8, d8, _ = oracle.quantize_q8_1(x)
             oracle.gemv_q4_0_q8_1(qs, d4, q8, d8)
             nbytes += cls.gemv_bytes(rows, k) + cls.quant_bytes(k)
+        return nbytes
+
+
+class Q4M1Fused(Q4M1):
+    """The same decode with the Q8_1 quantisation fused into the GEMV
+    (wobs_gemv_q4_0_f32): one launch per shape reads the fp32 activations,
+    writes their Q8_1 blocks (sum field included) and the outputs."""
+    name = "q4_0_q8_1_m1_8b_shapes"
+    kernel = "q4_0_f32_m1_cp"
+    launches_per_step = 4
+
+    @staticmethod
+    def fused_bytes(n, k):
+        return int(0.5625 * n * k) + 4 * k + 36 * k // 32 + 4 * n
+
+    def bytes_per_step(self):
+        return sum(self.fused_bytes(n, k) for n, k in self.shapes)
+
+    def step(self, c):
+        w = self.wobs
+        for s in range(len(self.shapes)):
+            qs, d = self.planes[c][s]
+            w.wobs_gemv_q4_0_f32(qs, d, self.x[s], y=self.y[s], xq_out=self.xq[s])
+
+    def kernel_calls(self):
+        out = []
+        for s, (n, k) in enumerate(self.shapes):
+            def fn(c, s=s):
+                qs, d = self.planes[c][s]
+                self.wobs.wobs_gemv_q4_0_f32(qs, d, self.x[s], y=self.y[s], xq_out=self.xq[s])
+            out.append((f"{n}x{k}", self.fused_bytes(n, k), fn))
+        return out
+
+    def config(self):
+        cfg = super().config()
+        cfg["step"] = ("per shape: gemv_q4_0_f32(x) -- quantize_q8_1 fused into the GEMV kernel "
+                       "(Q8_1 blocks written, bit-identical to the two-launch path)")
+        return cfg
+
+    @classmethod
+    def oracle_step(cls, prep):
+        import oracle
+        nbytes = 0
+        for qs, d4, x, rows, k in prep:
+            q8, d8, s8 = oracle.quantize_q8_1(x)
+            oracle.pack_q8_1(q8, d8, s8)
+            oracle.gemv_q4_0_q8_1(qs, d4, q8, d8)
+            nbytes += cls.fused_bytes(rows, k)
         return nbytes
 
 
@@ -894,10 +946,10 @@ class ArgCmp:
         return nbytes
 
 
-WORKLOADS = {"q4_m1": Q4M1, "q4_m_sweep": Q4Sweep, "fp16_4096": DenseF16, "nf4": NF4,
+WORKLOADS = {"q4_m1": Q4M1Fused, "q4_m1_2call": Q4M1, "q4_m_sweep": Q4Sweep, "fp16_4096": DenseF16, "nf4": NF4,
              "lm_head": LmHead, "argcmp": ArgCmp, "q8_m1": Q8M1}
 # oracle row fraction per step (bounds the CPU time of one oracle step)
-ORACLE_FRACTION = {"q4_m1": 0.125, "q4_m_sweep": 1 / 64, "fp16_4096": 0.5, "nf4": 1 / 32,
+ORACLE_FRACTION = {"q4_m1": 0.125, "q4_m1_2call": 0.125, "q4_m_sweep": 1 / 64, "fp16_4096": 0.5, "nf4": 1 / 32,
                    "lm_head": 1 / 256, "argcmp": 1 / 4, "q8_m1": 1 / 16}
 
 

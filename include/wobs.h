@@ -82,6 +82,7 @@ extern "C" {
 #define WOBS_OP_GEMV_NF4 4
 #define WOBS_OP_ARGCMP 5     /* wobs_argmax / wobs_argmin; K = element bytes */
 #define WOBS_OP_GEMV_Q8_0_Q8_1 6
+#define WOBS_OP_GEMV_Q4_0_F32 7   /* wobs_gemv_q4_0_f32 */
 
 /* ---- element types of wobs_argmax / wobs_argmin ---- */
 #define WOBS_DTYPE_F16 1
@@ -237,6 +238,31 @@ WOBS_API int wobs_quantize_nf4(const void* W, int64_t ldw, int N, int K,
 WOBS_API int wobs_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* xq, int M,
                                  float* y, int64_t* argmax, int N, int K, void* ws,
                                  size_t ws_bytes, void* stream);
+
+/*
+ * Q4_0 GEMV on one fp32 activation vector, its Q8_1 quantisation fused into
+ * the GEMV ("The kernel that waited for itself", section "Seven variants,
+ * one microbenchmark, many mistakes": the decode product over Q4_0 weights
+ * and Q8_1-quantised activations).  One kernel: every CTA quantises x into
+ * shared memory itself, taking every decision of the quantiser (IEEE
+ * float32 block scale and quotients, round half away from zero), and
+ * y and argmax are bit-identical to wobs_quantize_q8_1(x) followed by
+ * wobs_gemv_q4_0_q8_1 with M = 1.  When xq_out is not NULL the kernel also
+ * writes the K/32 Q8_1 blocks there, bit-identical to wobs_quantize_q8_1
+ * (for other GEMVs on the same activation vector).
+ *
+ *   qs, d, y, argmax, N: as wobs_gemv_q4_0_q8_1 with M = 1; x fp32 [K];
+ *   xq_out [K/32] blocks of 36 bytes or NULL (must not overlap x).
+ *   qs, d and x 16-byte aligned, y and xq_out 4-byte aligned; K a multiple
+ *   of 256 and at most 104704 (the activation planes live in shared memory).
+ *   ws  workspace (op WOBS_OP_GEMV_Q4_0_F32), needed only for the argmax.
+ *   Errors: WOBS_ERR_UNSUPPORTED_SHAPE for another K (quantise with
+ *   wobs_quantize_q8_1 and call wobs_gemv_q4_0_q8_1 instead),
+ *   WOBS_ERR_MISALIGNED, WOBS_ERR_INVALID_ARG for a null pointer.
+ */
+WOBS_API int wobs_gemv_q4_0_f32(const uint8_t* qs, const void* d, const float* x, void* xq_out,
+                                float* y, int64_t* argmax, int N, int K, void* ws,
+                                size_t ws_bytes, void* stream);
 
 /*
  * Q8_0 weight quantisation ("The kernel that waited for itself", section

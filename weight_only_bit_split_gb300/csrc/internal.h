@@ -72,6 +72,11 @@ int q4_mma_splits(int M, int N, int K, int forced);
 size_t q4_mma_partial_bytes(int M, int N, int K, int forced);
 // The few-column (2..8) whole-row kernel applies (it needs no K split).
 bool q4_mc_applies(int M, int K);
+// Q8_1 quantisation fused into the M = 1 cp.async kernel (one launch).
+bool q4_0_f32_fused_applies(const void* d, int M, int K);
+cudaError_t launch_gemv_q4_0_f32_fused(const uint8_t* qs, const void* d, const float* x,
+                                       void* xq_out, float* y, int N, int K, const ArgmaxArgs& am,
+                                       cudaStream_t st, Launch* info);
 // WOBS_SPLITK, or 0 when unset.
 int forced_splits();
 cudaError_t launch_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, int N, int K,

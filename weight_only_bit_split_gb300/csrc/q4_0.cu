@@ -20,6 +20,10 @@
 // broadcast, so every unpacked weight block is reused for all M columns
 // from registers.  K is split across CTAs when the rows alone cannot fill
 // the GPU; the last CTA of a row group adds the partials in a fixed order.
+#include <cstdlib>
+#include <cstring>
+
+
 #include "common.cuh"
 
 namespace wobs {
@@ -220,18 +224,118 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
-template <bool kArgmax>
-__global__ void __launch_bounds__(kCpThreads) q4_m1_cp_kernel(const uint8_t* __restrict__ qs,
+// The IEEE float32 quotient, kept out of line: it is the rare fallback of
+// q8_1_codes and must not be evaluated (predicated) on the fast path.
+__device__ __noinline__ float ieee_div(float x, float d) { return x / d; }
+
+// q = roundf(x / d) for four elements of one block, as the Q8_1 format
+// defines it (IEEE float32 quotient, then round half away from zero),
+// without a full division for almost every element.  For 2^-126 <= d <
+// 2^126, __fdividef(x, d) is within 2 ulp of the exact quotient (CUDA's
+// documented bound) and the IEEE quotient is within 0.5 ulp of it; with
+// |x / d| <= 127 (x is in the block whose maximum defines d) one ulp is at
+// most 2^-17, so both lie within 2^-14 of each other.  roundf changes value
+// only at the half-integers k + 1/2, so when the approximation is farther
+// than 2^-14 from the nearest one, both quotients round to the same
+// integer; otherwise (and for d outside the bound's range) the IEEE
+// division decides.
+__device__ __forceinline__ float q8_1_quotient(float x, float d, bool d_ok) {
+  const float t = __fdividef(x, d);
+  const float h = floorf(t) + 0.5f;
+  return (d_ok && fabsf(t - h) > 0x1p-14f) ? t : __int_as_float(0x7fc00000);   // NaN: decide exactly
+}
+__device__ __forceinline__ void q8_1_codes(const float4& v, float d, int& q0, int& q1, int& q2,
+                                           int& q3) {
+  const bool d_ok = d >= 0x1p-126f && d < 0x1p126f;
+  float t0 = q8_1_quotient(v.x, d, d_ok), t1 = q8_1_quotient(v.y, d, d_ok);
+  float t2 = q8_1_quotient(v.z, d, d_ok), t3 = q8_1_quotient(v.w, d, d_ok);
+  if (__builtin_expect(isnan(t0) || isnan(t1) || isnan(t2) || isnan(t3), 0)) {
+    if (isnan(t0)) t0 = ieee_div(v.x, d);
+    if (isnan(t1)) t1 = ieee_div(v.y, d);
+    if (isnan(t2)) t2 = ieee_div(v.z, d);
+    if (isnan(t3)) t3 = ieee_div(v.w, d);
+  }
+  q0 = static_cast<int>(roundf(t0));
+  q1 = static_cast<int>(roundf(t1));
+  q2 = static_cast<int>(roundf(t2));
+  q3 = static_cast<int>(roundf(t3));
+}
+
+// Q8_1 quantisation of one fp32 activation vector straight into the
+// shared-memory planes of the M = 1 kernel (every CTA quantises the whole
+// vector).  The decisions are the quantiser's: eight threads per 32-block,
+// four elements each, amax over the block, d = amax / 127 in IEEE float32,
+// q = roundf(x / d) (q8_1_codes; 0 when d = 0), d widened back from its fp16
+// rounding, exact integer code sum -- so the planes hold exactly what
+// staging the stored Q8_1 blocks would.  Every thread of the CTA (NT of
+// them) calls this: the shuffles and the loop bounds are warp-uniform
+// because nb % 8 == 0 and a warp's four groups are consecutive.
+template <int NT>
+__device__ __forceinline__ void q8_1_planes_from_f32(const float* __restrict__ X, int nb, int4* x_lo,
+                                                     int4* x_hi, float* x_d, int* x_s,
+                                                     uint8_t* __restrict__ xq_out) {
+  constexpr int kGroups = NT / 8;
+  constexpr int kBatch = 4;                    // loads in flight per thread
+  const int g = threadIdx.x >> 3, j = threadIdx.x & 7;
+  for (int b0 = g; b0 < nb; b0 += kBatch * kGroups) {
+    float4 v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int b = b0 + u * kGroups;
+      v[u] = b < nb ? *reinterpret_cast<const float4*>(X + 32 * b + 4 * j)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int b = b0 + u * kGroups;
+      if (b >= nb) break;                      // warp-uniform
+      float amax = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float d = amax / 127.0f;
+      int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+      if (d != 0.0f) q8_1_codes(v[u], d, q0, q1, q2, q3);
+      int sum = q0 + q1 + q2 + q3;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      const uint32_t packed = (static_cast<uint32_t>(q0) & 0xFFu) |
+                              ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
+                              ((static_cast<uint32_t>(q2) & 0xFFu) << 16) |
+                              (static_cast<uint32_t>(q3) << 24);
+      reinterpret_cast<int*>(j < 4 ? &x_lo[b] : &x_hi[b])[j & 3] = static_cast<int>(packed);
+      if (j == 0) {
+        x_d[b] = __half2float(__float2half_rn(d));
+        x_s[b] = sum;
+      }
+      // the 36-byte Q8_1 block {fp16 d, fp16 d * sum, codes}, each block
+      // written by one CTA
+      if (xq_out != nullptr && b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
+        uint8_t* blk = xq_out + 36 * static_cast<int64_t>(b);
+        *reinterpret_cast<uint32_t*>(blk + 4 + 4 * j) = packed;
+        if (j == 0) {
+          const float sd = d * static_cast<float>(sum);
+          *reinterpret_cast<__half2*>(blk) = __halves2half2(__float2half_rn(d), __float2half_rn(sd));
+        }
+      }
+    }
+  }
+}
+
+// kF32X: xsrc is the fp32 activation vector, quantised to Q8_1 in the
+// prologue; otherwise it holds the Q8_1 blocks.  W warps per CTA.
+template <bool kArgmax, bool kF32X, int W = kCpWarps>
+__global__ void __launch_bounds__(W * 32) q4_m1_cp_kernel(const uint8_t* __restrict__ qs,
                                                                const uint16_t* __restrict__ d4,
-                                                               const uint8_t* __restrict__ xq,
+                                                               const void* __restrict__ xsrc,
                                                                float* __restrict__ y, int N, int K,
-                                                               ArgmaxArgs am) {
+                                                               ArgmaxArgs am,
+                                                               uint8_t* __restrict__ xq_out) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int nb = K >> 5;
   const int kh = K >> 1;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int total_warps = gridDim.x * kCpWarps;
+  const int total_warps = gridDim.x * W;
   // rows spread round-robin over the CTAs first, so every SM gets an
   // equal share even when there are fewer rows than warps
   const int wg = warp * gridDim.x + blockIdx.x;
@@ -239,7 +343,7 @@ __global__ void __launch_bounds__(kCpThreads) q4_m1_cp_kernel(const uint8_t* __r
   const int rows_w = wg < N ? (N - 1 - wg) / total_warps + 1 : 0;
   const int T = rows_w * nseg;
   uint8_t* myring = smem + warp * (kRing * kSegBytes);
-  int4* x_lo = reinterpret_cast<int4*>(smem + kRingBytes);
+  int4* x_lo = reinterpret_cast<int4*>(smem + W * kRing * kSegBytes);
   int4* x_hi = x_lo + nb;
   float* x_d = reinterpret_cast<float*>(x_hi + nb);
   int* x_s = reinterpret_cast<int*>(x_d + nb);
@@ -265,14 +369,20 @@ __global__ void __launch_bounds__(kCpThreads) q4_m1_cp_kernel(const uint8_t* __r
     if (i < T) issue(i);
     cp_async_commit();
   }
+  // this CTA has started: after the matching wait, peers may store into its planes
   pdl_launch_dependents();
   pdl_wait();
-  for (int b = threadIdx.x; b < nb; b += kCpThreads) {
-    const XBlock xb = load_xblock(xq + 36 * static_cast<int64_t>(b));
-    x_lo[b] = xb.lo;
-    x_hi[b] = xb.hi;
-    x_d[b] = xb.d;
-    x_s[b] = xb.s;
+  if constexpr (kF32X) {
+    q8_1_planes_from_f32<W * 32>(static_cast<const float*>(xsrc), nb, x_lo, x_hi, x_d, x_s, xq_out);
+  } else {
+    const uint8_t* xq = static_cast<const uint8_t*>(xsrc);
+    for (int b = threadIdx.x; b < nb; b += W * 32) {
+      const XBlock xb = load_xblock(xq + 36 * static_cast<int64_t>(b));
+      x_lo[b] = xb.lo;
+      x_hi[b] = xb.hi;
+      x_d[b] = xb.d;
+      x_s[b] = xb.s;
+    }
   }
   __syncthreads();
 
@@ -315,13 +425,13 @@ __global__ void __launch_bounds__(kCpThreads) q4_m1_cp_kernel(const uint8_t* __r
   }
   cp_async_wait<0>();
   if (kArgmax) {
-    __shared__ uint64_t s_best[kCpWarps];
+    __shared__ uint64_t s_best[W];
     __shared__ uint64_t s_cta[1];
     if (lane == 0) s_best[warp] = best;
     __syncthreads();
     if (threadIdx.x == 0) {
       uint64_t bk = 0;
-      for (int i = 0; i < kCpWarps; ++i) bk = s_best[i] > bk ? s_best[i] : bk;
+      for (int i = 0; i < W; ++i) bk = s_best[i] > bk ? s_best[i] : bk;
       s_cta[0] = bk;
     }
     __syncthreads();
@@ -329,29 +439,38 @@ __global__ void __launch_bounds__(kCpThreads) q4_m1_cp_kernel(const uint8_t* __r
   }
 }
 
-template <bool kArgmax>
-cudaError_t run_m1_cp_t(const uint8_t* qs, const void* d, const void* xq, float* y, int N, int K,
+template <bool kArgmax, bool kF32X>
+cudaError_t run_m1_cp_t(const uint8_t* qs, const void* d, const void* xsrc, float* y, int N, int K,
                         const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   const int nb = K / 32;
   const int smem = kRingBytes + nb * 40;
-  cudaError_t e = cudaFuncSetAttribute(q4_m1_cp_kernel<kArgmax>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = q4_m1_cp_kernel<kArgmax, kF32X>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int grid = 2 * device_sm_count();
   if (grid > N) grid = N;
   info->grid_x = grid;
   info->block = kCpThreads;
   info->smem = smem;
-  info->kernel = "q4_0_q8_1_m1_cp";
-  return launch_k(q4_m1_cp_kernel<kArgmax>, dim3(grid), dim3(kCpThreads), smem, st, true, qs,
-                  static_cast<const uint16_t*>(d), static_cast<const uint8_t*>(xq), y, N, K, am);
+  info->kernel = kF32X ? "q4_0_f32_m1_cp" : "q4_0_q8_1_m1_cp";
+  return launch_k(kern, dim3(grid), dim3(kCpThreads), smem, st, true, qs,
+                  static_cast<const uint16_t*>(d), xsrc, y, N, K, am,
+                  static_cast<uint8_t*>(nullptr));
 }
 
 cudaError_t run_m1_cp(const uint8_t* qs, const void* d, const void* xq, float* y, int N, int K,
                       const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
-  return am.out ? run_m1_cp_t<true>(qs, d, xq, y, N, K, am, st, info)
-                : run_m1_cp_t<false>(qs, d, xq, y, N, K, am, st, info);
+  return am.out ? run_m1_cp_t<true, false>(qs, d, xq, y, N, K, am, st, info)
+                : run_m1_cp_t<false, false>(qs, d, xq, y, N, K, am, st, info);
 }
+
+// The M = 1 cp.async kernel applies: whole 256-element scale segments,
+// 16-byte aligned scale plane, ring and planes within 200 KB.
+bool m1_cp_shape(const void* d, int K) {
+  return (K % 256 == 0) && (reinterpret_cast<uintptr_t>(d) % 16 == 0) &&
+         (kRingBytes + (K / 32) * 40 <= 200 * 1024);
+}
+bool m1_cp_applies(const void* d, int K) { return m1_cp_shape(d, K) && !m1_ldg_forced(); }
 
 // ------------------------------------- 2..8 columns, cp.async staging
 
@@ -711,9 +830,7 @@ cudaError_t launch_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* 
                                   const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   if (M == 1 && sk.splits <= 1) {
     // 16-byte asynchronous copies need 16-byte aligned scale segments
-    const bool cp_ok = (K % 256 == 0) && (reinterpret_cast<uintptr_t>(d) % 16 == 0) &&
-                       (kRingBytes + (K / 32) * 40 <= 200 * 1024);
-    if (cp_ok && !m1_ldg_forced()) return run_m1_cp(qs, d, xq, Y, N, K, am, st, info);
+    if (m1_cp_applies(d, K)) return run_m1_cp(qs, d, xq, Y, N, K, am, st, info);
     return run_m1(qs, d, xq, Y, N, K, am, st, info);
   }
   const bool cp_shape = K % 256 == 0 && reinterpret_cast<uintptr_t>(d) % 16 == 0;
@@ -733,6 +850,50 @@ cudaError_t launch_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* 
   if (M <= 16) return run_mn<16>(qs, d, xq, M, Y, N, K, sk, am, st, info);
   if (M <= 24) return run_mn<24>(qs, d, xq, M, Y, N, K, sk, am, st, info);
   return run_mn<32>(qs, d, xq, M, Y, N, K, sk, am, st, info);
+}
+
+bool q4_0_f32_fused_applies(const void* d, int M, int K) { return M == 1 && m1_cp_shape(d, K); }
+
+// CTA-local quantisation: W warps per CTA, 2 CTAs per SM for W = 16, one
+// for W = 32 (each SM then quantises x once).
+template <bool kArgmax, int W>
+cudaError_t run_m1_local_t(const uint8_t* qs, const void* d, const float* x, uint8_t* xq_out,
+                           float* y, int N, int K, const ArgmaxArgs& am, cudaStream_t st,
+                           Launch* info) {
+  const int smem = W * kRing * kSegBytes + (K / 32) * 40;
+  auto kern = q4_m1_cp_kernel<kArgmax, true, W>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int grid = (W >= 32 ? 1 : 2) * device_sm_count();
+  if (grid > N) grid = N;
+  info->grid_x = grid;
+  info->block = W * 32;
+  info->smem = smem;
+  info->kernel = "q4_0_f32_m1_cp";
+  return launch_k(kern, dim3(grid), dim3(W * 32), smem, st, true, qs,
+                  static_cast<const uint16_t*>(d), static_cast<const void*>(x), y, N, K, am,
+                  xq_out);
+}
+
+// 32 warps and one CTA per SM (each SM quantises x once) when the ring and
+// planes fit, else 16 warps and two CTAs per SM; WOBS_Q4F32=16 forces the
+// latter.
+template <bool kArgmax>
+cudaError_t run_m1_fused(const uint8_t* qs, const void* d, const float* x, uint8_t* xq_out, float* y,
+                         int N, int K, const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
+  const char* v = std::getenv("WOBS_Q4F32");
+  const bool force16 = v && std::strcmp(v, "16") == 0;
+  const bool fits32 = 32 * kRing * kSegBytes + (K / 32) * 40 <= 220 * 1024;
+  if (fits32 && !force16) return run_m1_local_t<kArgmax, 32>(qs, d, x, xq_out, y, N, K, am, st, info);
+  return run_m1_local_t<kArgmax, 16>(qs, d, x, xq_out, y, N, K, am, st, info);
+}
+
+cudaError_t launch_gemv_q4_0_f32_fused(const uint8_t* qs, const void* d, const float* x,
+                                       void* xq_out, float* y, int N, int K, const ArgmaxArgs& am,
+                                       cudaStream_t st, Launch* info) {
+  uint8_t* xo = static_cast<uint8_t*>(xq_out);
+  return am.out ? run_m1_fused<true>(qs, d, x, xo, y, N, K, am, st, info)
+                : run_m1_fused<false>(qs, d, x, xo, y, N, K, am, st, info);
 }
 
 cudaError_t launch_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, int N, int K,
