@@ -47,7 +47,10 @@ def _q4(n, k, m):
 @pytest.mark.parametrize("m,n,k,env", [(1, 1000, 4096, None), (1, 333, 4160, None),
                                        (1, 1000, 4096, ("WOBS_M1", "ldg")), (3, 700, 2048, None),
                                        (12, 600, 2048, None), (6, 70, 2080, None),
-                                       (6, 517, 2048, ("WOBS_SPLITK", "5"))])
+                                       (6, 517, 2048, ("WOBS_SPLITK", "5")),
+                                       (32, 1000, 4096, ("WOBS_Q4TC", "1")),
+                                       (9, 333, 1280, ("WOBS_Q4TC", "1")),
+                                       (28, 6000, 4096, None)])
 def test_q4_0_outputs_and_workspace_stay_in_bounds(m, n, k, env, monkeypatch):
     if env:
         monkeypatch.setenv(*env)

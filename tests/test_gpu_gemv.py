@@ -24,6 +24,15 @@ def m1_path(request, monkeypatch):
 
 
 @pytest.fixture(params=["tc", "mma"])
+def q4_mc_path(request, monkeypatch):
+    """Run a multi-column Q4_0 test through the tcgen05 kernel (forced for 5..32
+    columns wherever its plan applies) and with it disabled (mma.sync / few-
+    column / CUDA-core kernels)."""
+    monkeypatch.setenv("WOBS_Q4TC", "1" if request.param == "tc" else "0")
+    return request.param
+
+
+@pytest.fixture(params=["tc", "mma"])
 def mc_path(request, monkeypatch):
     """Run a multi-column dense test through the tcgen05 kernel and the mma.sync one."""
     if request.param == "mma":
@@ -188,7 +197,7 @@ def test_q4_0_h4_worked_example_on_gpu():
 
 
 @pytest.mark.parametrize("m", [2, 4, 8, 12, 16, 24, 32])
-def test_gemv_q4_0_multi_column(m):
+def test_gemv_q4_0_multi_column(m, q4_mc_path):
     (qs, d, xq), ref, ad, _ = _q4_case(600, 2048, m)
     y, am = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq, want_argmax=True)
     yn = y.cpu().numpy()
@@ -213,7 +222,7 @@ def _q4_unit_scale_case(n, k, m, seed):
 
 @pytest.mark.parametrize("m", [2, 3, 8, 9, 16, 17, 24, 32])
 @pytest.mark.parametrize("n,k", [(16, 256), (37, 1024), (300, 4096), (129, 14336)])
-def test_q4_0_multi_column_block_dots_are_exact(n, k, m):
+def test_q4_0_multi_column_block_dots_are_exact(n, k, m, q4_mc_path):
     # unit scales make every output an integer below 2^24, so any exact block
     # dot and any summation order give the same float: equality, not tolerance
     (qs, d, xq), exact = _q4_unit_scale_case(n, k, m, seed=n * 1000 + m)
@@ -225,7 +234,7 @@ def test_q4_0_multi_column_block_dots_are_exact(n, k, m):
 
 @pytest.mark.parametrize("m,n,k", [(2, 1, 256), (5, 15, 512), (7, 17, 768), (32, 4100, 4096),
                                    (12, 1000, 14336), (32, 333, 8192)])
-def test_gemv_q4_0_multi_column_ragged(m, n, k):
+def test_gemv_q4_0_multi_column_ragged(m, n, k, q4_mc_path):
     (qs, d, xq), ref, ad, _ = _q4_case(n, k, m)
     y, am = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq, want_argmax=True)
     yn = y.cpu().numpy()
@@ -260,6 +269,30 @@ def test_q4_0_multi_column_paths_agree_exactly(monkeypatch, capfd):
     assert kernels == expect, kernels
 
 
+@pytest.mark.parametrize("m,n,k", [(25, 4096, 4096), (32, 6144, 4096), (32, 2048, 14336), (26, 19000, 2048),
+                                   (32, 600, 768)])
+def test_q4_0_tensor_memory_kernel_dispatch_and_parity(m, n, k, monkeypatch, capfd):
+    """Shapes with 25..32 columns that fill the GPU take the tcgen05 kernel by
+    default (K split into ranges of 1024 or 768 elements: 1, 2, 4 and 14
+    splits here; 600 x 768 is forced); outputs within the bound, argmax exact,
+    the workspace left zero."""
+    if n * k < 1 << 20:
+        monkeypatch.setenv("WOBS_Q4TC", "1")
+    else:
+        monkeypatch.delenv("WOBS_Q4TC", raising=False)
+    monkeypatch.setenv("WOBS_DEBUG", "1")
+    (qs, d, xq), ref, ad, _ = _q4_case(n, k, m)
+    ws = wobs.workspace(wobs.OP_GEMV_Q4_0_Q8_1, m, n, k, dev())
+    y, am = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq, want_argmax=True, ws=ws)
+    yn = y.cpu().numpy()
+    err = assert_within(yn, ref, ad, "f32", f"q4_0 tc M={m} {n}x{k}")
+    assert err < 1e-4
+    assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
+    assert int(ws.count_nonzero()) == 0
+    log = capfd.readouterr().err
+    assert "kernel=q4_0_q8_1_tc" in log, log
+
+
 @pytest.mark.parametrize("splits", ["2", "5", "64"])
 def test_gemv_q4_0_forced_split_k(monkeypatch, splits):
     monkeypatch.setenv("WOBS_SPLITK", splits)
@@ -271,7 +304,7 @@ def test_gemv_q4_0_forced_split_k(monkeypatch, splits):
         assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
 
 
-def test_q4_0_column_symmetry_and_determinism():
+def test_q4_0_column_symmetry_and_determinism(q4_mc_path):
     n, k = 1000, 4096
     w, x = w_x_fp32(4, n, k, 1)
     xs = np.repeat(x, 16, axis=0)

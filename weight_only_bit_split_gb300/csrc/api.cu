@@ -79,7 +79,11 @@ WsLayout ws_layout(int op, int M, int N, int K) {
       if (tb > pb) pb = tb;
     }
     if (op == WOBS_OP_GEMV_Q4_0_Q8_1 && M >= 2 && K % 256 == 0) {
-      const size_t tb = wobs::q4_mma_partial_bytes(M, N, K, env_splits());
+      size_t tb = wobs::q4_mma_partial_bytes(M, N, K, env_splits());
+      if (!env_splits() && M >= 5 && wobs::q4_tc_enabled()) {
+        const size_t tc = wobs::q4_tc_partial_bytes(M, N, K);
+        if (tc > tb) tb = tc;
+      }
       if (tb > pb) pb = tb;
     }
     off += pb;
@@ -197,6 +201,10 @@ int choose_splits(int op, int M, int N, int K) {
     case WOBS_OP_GEMV_Q4_0_Q8_1: {
       const int nb = K / 32 > 0 ? K / 32 : 1;
       if (M == 1 && !forced) return 1;
+      if (!forced && M >= 5 && q4_tc_enabled()) {
+        const Q4TcPlan tp = q4_tc_plan(M, N, K);
+        if (tp.ok) return tp.splits;
+      }
       int s;
       if (M == 1) return forced < nb ? forced : nb;
       if (!forced && q4_mc_applies(M, K)) return 1;
@@ -392,8 +400,16 @@ int wobs_gemv_q4_0_q8_1(const uint8_t* qs, const void* d, const void* xq, int M,
   int rc = prepare_ws(WOBS_OP_GEMV_Q4_0_Q8_1, M, N, K, argmax, ws, ws_bytes, &p);
   if (rc) return rc;
   wobs::Launch L;
-  cudaError_t e = wobs::launch_gemv_q4_0_q8_1(qs, d, xq, M, y, N, K, p.sk, p.am,
-                                              static_cast<cudaStream_t>(stream), &L);
+  cudaError_t e;
+  // 5..32 columns: the tcgen05 kernel where its plan applies (TMA needs a
+  // 16-byte aligned scale plane); otherwise the CUDA-core / mma.sync kernels
+  const bool tc = M >= 5 && !env_splits() && wobs::q4_tc_enabled() && aligned16(d) &&
+                  wobs::q4_tc_plan(M, N, K).ok;
+  if (tc)
+    e = wobs::launch_q4_tc(qs, d, xq, M, y, N, K, p.sk, p.am, static_cast<cudaStream_t>(stream), &L);
+  else
+    e = wobs::launch_gemv_q4_0_q8_1(qs, d, xq, M, y, N, K, p.sk, p.am,
+                                    static_cast<cudaStream_t>(stream), &L);
   return finish_launch(e, "gemv_q4_0_q8_1", M, N, K, L, p.sk.splits);
 }
 

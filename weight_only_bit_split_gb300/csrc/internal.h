@@ -77,6 +77,19 @@ bool q4_0_f32_fused_applies(const void* d, int M, int K);
 cudaError_t launch_gemv_q4_0_f32_fused(const uint8_t* qs, const void* d, const float* x,
                                        void* xq_out, float* y, int N, int K, const ArgmaxArgs& am,
                                        cudaStream_t st, Launch* info);
+// Multi-column (5..32) tcgen05 kernel: weights decoded into tensor memory,
+// block scales folded into f16 operands.  The plan fixes the K range of a
+// work unit, the split count (K / range) and the grid.
+struct Q4TcPlan {
+  bool ok = false;
+  int range = 0, splits = 1, grid = 0;
+};
+bool q4_tc_enabled();      // WOBS_Q4TC != 0
+Q4TcPlan q4_tc_plan(int M, int N, int K);
+size_t q4_tc_partial_bytes(int M, int N, int K);
+cudaError_t launch_q4_tc(const uint8_t* qs, const void* d, const void* xq, int M, float* Y, int N,
+                         int K, const SplitArgs& sk, const ArgmaxArgs& am, cudaStream_t st,
+                         Launch* info);
 // WOBS_SPLITK, or 0 when unset.
 int forced_splits();
 cudaError_t launch_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, int N, int K,
