@@ -51,11 +51,7 @@ constexpr int kRows = 128;                       // weight rows per tile (MMA M)
 constexpr int kSK = 256;                         // K elements per TMA stage (8 blocks)
 constexpr int kCodeBytes = kRows * kSK / 2;      // 16384
 constexpr int kStageBytes = kCodeBytes;
-constexpr int kStages = 8;
-constexpr int kMaxR = 1024;                      // K elements of one work unit
 constexpr int kMaxUnits = 256;                   // work units of one CTA at most
-constexpr int kSRow = kMaxR / 16;                // scale bytes per row of one unit (fp16 per block)
-constexpr int kSBuf = kRows * kSRow;             // one unit's scales: 8 KB
 constexpr int kThreads = 448;                    // TMA, MMA, 8 decoder, 4 epilogue warps
 constexpr int kAcols = kSK / 2;                  // tensor-memory columns of one A buffer
 constexpr int kAbufs = 3;                        // A buffers in tensor memory
@@ -64,8 +60,15 @@ constexpr int kTmemCols = 512;
 
 static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 
+// The longest K range of a unit (its activation tile, BN x R f16, takes up
+// to 64 KB), the copy ring depth and one unit's scales.  Ranges of 2048 for
+// 16 columns were measured slower (8 columns: 13.8 / 21.5 us against
+// 9.5 / 18.7 us on 4096^2 / 14336 x 4096): half the units, worse balance.
 template <int BN>
 struct TcQ {
+  static constexpr int kMaxR = 1024;
+  static constexpr int kStages = 8;
+  static constexpr int kSBuf = kRows * (kMaxR / 16);   // fp16 per block and row
   static constexpr int kBoxBytes = BN * 128;     // one 64-element K box of B
   static constexpr int kBBytes = (kMaxR / 64) * kBoxBytes;
   static constexpr int kSmem = 1024 + kStages * kStageBytes + 2 * kSBuf + kBBytes;
@@ -115,6 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
                                                             int S, SplitArgs sk, ArgmaxArgs am,
                                                             int* err) {
   using Sh = TcQ<BN>;
+  constexpr int kStages = Sh::kStages;
+  constexpr int kSBuf = Sh::kSBuf;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], afull[kAbufs], aempty[kAbufs], tfull[2],
       tempty[2], sfull[2], sempty[2], bready, done;
@@ -245,15 +250,16 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
     // swizzle layout (one 64-element box of BN rows per 4 KB), K order as
     // the weights'
     {
-      // at most BN / 2 items per thread (R <= 1024): every thread's loads are
-      // issued before any is used, so the conversion costs one L2 round trip
-      constexpr int kIt = BN / 2;
+      // batches of eight items per thread: every load of a batch is issued
+      // before any is used, so a batch costs one L2 round trip
+      constexpr int kIt = 8;
       const int nbr = R >> 5;
       const int items = BN * nbr * 4;
+      for (int it0 = 0; it0 < items; it0 += 256 * kIt) {
       uint32_t w[kIt][3];
 #pragma unroll
       for (int j = 0; j < kIt; ++j) {
-        const int it = dw * 32 + lane + 256 * j;
+        const int it = it0 + dw * 32 + lane + 256 * j;
         const int m = it / (nbr * 4), rem = it - m * (nbr * 4);
         const int bl = rem >> 2, i = rem & 3;
         w[j][0] = w[j][1] = w[j][2] = 0u;
@@ -267,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
       }
 #pragma unroll
       for (int j = 0; j < kIt; ++j) {
-        const int it = dw * 32 + lane + 256 * j;
+        const int it = it0 + dw * 32 + lane + 256 * j;
         if (it >= items) break;
         const int m = it / (nbr * 4), rem = it - m * (nbr * 4);
         const int bl = rem >> 2, i = rem & 3;
@@ -282,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
         const int chunk = 4 * (bl & 1) + i;
         *reinterpret_cast<uint4*>(gbase + (bbase - base) + (bl >> 1) * Sh::kBoxBytes + m * 128 +
                                   ((chunk ^ (m & 7)) << 4)) = v;
+      }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -507,9 +514,10 @@ bool q4_tc_forced() {
 Q4TcPlan q4_tc_plan(int M, int N, int K) {
   Q4TcPlan p;
   if (M < 5 || M > WOBS_MAX_M || N < 1 || K < kSK || K % kSK) return p;
-  const int cand[4] = {1024, 768, 512, 256};
+  const int cand[5] = {2048, 1024, 768, 512, 256};
+  const int rmax = M <= 16 ? TcQ<16>::kMaxR : TcQ<32>::kMaxR;
   for (int c : cand)
-    if (K % c == 0) { p.range = c; break; }
+    if (c <= rmax && K % c == 0) { p.range = c; break; }
   p.splits = K / p.range;
   const int sms = device_sm_count();
   if (p.splits > sms) return Q4TcPlan{};
