@@ -13,7 +13,7 @@ for the same reason), so every step reads its weights from HBM, not L2.
 
 Other workloads (``--workload``): q4_m1_2call (the same decode as two
 launches per shape, quantize_q8_1 then gemv_q4_0_q8_1), q8_m1 (Q8_0
-weights, same shapes), argcmp (standalone argmax / argmin rows),
+weights, same shapes, quantisation fused; q8_m1_2call: two launches), argcmp (standalone argmax / argmin rows),
 fp16_4096 (dense fp16 4096x4096), nf4
 (NF4 28672x8192), q4_m_sweep (Q4_0 x Q8_1 for M in {1,..,32} on 4096x4096
 and 14336x4096), lm_head (bf16 128000x4096 with fused argmax, M = 1 and 32).
@@ -778,8 +778,8 @@ class LmHead:
 
 class Q8M1(Q4M1):
     """Q8_0 x Q8_1, M = 1, the four 8B projection shapes (the case study's
-    other tested weight format)."""
-    name = "q8_0_q8_1_m1_8b_shapes"
+    other tested weight format): quantise then GEMV, two launches per shape."""
+    name = "q8_0_q8_1_m1_8b_shapes_two_launch"
     kernel = "q8_0_q8_1_mc_cp"
     kernel_src = "q8_0.cu"
     wbpw = 1.0625                                   # bytes per weight
@@ -852,6 +852,53 @@ class Q8M1(Q4M1):
             q8, d8, _ = oracle.quantize_q8_1(x)
             oracle.gemv_q8_0_q8_1(qw, dw, q8, d8)
             nbytes += cls.gemv_bytes(rows, k) + cls.quant_bytes(k)
+        return nbytes
+
+
+class Q8M1Fused(Q8M1):
+    """Q8_0, M = 1, the four 8B shapes with the Q8_1 quantisation fused into
+    the GEMV (wobs_gemv_q8_0_f32): one launch per shape."""
+    name = "q8_0_q8_1_m1_8b_shapes"
+    kernel = "q8_0_f32_m1_cp"
+    launches_per_step = 4
+
+    @classmethod
+    def fused_bytes(cls, n, k):
+        return n * k + 2 * (n * k // 32) + 4 * k + 36 * k // 32 + 4 * n
+
+    def bytes_per_step(self):
+        return sum(self.fused_bytes(n, k) for n, k in self.shapes)
+
+    def step(self, c):
+        w = self.wobs
+        for s in range(len(self.shapes)):
+            qs, d = self.planes[c][s]
+            w.wobs_gemv_q8_0_f32(qs, d, self.x[s], y=self.y[s], xq_out=self.xq[s])
+
+    def kernel_calls(self):
+        out = []
+        for s, (n, k) in enumerate(self.shapes):
+            def fn(c, s=s):
+                qs, d = self.planes[c][s]
+                self.wobs.wobs_gemv_q8_0_f32(qs, d, self.x[s], y=self.y[s], xq_out=self.xq[s])
+            out.append((f"{n}x{k}", self.fused_bytes(n, k), fn))
+        return out
+
+    def config(self):
+        cfg = super().config()
+        cfg["step"] = ("per shape: gemv_q8_0_f32(x) -- quantize_q8_1 fused into the GEMV kernel "
+                       "(Q8_1 blocks written, bit-identical to the two-launch path)")
+        return cfg
+
+    @classmethod
+    def oracle_step(cls, prep):
+        import oracle
+        nbytes = 0
+        for qw, dw, x, rows, k in prep:
+            q8, d8, s8 = oracle.quantize_q8_1(x)
+            oracle.pack_q8_1(q8, d8, s8)
+            oracle.gemv_q8_0_q8_1(qw, dw, q8, d8)
+            nbytes += cls.fused_bytes(rows, k)
         return nbytes
 
 
@@ -947,10 +994,10 @@ class ArgCmp:
 
 
 WORKLOADS = {"q4_m1": Q4M1Fused, "q4_m1_2call": Q4M1, "q4_m_sweep": Q4Sweep, "fp16_4096": DenseF16, "nf4": NF4,
-             "lm_head": LmHead, "argcmp": ArgCmp, "q8_m1": Q8M1}
+             "lm_head": LmHead, "argcmp": ArgCmp, "q8_m1": Q8M1Fused, "q8_m1_2call": Q8M1}
 # oracle row fraction per step (bounds the CPU time of one oracle step)
 ORACLE_FRACTION = {"q4_m1": 0.125, "q4_m1_2call": 0.125, "q4_m_sweep": 1 / 64, "fp16_4096": 0.5, "nf4": 1 / 32,
-                   "lm_head": 1 / 256, "argcmp": 1 / 4, "q8_m1": 1 / 16}
+                   "lm_head": 1 / 256, "argcmp": 1 / 4, "q8_m1": 1 / 16, "q8_m1_2call": 1 / 16}
 
 
 def oracle_rate(cls, frac, min_seconds, max_steps=None):

@@ -83,6 +83,7 @@ extern "C" {
 #define WOBS_OP_ARGCMP 5     /* wobs_argmax / wobs_argmin; K = element bytes */
 #define WOBS_OP_GEMV_Q8_0_Q8_1 6
 #define WOBS_OP_GEMV_Q4_0_F32 7   /* wobs_gemv_q4_0_f32 */
+#define WOBS_OP_GEMV_Q8_0_F32 8   /* wobs_gemv_q8_0_f32 */
 
 /* ---- element types of wobs_argmax / wobs_argmin ---- */
 #define WOBS_DTYPE_F16 1
@@ -295,6 +296,28 @@ WOBS_API int wobs_quantize_q8_0(const float* W, int64_t ldw, int N, int K, int8_
 WOBS_API int wobs_gemv_q8_0_q8_1(const int8_t* qs, const void* d, const void* xq, int M,
                                  float* y, int64_t* argmax, int N, int K, void* ws,
                                  size_t ws_bytes, void* stream);
+
+/*
+ * Q8_0 GEMV on one fp32 activation vector, its Q8_1 quantisation fused into
+ * the GEMV (the case study's Q8_0 weights with Q8_1-quantised activations).
+ * One kernel: every CTA quantises x into shared memory with the quantiser's
+ * IEEE float32 decisions, and y and argmax are bit-identical to
+ * wobs_quantize_q8_1(x) followed by wobs_gemv_q8_0_q8_1 with M = 1.  When
+ * xq_out is not NULL the K/32 Q8_1 blocks are also written there,
+ * bit-identical to wobs_quantize_q8_1.
+ *
+ *   qs, d, y, argmax, N: as wobs_gemv_q8_0_q8_1 with M = 1; x fp32 [K];
+ *   xq_out [K/32] blocks of 36 bytes or NULL (must not overlap x).
+ *   qs, d and x 16-byte aligned, y and xq_out 4-byte aligned; K a multiple
+ *   of 256 whose activation planes (36 bytes per block) fit in shared memory
+ *   beside the weight ring (K up to 143616 with 227 KB of shared memory per CTA).
+ *   ws  workspace (op WOBS_OP_GEMV_Q8_0_F32), needed only for the argmax.
+ *   Errors: WOBS_ERR_UNSUPPORTED_SHAPE for another K, WOBS_ERR_MISALIGNED,
+ *   WOBS_ERR_INVALID_ARG for a null pointer.
+ */
+WOBS_API int wobs_gemv_q8_0_f32(const int8_t* qs, const void* d, const float* x, void* xq_out,
+                                float* y, int64_t* argmax, int N, int K, void* ws,
+                                size_t ws_bytes, void* stream);
 
 /*
  * NF4 GEMV, M = 1 (bitsandbytes issue #1842: the fused 4-bit inference GEMV

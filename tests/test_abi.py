@@ -202,9 +202,25 @@ def test_q4_0_f32_argument_checks():
     assert rc == -2                        # x not 16-byte aligned
     rc, msg = _status(g, FAKE16, FAKE16, FAKE16, None, FAKE16, None, 8, 131072, None, 0, None)
     assert rc == -3 and "shared-memory" in msg
+    rc, msg = _status(g, FAKE16, FAKE16, FAKE16, None, FAKE16, None, 8, 104960, None, 0, None)
+    assert rc == -3 and "shared-memory" in msg   # one 256-block past the largest K, 104704
     rc, msg = _status(g, FAKE16, FAKE16, FAKE16, None, FAKE16, FAKE16, 8, 256, None, 0, None)
     assert rc == -1 and "workspace" in msg  # argmax without a workspace
     rc, _ = _status(g, FAKE16, FAKE16, FAKE16, FAKE_ODD, FAKE16, None, 8, 256, None, 0, None)
     assert rc == -2                        # xq_out not 4-byte aligned
     lib = _lib.get()
     assert lib.wobs_workspace_size(7, 1, 4096, 4096) == lib.wobs_workspace_size(3, 1, 4096, 4096)
+
+
+def test_q8_0_f32_argument_checks():
+    g = "wobs_gemv_q8_0_f32"
+    rc, _ = _status(g, FAKE16, FAKE16, None, None, FAKE16, None, 8, 256, None, 0, None)
+    assert rc == -1
+    rc, msg = _status(g, FAKE16, FAKE16, FAKE16, None, FAKE16, None, 8, 4160, None, 0, None)
+    assert rc == -3 and "256" in msg
+    rc, _ = _status(g, FAKE16, ctypes.c_void_p(0x10008), FAKE16, None, FAKE16, None, 8, 256, None, 0, None)
+    assert rc == -2
+    rc, _ = _status(g, FAKE16, FAKE16, FAKE16, FAKE_ODD, FAKE16, None, 8, 256, None, 0, None)
+    assert rc == -2
+    rc, msg = _status(g, FAKE16, FAKE16, FAKE16, None, FAKE16, FAKE16, 8, 256, None, 0, None)
+    assert rc == -1 and "workspace" in msg

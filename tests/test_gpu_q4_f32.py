@@ -42,7 +42,7 @@ def _two_call(qs_d, d_d, x_d, want_argmax):
 
 
 @pytest.mark.parametrize("n,k", [(1, 256), (7, 512), (100, 4096), (305, 1024), (1000, 4096),
-                                 (33, 14336), (4097, 2048), (64, 65536)])
+                                 (33, 14336), (4097, 2048), (64, 65536), (16, 104704)])
 def test_fused_matches_oracle_and_the_two_call_path(n, k, variant):
     w, x = w_x_fp32(7, n, k, 1)
     qs, d4 = _planes(w)

@@ -22,6 +22,7 @@ OP_GEMV_NF4 = 4
 OP_ARGCMP = 5
 OP_GEMV_Q8_0_Q8_1 = 6
 OP_GEMV_Q4_0_F32 = 7
+OP_GEMV_Q8_0_F32 = 8
 DTYPE_CODES = {torch.float16: 1, torch.bfloat16: 2, torch.float32: 3}
 MAX_M = 32
 Q8_1_BLOCK_BYTES = 36
@@ -380,6 +381,37 @@ def wobs_gemv_q8_0_q8_1(qs, d, xq, y=None, argmax=None, want_argmax=False, ws=No
     rc = lib.wobs_gemv_q8_0_q8_1(_ptr(qs), _ptr(d), _ptr(xq2), M, _ptr(y), _ptr(argmax), N, K,
                                  _ptr(ws), ws.numel() if ws is not None else 0,
                                  _stream(qs.device))
+    _check(rc, lib)
+    return y, argmax
+
+
+def wobs_gemv_q8_0_f32(qs, d, x, y=None, argmax=None, want_argmax=False, ws=None, xq_out=None):
+    """y[1, N] (fp32) from Q8_0 planes (qs int8 [N, K], d [N, K/32]) and one fp32 activation
+    vector x [K] (or [1, K]), quantised to Q8_1 inside the GEMV kernel; the Q8_1 blocks are
+    also written to ``xq_out`` (uint8, K/32*36 bytes) when it is given."""
+    lib = _lib.get()
+    _need(qs, "qs", torch.int8, 2)
+    _need(d, "d", torch.float16, 2, qs.device)
+    x1 = x.reshape(-1) if x.dim() == 2 and x.shape[0] == 1 else x
+    _need(x1, "x", torch.float32, 1, qs.device)
+    N, K = qs.shape
+    if x1.shape[0] != K or not x1.is_contiguous():
+        raise ValueError("x must be a contiguous fp32 vector of K elements")
+    if not (qs.is_contiguous() and d.is_contiguous()) or d.shape != (N, K // 32):
+        raise ValueError("qs/d must be contiguous planes [N, K] and [N, K/32]")
+    if y is None:
+        y = torch.empty(1, N, dtype=torch.float32, device=qs.device)
+    _need(y, "y", torch.float32, None, qs.device)
+    if argmax is None and want_argmax:
+        argmax = torch.empty(1, dtype=torch.int64, device=qs.device)
+    if xq_out is not None:
+        _need(xq_out, "xq_out", torch.uint8, None, qs.device)
+        if xq_out.numel() < (K // 32) * Q8_1_BLOCK_BYTES or not xq_out.is_contiguous():
+            raise ValueError("xq_out must be a contiguous uint8 buffer of K/32*36 bytes")
+    if ws is None:
+        ws = _auto_ws(OP_GEMV_Q8_0_F32, 1, N, K, qs.device, argmax)
+    rc = lib.wobs_gemv_q8_0_f32(_ptr(qs), _ptr(d), _ptr(x1), _ptr(xq_out), _ptr(y), _ptr(argmax), N, K,
+                                _ptr(ws), ws.numel() if ws is not None else 0, _stream(qs.device))
     _check(rc, lib)
     return y, argmax
 

@@ -36,6 +36,8 @@ SIGNATURES = {
                                     c_int, c_void_p, c_size_t, c_void_p]),
     "wobs_gemv_q4_0_f32": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                    c_int, c_int, c_void_p, c_size_t, c_void_p]),
+    "wobs_gemv_q8_0_f32": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                   c_int, c_int, c_void_p, c_size_t, c_void_p]),
     "wobs_quantize_q8_0": (c_int, [c_void_p, c_int64, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "wobs_gemv_q8_0_q8_1": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
                                     c_int, c_void_p, c_size_t, c_void_p]),

@@ -279,7 +279,8 @@ size_t wobs_workspace_size(int op, int M, int N, int K) {
     return (12ull * M + 15ull) & ~15ull;   // keys [M] (8 bytes), then counters [M] (4 bytes)
   }
   const bool known = (op >= WOBS_OP_GEMV_F16 && op <= WOBS_OP_GEMV_NF4) ||
-                     op == WOBS_OP_GEMV_Q8_0_Q8_1 || op == WOBS_OP_GEMV_Q4_0_F32;
+                     op == WOBS_OP_GEMV_Q8_0_Q8_1 || op == WOBS_OP_GEMV_Q4_0_F32 ||
+                     op == WOBS_OP_GEMV_Q8_0_F32;
   if (!known || M < 1 || M > WOBS_MAX_M || N < 1 || K < 1) return 0;
   return ws_layout(op, M, N, K).total;
 }
@@ -432,6 +433,27 @@ int wobs_gemv_q4_0_f32(const uint8_t* qs, const void* d, const float* X, void* x
   cudaError_t e = wobs::launch_gemv_q4_0_f32_fused(qs, d, X, xq_out, y, N, K, p.am,
                                                    static_cast<cudaStream_t>(stream), &L);
   return finish_launch(e, "gemv_q4_0_f32", M, N, K, L, 1);
+}
+
+int wobs_gemv_q8_0_f32(const int8_t* qs, const void* d, const float* X, void* xq_out, float* y,
+                       int64_t* argmax, int N, int K, void* ws, size_t ws_bytes, void* stream) {
+  const int M = 1;
+  if (!qs || !d || !X || !y) return fail(WOBS_ERR_INVALID_ARG, "gemv_q8_0_f32: null pointer");
+  if (xq_out && !aligned4(xq_out)) return fail(WOBS_ERR_MISALIGNED, "gemv_q8_0_f32: xq_out not 4-byte aligned");
+  if (N < 1 || K < 256 || (K % 256)) return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "gemv_q8_0_f32: N=%d K=%d (K must be a positive multiple of 256)", N, K);
+  if (!aligned16(X) || !aligned16(qs) || !aligned16(d) || !aligned4(y))
+    return fail(WOBS_ERR_MISALIGNED, "gemv_q8_0_f32: X, qs and d must be 16-byte aligned, y 4-byte aligned");
+  if (argmax && (reinterpret_cast<uintptr_t>(argmax) & 7u))
+    return fail(WOBS_ERR_MISALIGNED, "gemv_q8_0_f32: argmax not 8-byte aligned");
+  if (!wobs::q8_0_f32_fused_applies(K))
+    return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "gemv_q8_0_f32: K=%d too long for the shared-memory activation planes", K);
+  Prepared p;
+  int rc = prepare_ws(WOBS_OP_GEMV_Q8_0_F32, M, N, K, argmax, ws, ws_bytes, &p);
+  if (rc) return rc;
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_gemv_q8_0_f32_fused(qs, d, X, xq_out, y, N, K, p.am,
+                                                   static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "gemv_q8_0_f32", M, N, K, L, 1);
 }
 
 int wobs_quantize_q8_0(const float* W, int64_t ldw, int N, int K, int8_t* qs, void* d,

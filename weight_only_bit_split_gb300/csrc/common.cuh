@@ -150,6 +150,45 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
   return v;
 }
 
+// ------------------------------------------------ Q8_1 codes in a prologue
+
+// The IEEE float32 quotient, kept out of line: it is the rare fallback of
+// q8_1_codes and must not be evaluated (predicated) on the fast path.
+static __device__ __noinline__ float ieee_div(float x, float d) { return x / d; }
+
+// q = roundf(x / d) for four elements of one block, as the Q8_1 format
+// defines it (IEEE float32 quotient, then round half away from zero),
+// without a full division for almost every element.  For 2^-126 <= d <
+// 2^126, __fdividef(x, d) is within 2 ulp of the exact quotient (CUDA's
+// documented bound) and the IEEE quotient is within 0.5 ulp of it; with
+// |x / d| <= 127 (x is in the block whose maximum defines d) one ulp is at
+// most 2^-17, so both lie within 2^-14 of each other.  roundf changes value
+// only at the half-integers k + 1/2, so when the approximation is farther
+// than 2^-14 from the nearest one, both quotients round to the same
+// integer; otherwise (and for d outside the bound's range) the IEEE
+// division decides.
+__device__ __forceinline__ float q8_1_quotient(float x, float d, bool d_ok) {
+  const float t = __fdividef(x, d);
+  const float h = floorf(t) + 0.5f;
+  return (d_ok && fabsf(t - h) > 0x1p-14f) ? t : __int_as_float(0x7fc00000);   // NaN: decide exactly
+}
+__device__ __forceinline__ void q8_1_codes(const float4& v, float d, int& q0, int& q1, int& q2,
+                                           int& q3) {
+  const bool d_ok = d >= 0x1p-126f && d < 0x1p126f;
+  float t0 = q8_1_quotient(v.x, d, d_ok), t1 = q8_1_quotient(v.y, d, d_ok);
+  float t2 = q8_1_quotient(v.z, d, d_ok), t3 = q8_1_quotient(v.w, d, d_ok);
+  if (__builtin_expect(isnan(t0) || isnan(t1) || isnan(t2) || isnan(t3), 0)) {
+    if (isnan(t0)) t0 = ieee_div(v.x, d);
+    if (isnan(t1)) t1 = ieee_div(v.y, d);
+    if (isnan(t2)) t2 = ieee_div(v.z, d);
+    if (isnan(t3)) t3 = ieee_div(v.w, d);
+  }
+  q0 = static_cast<int>(roundf(t0));
+  q1 = static_cast<int>(roundf(t1));
+  q2 = static_cast<int>(roundf(t2));
+  q3 = static_cast<int>(roundf(t3));
+}
+
 // ------------------------------------------------------- argmax key
 
 // Greedy-argmax key: the float maps to an unsigned integer with the same

@@ -77,6 +77,11 @@ bool q4_0_f32_fused_applies(const void* d, int M, int K);
 cudaError_t launch_gemv_q4_0_f32_fused(const uint8_t* qs, const void* d, const float* x,
                                        void* xq_out, float* y, int N, int K, const ArgmaxArgs& am,
                                        cudaStream_t st, Launch* info);
+// Q8_1 quantisation fused into the Q8_0 M = 1 kernel (one launch).
+bool q8_0_f32_fused_applies(int K);
+cudaError_t launch_gemv_q8_0_f32_fused(const int8_t* qs, const void* d, const float* x,
+                                       void* xq_out, float* y, int N, int K, const ArgmaxArgs& am,
+                                       cudaStream_t st, Launch* info);
 // Multi-column (5..32) tcgen05 kernel: weights decoded into tensor memory,
 // block scales folded into f16 operands.  The plan fixes the K range of a
 // work unit, the split count (K / range) and the grid.

@@ -89,13 +89,67 @@ __device__ __forceinline__ int q8_dot16(uint4 w, int4 x) {
   return s;
 }
 
+// Q8_1 quantisation of one fp32 activation vector into this kernel's
+// planes (code chunks in block order, fp16-rounded scales), every CTA the
+// whole vector, taking the quantiser's decisions: eight threads per 32-block,
+// four elements each, amax, d = amax / 127 in IEEE float32, q = roundf(x / d)
+// (q8_1_codes; 0 when d = 0).  Block b's 36-byte Q8_1 block is also written
+// to xq_out (when given) by CTA b mod grid.  All NT threads call this; nb is
+// a multiple of 8, so the shuffles and loop bounds are warp-uniform.
+template <int NT>
+__device__ __forceinline__ void q8_planes_from_f32(const float* __restrict__ X, int nb, int4* x_c,
+                                                   float* x_d, uint8_t* __restrict__ xq_out) {
+  constexpr int kGroups = NT / 8;
+  constexpr int kBatch = 4;
+  const int g = threadIdx.x >> 3, j = threadIdx.x & 7;
+  for (int b0 = g; b0 < nb; b0 += kBatch * kGroups) {
+    float4 v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int b = b0 + u * kGroups;
+      v[u] = b < nb ? *reinterpret_cast<const float4*>(X + 32 * b + 4 * j)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int b = b0 + u * kGroups;
+      if (b >= nb) break;                      // warp-uniform
+      float amax = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float d = amax / 127.0f;
+      int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+      if (d != 0.0f) q8_1_codes(v[u], d, q0, q1, q2, q3);
+      const uint32_t packed = (static_cast<uint32_t>(q0) & 0xFFu) |
+                              ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
+                              ((static_cast<uint32_t>(q2) & 0xFFu) << 16) |
+                              (static_cast<uint32_t>(q3) << 24);
+      reinterpret_cast<uint32_t*>(x_c)[8 * b + j] = packed;
+      if (j == 0) x_d[b] = __half2float(__float2half_rn(d));
+      if (xq_out != nullptr) {
+        int sum = q0 + q1 + q2 + q3;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
+          uint8_t* blk = xq_out + 36 * static_cast<int64_t>(b);
+          *reinterpret_cast<uint32_t*>(blk + 4 + 4 * j) = packed;
+          if (j == 0) {
+            const float sd = d * static_cast<float>(sum);
+            *reinterpret_cast<__half2*>(blk) = __halves2half2(__float2half_rn(d), __float2half_rn(sd));
+          }
+        }
+      }
+    }
+  }
+}
+
 // Columns [0, M) of this launch (M <= MC); xq, Y and the argmax state are
-// already offset to the launch's first column.
-template <int MC, bool kArgmax>
-__global__ void __launch_bounds__(Q8Shape<MC>::kThreads) q8_mc_cp_kernel(
+// already offset to the launch's first column.  kF32X (MC = 1): xq is the
+// fp32 activation vector, quantised in the prologue; W warps per CTA.
+template <int MC, bool kArgmax, bool kF32X = false, int W = Q8Shape<MC>::kWarps>
+__global__ void __launch_bounds__(W * 32) q8_mc_cp_kernel(
     const int8_t* __restrict__ qs, const uint16_t* __restrict__ dw, const uint8_t* __restrict__ xq,
-    int M, float* __restrict__ Y, int N, int K, ArgmaxArgs am) {
-  constexpr int W = Q8Shape<MC>::kWarps;
+    int M, float* __restrict__ Y, int N, int K, ArgmaxArgs am, uint8_t* __restrict__ xq_out) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int nb = K >> 5;
   const int lane = threadIdx.x & 31;
@@ -106,7 +160,7 @@ __global__ void __launch_bounds__(Q8Shape<MC>::kThreads) q8_mc_cp_kernel(
   const int rows_w = wg < N ? (N - 1 - wg) / total_warps + 1 : 0;
   const int T = rows_w * nseg;
   uint8_t* myring = smem + warp * (kRing * kSegBytes);
-  int4* x_c = reinterpret_cast<int4*>(smem + Q8Shape<MC>::kRingBytes);    // [MC][2 nb] code chunks
+  int4* x_c = reinterpret_cast<int4*>(smem + W * kRing * kSegBytes);     // [MC][2 nb] code chunks
   float* x_d = reinterpret_cast<float*>(x_c + 2 * MC * nb);                 // [MC][nb] scales
 
   int prow = wg, pseg = 0;   // next segment to request
@@ -133,6 +187,9 @@ __global__ void __launch_bounds__(Q8Shape<MC>::kThreads) q8_mc_cp_kernel(
   }
   pdl_launch_dependents();
   pdl_wait();
+  if constexpr (kF32X) {
+    q8_planes_from_f32<W * 32>(reinterpret_cast<const float*>(xq), nb, x_c, x_d, xq_out);
+  } else {
   for (int i = threadIdx.x; i < MC * nb; i += W * 32) {
     const int m = i / nb, b = i - m * nb;
     if (m < M) {
@@ -145,6 +202,7 @@ __global__ void __launch_bounds__(Q8Shape<MC>::kThreads) q8_mc_cp_kernel(
       x_c[2 * i] = make_int4(0, 0, 0, 0);
       x_c[2 * i + 1] = make_int4(0, 0, 0, 0);
     }
+  }
   }
   __syncthreads();
 
@@ -241,7 +299,35 @@ cudaError_t run_t(const int8_t* qs, const uint16_t* d, const uint8_t* xq, int M,
   info->block = W * 32;
   info->smem = smem;
   info->kernel = "q8_0_q8_1_mc_cp";
-  return launch_k(kern, dim3(grid), dim3(W * 32), smem, st, true, qs, d, xq, M, Y, N, K, am);
+  return launch_k(kern, dim3(grid), dim3(W * 32), smem, st, true, qs, d, xq, M, Y, N, K, am,
+                  static_cast<uint8_t*>(nullptr));
+}
+
+// The fused entry: 32 warps and one CTA per SM (each SM quantises x once)
+// when the ring and planes fit, else 16 warps and two CTAs per SM.
+template <bool kArgmax, int W>
+cudaError_t run_fused_t(const int8_t* qs, const uint16_t* d, const float* x, uint8_t* xq_out,
+                        float* Y, int N, int K, const ArgmaxArgs& am, cudaStream_t st,
+                        Launch* info) {
+  const int smem = W * kRing * kSegBytes + (K / 32) * 36;
+  auto kern = q8_mc_cp_kernel<1, kArgmax, true, W>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int grid = (W >= 32 ? 1 : 2) * device_sm_count();
+  if (grid > N) grid = N;
+  info->grid_x = grid;
+  info->block = W * 32;
+  info->smem = smem;
+  info->kernel = "q8_0_f32_m1_cp";
+  return launch_k(kern, dim3(grid), dim3(W * 32), smem, st, true, qs, d,
+                  reinterpret_cast<const uint8_t*>(x), 1, Y, N, K, am, xq_out);
+}
+
+int fused_warps(int K) {
+  if (32 * kRing * kSegBytes + (K / 32) * 36 <= 220 * 1024) return 32;
+  // 1 KB left for the kernel's static shared memory (argmax keys)
+  if (16 * kRing * kSegBytes + (K / 32) * 36 <= optin_smem() - 1024) return 16;
+  return 0;
 }
 
 template <int MC>
@@ -263,6 +349,22 @@ cudaError_t launch_quantize_q8_0(const float* W, int64_t ldw, int N, int K, int8
   q8_0_quant_kernel<<<static_cast<unsigned>(grid), kQThreads, 0, st>>>(W, ldw, N, K, qs,
                                                                         static_cast<__half*>(d));
   return cudaGetLastError();
+}
+
+bool q8_0_f32_fused_applies(int K) { return fused_warps(K) > 0; }
+
+cudaError_t launch_gemv_q8_0_f32_fused(const int8_t* qs, const void* d, const float* x,
+                                       void* xq_out, float* y, int N, int K, const ArgmaxArgs& am,
+                                       cudaStream_t st, Launch* info) {
+  const int w = fused_warps(K);
+  if (w == 0) return cudaErrorNotSupported;
+  const uint16_t* dp = static_cast<const uint16_t*>(d);
+  uint8_t* xo = static_cast<uint8_t*>(xq_out);
+  if (w == 32)
+    return am.out ? run_fused_t<true, 32>(qs, dp, x, xo, y, N, K, am, st, info)
+                  : run_fused_t<false, 32>(qs, dp, x, xo, y, N, K, am, st, info);
+  return am.out ? run_fused_t<true, 16>(qs, dp, x, xo, y, N, K, am, st, info)
+                : run_fused_t<false, 16>(qs, dp, x, xo, y, N, K, am, st, info);
 }
 
 int q8_0_columns_per_launch(int K) {
