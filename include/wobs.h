@@ -33,11 +33,15 @@
  *     give 16-byte aligned rows; violations return WOBS_ERR_MISALIGNED.
  *   - Workspace: calls that take (ws, ws_bytes) need at least
  *     wobs_workspace_size(op, M, N, K) bytes, ZERO-FILLED before its first
- *     use.  Every call that returns WOBS_OK leaves it zero-filled again
- *     (counters and argmax keys are reset by the last arrival, and split-K
- *     partials are cleared by the warp that adds them up), so one zeroing
- *     serves any number of calls, whatever their shapes.  Calls that overlap on the GPU must not share one
- *     workspace.  Size 0 means no workspace is needed (ws may be NULL).
+ *     use.  Its first WOBS_WS_ZERO_BYTES bytes (or all of it, if smaller)
+ *     hold arrival counters and argmax keys; every call that returns
+ *     WOBS_OK leaves them zero again (reset by the last arrival).  Bytes
+ *     past that offset are split-K partials: scratch that a call writes
+ *     before it reads, which may be left non-zero.  So one zeroing serves
+ *     any number of calls, whatever their shapes.  Split-K calls support
+ *     N up to 1048576 rows (WOBS_ERR_UNSUPPORTED_SHAPE beyond).  Calls that
+ *     overlap on the GPU must not share one workspace.  Size 0 means no
+ *     workspace is needed (ws may be NULL).
  *   - Environment: WOBS_DEBUG=1 logs every dispatch (op, shape, kernel,
  *     grid, split) to stderr; WOBS_SPLITK=<s> overrides the split-K factor
  *     of the dense and Q4_0 multi-column kernels (testing only; the
@@ -89,6 +93,9 @@ extern "C" {
 #define WOBS_DTYPE_F16 1
 #define WOBS_DTYPE_BF16 2
 #define WOBS_DTYPE_F32 3
+
+/* Leading workspace bytes that hold counters and keys (zero between calls). */
+#define WOBS_WS_ZERO_BYTES 262408
 
 /* Largest activation-column count of the multi-column entry points. */
 #define WOBS_MAX_M 32

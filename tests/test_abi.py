@@ -224,3 +224,20 @@ def test_q8_0_f32_argument_checks():
     assert rc == -2
     rc, msg = _status(g, FAKE16, FAKE16, FAKE16, None, FAKE16, FAKE16, 8, 256, None, 0, None)
     assert rc == -1 and "workspace" in msg
+
+
+def test_workspace_counter_region_and_split_k_row_limit(monkeypatch):
+    """Split-K partials start past a fixed counter region of WOBS_WS_ZERO_BYTES,
+    so no call's counters can fall on another call's partials; split-K calls
+    beyond 2^20 rows are refused before any launch."""
+    lib = _lib.get()
+    src = open(HEADER).read()
+    zero = int(re.search(r"#define WOBS_WS_ZERO_BYTES (\d+)", src).group(1))
+    from weight_only_bit_split_gb300 import WS_ZERO_BYTES
+    assert zero == WS_ZERO_BYTES == 264 + 4 * 65536
+    monkeypatch.setenv("WOBS_SPLITK", "2")
+    assert lib.wobs_workspace_size(3, 1, 4096, 4096) >= zero + 4 * 2 * 4096
+    n = (1 << 20) + 16
+    rc, msg = _status("wobs_gemv_q4_0_q8_1", FAKE16, FAKE16, FAKE16, 1, FAKE16, None, n, 4096,
+                      FAKE16, 1 << 30, None)
+    assert rc == -3 and "rows" in msg

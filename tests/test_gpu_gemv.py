@@ -140,7 +140,7 @@ def test_gemv_bf16_workspace_is_left_clean_and_reusable():
         for _ in range(3):
             lg, am = wobs.wobs_gemv_bf16(w, x, want_argmax=True, ws=ws)
             assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(lg.cpu().numpy()))
-            assert int(ws.count_nonzero()) == 0
+            assert int(ws[:wobs.WS_ZERO_BYTES].count_nonzero()) == 0
 
 
 @pytest.mark.parametrize("splits", ["2", "3", "7"])
@@ -269,10 +269,10 @@ def test_q4_0_multi_column_paths_agree_exactly(monkeypatch, capfd):
     assert kernels == expect, kernels
 
 
-@pytest.mark.parametrize("m,n,k", [(25, 4096, 4096), (32, 6144, 4096), (32, 2048, 14336), (26, 19000, 2048),
+@pytest.mark.parametrize("m,n,k", [(17, 4096, 4096), (32, 6144, 4096), (32, 2048, 14336), (26, 19000, 2048),
                                    (32, 600, 768)])
 def test_q4_0_tensor_memory_kernel_dispatch_and_parity(m, n, k, monkeypatch, capfd):
-    """Shapes with 25..32 columns that fill the GPU take the tcgen05 kernel by
+    """Shapes with 17..32 columns that fill the GPU take the tcgen05 kernel by
     default (K split into ranges of 1024 or 768 elements: 1, 2, 4 and 14
     splits here; 600 x 768 is forced); outputs within the bound, argmax exact,
     the workspace left zero."""
@@ -288,9 +288,33 @@ def test_q4_0_tensor_memory_kernel_dispatch_and_parity(m, n, k, monkeypatch, cap
     err = assert_within(yn, ref, ad, "f32", f"q4_0 tc M={m} {n}x{k}")
     assert err < 1e-4
     assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
-    assert int(ws.count_nonzero()) == 0
+    assert int(ws[:wobs.WS_ZERO_BYTES].count_nonzero()) == 0
     log = capfd.readouterr().err
     assert "kernel=q4_0_q8_1_tc" in log, log
+
+
+def test_one_workspace_across_split_k_layouts(monkeypatch):
+    """One workspace serves calls whose split-K layouts differ: the tcgen05
+    kernel leaves its partials in place, and the next calls (other ops, other
+    row counts) still find their counters zero and compute correct results."""
+    n_big = 6144
+    ws = torch.zeros(1 << 25, dtype=torch.uint8, device=dev())
+    cases = [("tc", 32, n_big, 4096), ("mma", 8, 9000, 2048), ("tc", 27, 2048, 14336),
+             ("mma", 12, 517, 2048), ("tc", 32, n_big, 4096)]
+    for path, m, n, k in cases:
+        monkeypatch.setenv("WOBS_Q4TC", "1" if path == "tc" else "0")
+        assert wobs.wobs_workspace_size(wobs.OP_GEMV_Q4_0_Q8_1, m, n, k) <= ws.numel()
+        (qs, d, xq), ref, ad, _ = _q4_case(n, k, m, seed_copy=m)
+        y, am = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq, want_argmax=True, ws=ws)
+        yn = y.cpu().numpy()
+        assert_within(yn, ref, ad, "f32", f"shared workspace {path} M={m} {n}x{k}")
+        assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yn))
+        assert int(ws[:wobs.WS_ZERO_BYTES].count_nonzero()) == 0
+    lg, amb = wobs.wobs_gemv_bf16(synth.weights(5, (3000, 512), dtype=torch.bfloat16).to(dev()),
+                                  synth.activations(5, (4, 512), copy=4, dtype=torch.bfloat16).to(dev()),
+                                  want_argmax=True, ws=ws)
+    assert np.array_equal(amb.cpu().numpy(), oracle.argmax_rows(lg.cpu().numpy()))
+    assert int(ws[:wobs.WS_ZERO_BYTES].count_nonzero()) == 0
 
 
 @pytest.mark.parametrize("splits", ["2", "5", "64"])

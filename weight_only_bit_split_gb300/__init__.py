@@ -23,6 +23,8 @@ OP_ARGCMP = 5
 OP_GEMV_Q8_0_Q8_1 = 6
 OP_GEMV_Q4_0_F32 = 7
 OP_GEMV_Q8_0_F32 = 8
+# leading workspace bytes that hold counters and keys: zero between calls
+WS_ZERO_BYTES = 262408
 DTYPE_CODES = {torch.float16: 1, torch.bfloat16: 2, torch.float32: 3}
 MAX_M = 32
 Q8_1_BLOCK_BYTES = 36
@@ -123,8 +125,10 @@ def _auto_ws(op, M, N, K, device, argmax):
 def workspace(op, M, N, K, device=None):
     """A zero-filled workspace for (op, M, N, K) on the current stream.
 
-    Cached per (device, stream) and grown as needed; the library leaves it
-    zero-filled after every successful call, so it is reused as is.  Calls
+    Cached per (device, stream) and grown as needed; the library leaves its
+    counter region (the first WS_ZERO_BYTES bytes) zero after every
+    successful call and overwrites split-K partials before reading them, so
+    it is reused as is.  Calls
     that may overlap on the GPU should run on different streams.
     """
     device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())

@@ -50,6 +50,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 constexpr int kRowsPerGroup = 16;    // smallest row group of the multi-column kernels
+// Split-K counters live in a fixed region (room for N up to 16 * kMaxGroups
+// rows) and every call's partials start past it, so no call's counters can
+// fall where another call left partials: only the header and the counter
+// region must stay zero between calls.
+constexpr int kMaxGroups = 65536;
 
 struct WsLayout {
   size_t counter = 0, keys = 0, groups = 0, partials = 0, total = 0;
@@ -67,7 +72,7 @@ WsLayout ws_layout(int op, int M, int N, int K) {
   L.keys = off;
   off += 8 * WOBS_MAX_M;
   L.groups = off;
-  off += 4 * static_cast<size_t>(L.ngroups);
+  off += 4 * static_cast<size_t>(L.splits > 1 ? kMaxGroups : 0);
   off = (off + 255) & ~static_cast<size_t>(255);
   L.partials = off;
   if (L.splits > 1) {
@@ -100,6 +105,9 @@ struct Prepared {
 int prepare_ws(int op, int M, int N, int K, int64_t* argmax, void* ws, size_t ws_bytes,
                Prepared* out) {
   const WsLayout L = ws_layout(op, M, N, K);
+  if (L.ngroups > kMaxGroups)
+    return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "N=%d: split-K calls support at most %d rows", N,
+                16 * kMaxGroups);
   const bool need = argmax != nullptr || L.splits > 1;
   out->sk = wobs::SplitArgs{nullptr, nullptr, L.splits};
   out->am = wobs::ArgmaxArgs{nullptr, nullptr, nullptr};
@@ -239,7 +247,8 @@ int choose_splits(int op, int M, int N, int K) {
 
 size_t workspace_layout(int op, int M, int N, int K, size_t* zero_prefix_bytes) {
   const WsLayout L = ws_layout(op, M, N, K);
-  if (zero_prefix_bytes) *zero_prefix_bytes = L.partials;
+  // the bytes this call needs zero: header and its own group counters
+  if (zero_prefix_bytes) *zero_prefix_bytes = L.groups + 4 * static_cast<size_t>(L.ngroups);
   return L.total;
 }
 

@@ -377,8 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
   if (S > 1 && !s_abort) {
     // Split K: one arrival per unit; the CTA that completes a tile adds its
     // splits in split order, all 448 threads over the tile's M x 128
-    // outputs (each with its splits' loads in flight), and leaves the
-    // partials zero.  s_abort no longer changes: every role is done.
+    // outputs (each with its splits' loads in flight).  The partials are
+    // scratch (written before they are read, never taken for counters), so
+    // they are not cleared.  s_abort no longer changes: every role is done.
     for (int u = threadIdx.x; u < my_units; u += kThreads) {
       const int tile = tile0 + u * tstep;
       const unsigned prev = atomicAdd(sk.counters + tile, 1u);
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
     __syncthreads();
     __threadfence();
     // per thread at most kE outputs of a tile; loads of four splits of all
-    // of them are in flight together, then the zero stores, then the outputs
+    // of them are in flight together, then the outputs
     constexpr int kE = (BN * kRows + kThreads - 1) / kThreads;
     const int64_t sstride = static_cast<int64_t>(ntiles) * (BN * kRows);
     for (int u = 0; u < my_units; ++u) {
@@ -412,12 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
         for (int b = 0; b < 4; ++b)
 #pragma unroll
           for (int i = 0; i < kE; ++i) v[i] += t[b][i];
-      }
-#pragma unroll
-      for (int i = 0; i < kE; ++i) {
-        const int e = threadIdx.x + i * kThreads;
-        if (e < M * kRows)
-          for (int sp = 0; sp < S; ++sp) __stcg(const_cast<float*>(pt) + sp * sstride + e, 0.f);
       }
 #pragma unroll
       for (int i = 0; i < kE; ++i) {
@@ -503,14 +498,12 @@ bool q4_tc_forced() {
 
 // Work plan: the K range of a unit is the largest of 1024, 768, 512, 256
 // elements that divides K; the grid is a multiple of the split count so
-// each CTA keeps one K range.  By default the kernel takes 25 to 32 columns
-// when the units can occupy at least half of the SMs: measured on GB300
-// against the mma.sync kernel it is faster there (32 columns: 12.7 vs
-// 16.5 us on 4096 x 4096, 25.7 vs 28.9 us on 14336 x 4096), even at 24
-// (12.0 / 23.9 against 12.7 / 22.9 us) and slower below (8 columns: 9.5 vs
-// 7.5 us, 18.7 vs 13.7 us), where the split-K partials,
-// their reduction and the zeroing that keeps the workspace clean cost more
-// than the per-block scaling saved.  WOBS_Q4TC=1 takes it from 5 columns.
+// each CTA keeps one K range.  By default the kernel takes 17 to 32 columns
+// when the units can occupy at least half of the SMs.  Measured on GB300
+// against the mma.sync kernel (4096 x 4096 / 14336 x 4096, us): 32 columns
+// 10.9 / 20.9 against 16.4 / 29.0; 24 columns 10.7 / 20.2 against
+// 12.8 / 22.8; 16 columns 9.2 / 17.8 against 9.8 / 17.2; 8 columns
+// 8.8 / 17.3 against 7.5 / 13.7.  WOBS_Q4TC=1 takes it from 5 columns.
 Q4TcPlan q4_tc_plan(int M, int N, int K) {
   Q4TcPlan p;
   if (M < 5 || M > WOBS_MAX_M || N < 1 || K < kSK || K % kSK) return p;
@@ -526,7 +519,7 @@ Q4TcPlan q4_tc_plan(int M, int N, int K) {
   const int groups = ntiles < per_split ? ntiles : per_split;
   p.grid = groups * p.splits;
   if ((ntiles + groups - 1) / groups > kMaxUnits) return Q4TcPlan{};
-  p.ok = q4_tc_forced() || (M > 24 && 2 * ntiles * p.splits >= sms);
+  p.ok = q4_tc_forced() || (M > 16 && 2 * ntiles * p.splits >= sms);
   return p;
 }
 
