@@ -242,9 +242,9 @@ __device__ __forceinline__ void argmax_publish(const uint64_t* cta_key, int ncol
 // Split-K arrival for one row group: returns true (in every thread) for
 // the CTA that arrives last among the `splits` CTAs of `group`; that CTA
 // resets the counter.  Call after the partial stores, from all threads.
-// Reads a split-K partial and leaves zero behind: after a call the whole
-// workspace is zero again, so a later call with another layout (whose
-// counters may fall where these partials were) starts from zeros.
+// Reads a split-K partial and leaves zero behind (the CUDA-core fallback
+// does so; partials lie past the counter region, so other kernels leave
+// them in place).
 __device__ __forceinline__ float take_partial(float* p) {
   const float v = __ldcg(p);
   __stcg(p, 0.f);

@@ -446,9 +446,7 @@ __global__ void __launch_bounds__(kMThreads, 1) dense_mma_kernel(const T* __rest
               d[n][0] += v[b][n].x; d[n][1] += v[b][n].y; d[n][2] += v[b][n].z; d[n][3] += v[b][n].w;
             }
         }
-        for (int sp = 0; sp < sk.splits; ++sp)
-#pragma unroll
-          for (int n = 0; n < NT; ++n) __stcg(pp + sp * tstride + f0 + n * 32, make_float4(0.f, 0.f, 0.f, 0.f));
+        // the partials are scratch (past the counter region): not cleared
       }
     }
     if (finish) {

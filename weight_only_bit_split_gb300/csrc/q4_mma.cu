@@ -405,14 +405,7 @@ __global__ void __launch_bounds__(Q4Shape<NT>::kThreads, NT == 1 ? 2 : 1) q4_mma
                 acc[r][n][2] += v[b][r][n].z; acc[r][n][3] += v[b][r][n].w;
               }
         }
-        for (int sp = 0; sp < sk.splits; ++sp) {
-          float4* pp = reinterpret_cast<float4*>(sk.partials) +
-                       (static_cast<int64_t>(sp) * ngr + grp) * (R * NT * 32) + lane;
-#pragma unroll
-          for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int n = 0; n < NT; ++n) __stcg(pp + (r * NT + n) * 32, make_float4(0.f, 0.f, 0.f, 0.f));
-        }
+        // the partials are scratch (past the counter region): not cleared
         emit(grp, acc);
 #pragma unroll
         for (int r = 0; r < R; ++r)
