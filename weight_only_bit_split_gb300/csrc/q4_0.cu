@@ -202,12 +202,14 @@ __global__ void __launch_bounds__(kThreads) q4_m1_kernel(const uint8_t* __restri
 // The warp-per-row computation with the weight stream staged through
 // shared memory by asynchronous copies (cp.async, 16 bytes per lane): each
 // warp owns a ring of kRing segments of kSegBlocks blocks (2048 bytes of
-// nibbles + 256 bytes of scales).  All kRing segments are requested before
+// nibbles + 256 bytes of scales).  The first segment is requested before
 // pdl_wait, so the stream starts while the previous kernel finishes; each
-// segment is refilled with the one kRing further on while the next is
-// consumed.  Reads from the ring are lane-contiguous 16-byte loads (no bank
-// conflicts).  16 warps per CTA and two CTAs per SM: the measured optimum
-// on GB300 between bytes in flight and warps available to consume them.
+// iteration requests the next segment into the slot consumed last, then
+// waits for the current one.  Reads from the ring are lane-contiguous
+// 16-byte loads (no bank conflicts).  16 warps per CTA and two CTAs per SM
+// for Q8_1 input (the measured optimum on GB300 between bytes in flight and
+// warps available to consume them); 32 warps and one CTA per SM when the CTA
+// quantises fp32 activations itself.
 constexpr int kCpWarps = 16;
 constexpr int kCpThreads = kCpWarps * 32;
 constexpr int kSegBlocks = 128;
@@ -332,7 +334,6 @@ __global__ void __launch_bounds__(W * 32) q4_m1_cp_kernel(const uint8_t* __restr
     if (i < T) issue(i);
     cp_async_commit();
   }
-  // this CTA has started: after the matching wait, peers may store into its planes
   pdl_launch_dependents();
   pdl_wait();
   if constexpr (kF32X) {
