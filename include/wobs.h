@@ -52,7 +52,11 @@
  *     wobs_argmin.  WOBS_NF4=cp selects the CUDA-core NF4 kernel,
  *     WOBS_NF4_P=0..3 sets how many code words in eight the tensor-core NF4
  *     kernel decodes in registers, and WOBS_NF4_STAGES=2..4 caps its copy
- *     ring (all three for measurements).
+ *     ring (all three for measurements).  WOBS_Q4TC=1 takes Q4_0 calls with
+ *     5..16 columns to the tcgen05 kernel as well (17..32 take it by
+ *     default where its plan fills the GPU), WOBS_Q4TC=0 keeps every Q4_0
+ *     call off it; WOBS_Q4F32=16 runs the fused quantise-and-GEMV kernel
+ *     with 16 warps and two CTAs per SM (testing only).
  */
 #ifndef WOBS_H
 #define WOBS_H
