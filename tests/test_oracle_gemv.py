@@ -252,3 +252,83 @@ def test_q8_0_q8_1_closed_forms():
     x8 = np.arange(1, 33, dtype=np.int8)[None, :]
     y = oracle.gemv_q8_0_q8_1(qw2, np.ones((5, 1), np.float16), x8, np.ones((1, 1), np.float16))[0]
     assert y.tolist() == [float((n + 1) * (n + 1)) for n in range(5)]
+
+
+def _abs_dot_q8_0_fraction(qw, dw, q8, d8, m, n):
+    # sum over blocks b and lanes i of |dw[n, b] qw[n, i]| * |d8[m, b] q8[m, i]|,
+    # term by term in exact rationals
+    acc = Fraction(0)
+    for kk in range(qw.shape[1]):
+        b = kk // 32
+        wv = Fraction(float(dw[n, b])) * int(qw[n, kk])
+        xv = Fraction(float(d8[m, b])) * int(q8[m, kk])
+        acc += abs(wv) * abs(xv)
+    return acc
+
+
+def _abs_dot_q8_0_signed_then_abs(qw, dw, q8, d8):
+    # a plausible mistake planted in a copy of the oracle: |.| taken after
+    # the signed dot instead of on every term
+    return np.abs(oracle.gemv_q8_0_q8_1(qw, dw, q8, d8))
+
+
+def _abs_dot_q8_0_scale_dropped(qw, dw, q8, d8):
+    # the other plausible mistake: the weight scale's magnitude left out
+    return oracle.gemv_q8_0_q8_1(np.abs(qw.astype(np.int16)).astype(np.int8), np.ones_like(dw),
+                                 np.abs(q8.astype(np.int16)).astype(np.int8), np.abs(d8))
+
+
+def _cancelling_q8_0_case():
+    # signed terms that cancel inside each block (codes +c / -c against equal
+    # activation codes) and negative scales: the signed dot is 0, the sum of
+    # magnitudes is not
+    rng = np.random.default_rng(41)
+    n, k, m = 3, 96, 2
+    half = rng.integers(1, 128, size=(n, k // 32, 16))
+    qw = np.concatenate([half, -half], axis=2).reshape(n, k).astype(np.int8)
+    q8 = np.ones((m, k), np.int8) * np.int8(5)
+    q8[1] = -q8[1]
+    dw = np.asarray([[0.5, -0.25, 2.0], [-1.0, 0.125, -0.5], [3.0, -3.0, 0.75]], np.float16)
+    d8 = np.asarray([[0.25, -1.0, 0.5], [-0.125, 2.0, -4.0]], np.float16)
+    return qw, dw, q8, d8
+
+
+def test_q8_0_q8_1_abs_dot_fractions_random_and_cancelling():
+    rng = np.random.default_rng(40)
+    qw = rng.integers(-127, 128, size=(4, 96)).astype(np.int8)
+    q8 = rng.integers(-127, 128, size=(3, 96)).astype(np.int8)
+    dw = (rng.standard_normal((4, 3)) * 0.01).astype(np.float16)   # signed on purpose
+    d8 = (rng.standard_normal((3, 3)) * 0.01).astype(np.float16)
+    for case in ((qw, dw, q8, d8), _cancelling_q8_0_case()):
+        a, b, c, d = case
+        got = oracle.abs_dot_q8_0_q8_1(a, b, c, d)
+        assert got.shape == (c.shape[0], a.shape[0])
+        for mm in range(c.shape[0]):
+            for nn in range(a.shape[0]):
+                ref = _abs_dot_q8_0_fraction(a, b, c, d, mm, nn)
+                assert abs(got[mm, nn] - float(ref)) <= 1e-13 * float(ref)
+    # the cancelling case has a zero signed dot in every output
+    a, b, c, d = _cancelling_q8_0_case()
+    assert np.all(oracle.gemv_q8_0_q8_1(a, b, c, d) == 0.0)
+
+
+def test_q8_0_q8_1_abs_dot_h8_worked_example():
+    # x = 64 ones -> Q8_1 codes 127, d8 = 129/16384 in both blocks.  Row 0:
+    # |h7 codes| sum 127+4+3+0+1+127+127 = 389 at dw = 1, then 32 codes 127 at
+    # dw = 129/16384; row 1: block 0 zero, block 1 |-127| + 31 * 32 = 1119 at
+    # dw = 129/16384
+    qw, dw = oracle.quantize_q8_0(_h8_inputs())
+    q8, d8, _ = oracle.quantize_q8_1(np.ones((1, 64), np.float32))
+    s = Fraction(129, 16384)
+    want = [389 * 127 * s + 32 * 127 * 127 * s * s, 1119 * 127 * s * s]
+    got = oracle.abs_dot_q8_0_q8_1(qw, dw, q8, d8)[0]
+    assert got.tolist() == [float(v) for v in want]
+
+
+def test_q8_0_q8_1_abs_dot_pins_catch_planted_mistakes():
+    a, b, c, d = _cancelling_q8_0_case()
+    for bad in (_abs_dot_q8_0_signed_then_abs, _abs_dot_q8_0_scale_dropped):
+        got = bad(a, b, c, d)
+        ref = np.asarray([[float(_abs_dot_q8_0_fraction(a, b, c, d, mm, nn)) for nn in range(a.shape[0])]
+                          for mm in range(c.shape[0])])
+        assert not np.allclose(got, ref, rtol=1e-6)
