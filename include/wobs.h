@@ -82,6 +82,7 @@ extern "C" {
 #define WOBS_ERR_WORKSPACE_TOO_SMALL (-4)
 #define WOBS_ERR_LAUNCH_FAILED (-5)       /* cudaGetLastError() after the launch */
 #define WOBS_ERR_CUDA (-6)                /* other CUDA runtime error (device query) */
+#define WOBS_ERR_DEVICE_TIMEOUT (-7)      /* wobs_error_word: a bounded device wait gave up */
 
 /* ---- ops for wobs_workspace_size ---- */
 #define WOBS_OP_GEMV_F16 1
@@ -166,11 +167,14 @@ WOBS_API int wobs_gemv_bf16(const void* W, int64_t ldw, const void* X, int64_t l
  * wobs_gemv_bf16 for callers that cannot give the library a workspace: the
  * same computation, outputs and argmax rule, with the workspace taken from a
  * fixed scratch array of WOBS_NOALLOC_SCRATCH_BYTES that the library keeps
- * in device memory.  The pages have no counterpart to this entry point; it
- * exists for code that may not allocate device memory when it calls the
- * GEMV -- code running inside a CUDA graph capture, engines that reserve all
- * their memory once at start-up through their own allocator, and plugins in
- * a host process that owns every device allocation.
+ * in device memory.  The pages have no counterpart to this entry point.
+ * It serves callers that may not allocate device memory at the point of the
+ * call: inference engines that reserve their whole memory budget once at
+ * start-up and hand it out through their own allocator (a further
+ * cudaMalloc can fail, or push them past the budget they planned for),
+ * plugins loaded into a host process that owns and accounts every device
+ * allocation, and latency-critical decode loops that cannot afford
+ * cudaMalloc/cudaFree, which may synchronise the device.
  *
  *   Arguments as wobs_gemv_bf16, without (ws, ws_bytes).  No cudaMalloc,
  *   cudaFree or other allocating call is made.
@@ -178,11 +182,15 @@ WOBS_API int wobs_gemv_bf16(const void* W, int64_t ldw, const void* X, int64_t l
  *     K)) exceeds WOBS_NOALLOC_SCRATCH_BYTES return
  *     WOBS_ERR_WORKSPACE_TOO_SMALL.
  *   - The first call made with a given device current looks up the scratch
- *     array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture.
- *   - Every call shares the one array: each call clears its counters and
- *     keys on `stream` before the kernel, and calls that may overlap on the
- *     GPU (unordered streams) race on the scratch and must not be issued.
+ *     array's device address (cudaGetSymbolAddress) and keeps it for the
+ *     life of the process; make that first call before any stream capture.
+ *     A cudaDeviceReset (or anything else that unloads the library's module
+ *     from the device) invalidates the kept address: do not call this entry
+ *     point on that device afterwards.
+ *   - Every call shares the one array and it keeps the last call's
+ *     contents: each call clears the counters and keys on `stream` before
+ *     its kernel, and calls that may overlap on the GPU (unordered streams
+ *     or threads) race on the scratch and must not be issued.
  *   - Every GPU that loads the library holds the array until the process
  *     exits.
  */
@@ -397,6 +405,10 @@ WOBS_API int wobs_q4_0_q8_1_blockdots(const uint8_t* qs, const void* xq, int M, 
  * Device error word: kernels that give up a bounded wait record a nonzero
  * code here instead of hanging.  Copies the word to *host_out (host pointer)
  * and clears it; synchronises `stream` to do so.  0 = no error.
+ * Returns WOBS_OK when the word was 0 and WOBS_ERR_DEVICE_TIMEOUT when it
+ * held a code (still copied to *host_out): a launch returns before its
+ * kernel runs, so a wait that gives up on the GPU can only be reported by
+ * this later, synchronising call.
  */
 WOBS_API int wobs_error_word(void* stream, int* host_out);
 

@@ -3,6 +3,8 @@ workspace) of each kernel path is a view inside a larger buffer whose guard
 regions hold a sentinel bit pattern, checked after the call; and the bounded-
 wait failure path, forced by the library's self test, leaves the context
 usable."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -11,7 +13,7 @@ import oracle
 import weight_only_bit_split_gb300 as wobs
 from parity import assert_within, dev, f16_to_dev, q4_inputs_from_oracle, to_dev, w_x_fp32
 from golden_io import nf4_codebook_fixture
-from weight_only_bit_split_gb300 import synth
+from weight_only_bit_split_gb300 import _lib, synth
 
 pytestmark = pytest.mark.gpu
 
@@ -140,6 +142,14 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     wobs.wobs_selftest_wait_timeout(2_000_000)          # about a millisecond
     assert wobs.wobs_error_word() == 3                   # recorded, then cleared by the read
     assert wobs.wobs_error_word() == 0
+    # through the C ABI the read reports the timeout as its status
+    lib = _lib.get()
+    word = ctypes.c_int(-1)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    wobs.wobs_selftest_wait_timeout(2_000_000)
+    assert lib.wobs_error_word(stream, ctypes.byref(word)) == wobs.ERR_DEVICE_TIMEOUT
+    assert word.value == 3 and "gave up" in lib.wobs_last_error().decode()
+    assert lib.wobs_error_word(stream, ctypes.byref(word)) == 0 and word.value == 0
     (qs, d, xq), ref, ad = _q4(300, 1024, 1)
     y, _ = wobs.wobs_gemv_q4_0_q8_1(qs, d, xq)
     assert_within(y.cpu().numpy(), ref, ad, "f32", "after the self test")

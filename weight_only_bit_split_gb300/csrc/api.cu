@@ -586,6 +586,9 @@ int wobs_error_word(void* stream, int* host_out) {
   if (!host_out) return fail(WOBS_ERR_INVALID_ARG, "error_word: null pointer");
   cudaError_t e = wobs::read_and_clear_error_word(static_cast<cudaStream_t>(stream), host_out);
   if (e != cudaSuccess) return cuda_fail(e, "error_word", WOBS_ERR_CUDA);
+  if (*host_out != 0)
+    return fail(WOBS_ERR_DEVICE_TIMEOUT, "error_word: a bounded device wait gave up (code %d)",
+                *host_out);
   g_err[0] = '\0';
   return WOBS_OK;
 }
