@@ -1,14 +1,20 @@
-"""The allocation-free bf16 GEMV entry point against the regular one.
+"""The allocation-free bf16 GEMV entry point, through the C ABI.
 
 wobs_gemv_bf16_noalloc serves callers that may not allocate device memory
-when they call the GEMV (inside a CUDA graph capture, or under an engine
-that owns every device allocation): its workspace is a fixed scratch array
-inside the library.  Here it is called through the C ABI directly, twice in
-a row per shape, and its logits and argmax are checked against
-wobs_gemv_bf16 with a caller-provided workspace.  This file is collected
-last and needs no state from other tests.
+when they call the GEMV (an engine that reserved its whole memory budget up
+front and owns every allocation, a plugin inside a host process that
+accounts all device memory): its workspace is a fixed scratch array inside
+the library.  Each shape is called twice in a row, so the second call runs
+on whatever the first left in the shared scratch; both results are checked
+against the fp64 oracle within the parity bound, their argmax against the
+oracle's argmax of the returned logits, and both against the regular entry
+point wobs_gemv_bf16 with a caller-provided workspace.  One shape splits K,
+so the scratch's split-K partials and counters are exercised.  This file is
+collected last and needs no state from other tests.
 """
 import ctypes
+import os
+import re
 
 import numpy as np
 import pytest
@@ -20,7 +26,15 @@ from weight_only_bit_split_gb300 import _lib, synth
 
 pytestmark = pytest.mark.gpu
 
-SCRATCH_BYTES = 4 << 20
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _scratch_bytes():
+    """WOBS_NOALLOC_SCRATCH_BYTES as the header defines it."""
+    text = open(os.path.join(ROOT, "include", "wobs.h")).read()
+    m = re.search(r"#define\s+WOBS_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "WOBS_NOALLOC_SCRATCH_BYTES not found in the header"
+    return int(m.group(1)) << int(m.group(2))
 
 
 def _noalloc(W, X, logits, argmax):
@@ -35,32 +49,48 @@ def _noalloc(W, X, logits, argmax):
     return rc, lib.wobs_last_error().decode()
 
 
-@pytest.mark.parametrize("m,n,k", [(1, 5000, 1024), (4, 3000, 2048), (32, 2000, 4096)])
-def test_noalloc_matches_workspace_entry_point_twice(m, n, k):
+# (M, N, K, split-K expected): the last shape has too few 256-row tiles to
+# fill the GPU, so K is split and the scratch holds partials past the counters
+SHAPES = [(1, 5000, 1024, False), (4, 3000, 2048, False), (32, 2000, 4096, False),
+          (4, 1000, 8192, True)]
+
+
+@pytest.mark.parametrize("m,n,k,splits", SHAPES)
+def test_noalloc_twice_against_the_oracle_and_the_workspace_entry_point(m, n, k, splits):
     dev = torch.device("cuda", 0)
+    need = wobs.wobs_workspace_size(wobs.OP_GEMV_BF16, m, n, k)
+    assert need <= _scratch_bytes()
+    if splits:
+        assert need > wobs.WS_ZERO_BYTES, "expected a split-K shape"
     W = synth.weights(5, (n, k), device=dev, dtype=torch.bfloat16)
     X = synth.activations(5, (m, k), copy=m, device=dev, dtype=torch.bfloat16)
-    assert wobs.wobs_workspace_size(wobs.OP_GEMV_BF16, m, n, k) <= SCRATCH_BYTES
-    ref_logits, ref_arg = wobs.wobs_gemv_bf16(W, X, want_argmax=True)
-    ref = ref_logits.cpu().numpy().astype(np.float64)
-    absdot = oracle.abs_dot_dense(W.float().cpu().numpy(), X.float().cpu().numpy())
-    bound = oracle.parity_bound(ref, absdot, "f32")
+    w64, x64 = W.float().cpu().numpy(), X.float().cpu().numpy()
+    y_ref = oracle.gemv_dense(w64, x64)
+    bound = oracle.parity_bound(y_ref, oracle.abs_dot_dense(w64, x64), "f32")
+    ws_logits, ws_arg = wobs.wobs_gemv_bf16(W, X, want_argmax=True)
+    ws_got = ws_logits.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(ws_got - y_ref) <= bound)
     for _ in range(2):
         logits = torch.full((m, n), float("nan"), dtype=torch.float32, device=dev)
         arg = torch.full((m,), -1, dtype=torch.int64, device=dev)
         rc, msg = _noalloc(W, X, logits, arg)
         assert rc == 0, msg
-        got = logits.cpu().numpy().astype(np.float64)
-        assert np.all(np.abs(got - ref) <= bound)
-        assert np.array_equal(arg.cpu().numpy(), ref_arg.cpu().numpy())
+        torch.cuda.synchronize()
+        got = logits.cpu().numpy()
+        assert np.all(np.abs(got.astype(np.float64) - y_ref) <= bound)
+        # the same kernel and split order as the workspace entry point
+        assert np.array_equal(got, ws_logits.cpu().numpy())
+        a = arg.cpu().numpy()
+        assert np.array_equal(a, oracle.argmax_rows(got))
+        assert np.array_equal(a, ws_arg.cpu().numpy())
 
 
 def test_noalloc_rejects_shapes_beyond_the_scratch():
     dev = torch.device("cuda", 0)
     m, n, k = 32, 8192, 4096
-    assert wobs.wobs_workspace_size(wobs.OP_GEMV_BF16, m, n, k) > SCRATCH_BYTES
+    assert wobs.wobs_workspace_size(wobs.OP_GEMV_BF16, m, n, k) > _scratch_bytes()
     W = torch.zeros(n, k, dtype=torch.bfloat16, device=dev)
     X = torch.zeros(m, k, dtype=torch.bfloat16, device=dev)
     logits = torch.empty(m, n, dtype=torch.float32, device=dev)
     rc, msg = _noalloc(W, X, logits, None)
-    assert rc == -4 and "scratch" in msg
+    assert rc == -4 and "scratch" in msg          # WOBS_ERR_WORKSPACE_TOO_SMALL

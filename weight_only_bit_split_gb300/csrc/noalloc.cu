@@ -1,11 +1,12 @@
 // wobs_gemv_bf16_noalloc: the bf16 GEMV with fused argmax, its workspace
 // taken from a fixed scratch array inside the library.
 //
-// Some callers cannot hand the library a workspace: code that runs while a
-// CUDA graph is being captured (a cudaMalloc there breaks the capture),
-// engines whose memory is carved up once at start-up by their own
-// allocator and that may not allocate again, and plugins loaded into a host
-// process that owns all device memory.  For them this entry point needs no
+// Some callers cannot hand the library a workspace because they may not
+// allocate device memory when they call it: inference engines that reserve
+// their whole memory budget at start-up and carve it up with their own
+// allocator, plugins inside a host process that owns every device
+// allocation, and decode loops that cannot pay for a cudaMalloc/cudaFree
+// (which may synchronise the device).  For them this entry point needs no
 // workspace argument and calls no allocating routine.
 //
 // The scratch is a file-scope __device__ array of kScratchBytes: every GPU
@@ -13,9 +14,10 @@
 // cannot use the array's name as a device address, so the device address is
 // looked up once per device with cudaGetSymbolAddress (on the first call
 // made with that device current; make that first call before any stream
-// capture).  All calls share the one array: the counters and keys are
-// cleared on the call's stream before every launch, and calls that overlap
-// on the GPU (different streams, no ordering) race on it.
+// capture) and kept: a cudaDeviceReset invalidates it.  All calls share the
+// one array, which keeps the last call's contents: the counters and keys
+// are cleared on the call's stream before every launch, and calls that
+// overlap on the GPU (different streams, no ordering) race on it.
 #include <mutex>
 
 #include "../../include/wobs.h"
