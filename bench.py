@@ -205,21 +205,57 @@ class ClockSampler:
 # ------------------------------------------------------------- timing
 
 
-def time_steps(cycle, singles, steps, stream):
-    """Run exactly ``steps`` steps: whole rotation cycles from one graph, then
-    single-step graphs for the remainder.  Milliseconds on ``stream``."""
-    q, r = divmod(steps, len(singles))
+class StepRunner:
+    """Replays exactly ``n`` steps from CUDA graphs: whole rotation cycles of
+    the weight copies from one graph, the remainder from one more graph
+    (captured once per remainder length), so any step count costs at most
+    q + 1 graph launches."""
+
+    def __init__(self, wl, stream):
+        self.wl, self.stream = wl, stream
+        self.cycle = capture(lambda: [wl.step(c) for c in range(wl.copies)], stream)
+        self.rest = {}
+
+    def _rest(self, r):
+        if r not in self.rest:
+            self.rest[r] = capture(lambda: [self.wl.step(c) for c in range(r)], self.stream)
+        return self.rest[r]
+
+    def replay(self, n):
+        q, r = divmod(n, self.wl.copies)
+        for _ in range(q):
+            self.cycle.replay()
+        if r:
+            self._rest(r).replay()
+
+    def prepare(self, n):
+        """Capture the remainder graph for ``n`` steps outside any timed region."""
+        r = n % self.wl.copies
+        if r:
+            self._rest(r)
+
+
+def time_steps(runner, steps, stream):
+    """Exactly ``steps`` steps between CUDA events on ``stream``: milliseconds."""
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(q):
-            cycle.replay()
-        for i in range(r):
-            singles[i].replay()
+        runner.replay(steps)
         e1.record(stream)
     e1.synchronize()
     return e0.elapsed_time(e1)
+
+
+class _GraphRunner:
+    """A single captured graph replayed ``n`` times (one call site over all copies)."""
+
+    def __init__(self, graph):
+        self.g = graph
+
+    def replay(self, n):
+        for _ in range(n):
+            self.g.replay()
 
 
 def packed(shapes, dtype, device):
@@ -1000,17 +1036,56 @@ ORACLE_FRACTION = {"q4_m1": 0.125, "q4_m1_2call": 0.125, "q4_m_sweep": 1 / 64, "
                    "lm_head": 1 / 256, "argcmp": 1 / 4, "q8_m1": 1 / 16, "q8_m1_2call": 1 / 16}
 
 
-def oracle_rate(cls, frac, min_seconds, max_steps=None):
-    """Run the oracle on a row sample until ``min_seconds`` pass; GB/s, steps, seconds."""
+def host_cpu():
+    """(usable host threads, CPU model name) of this machine."""
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    return n, model or "unknown"
+
+
+def oracle_rate(cls, frac, min_seconds, max_steps=None, threads=1):
+    """Run the oracle on a row sample until ``min_seconds`` pass; GB/s, steps, seconds.
+
+    With ``threads`` > 1 every host thread runs oracle steps on the same
+    (read-only) sample concurrently; numpy releases the interpreter lock
+    inside its array operations, so the threads use separate cores.
+    """
+    from concurrent.futures import ThreadPoolExecutor
     prep = cls.oracle_prepare(frac)
     t0 = time.perf_counter()
-    nbytes, steps = 0, 0
-    while True:
-        nbytes += cls.oracle_step(prep)
-        steps += 1
-        el = time.perf_counter() - t0
-        if el >= min_seconds or (max_steps is not None and steps >= max_steps):
-            break
+
+    def worker(_):
+        nbytes, steps = 0, 0
+        while True:
+            nbytes += cls.oracle_step(prep)
+            steps += 1
+            el = time.perf_counter() - t0
+            if el >= min_seconds or (max_steps is not None and steps >= max_steps):
+                return nbytes, steps
+
+    if threads <= 1:
+        nbytes, steps = worker(0)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            res = list(ex.map(worker, range(threads)))
+        nbytes, steps = sum(r[0] for r in res), sum(r[1] for r in res)
+    el = time.perf_counter() - t0
     return nbytes / el / 1e9, steps, el, nbytes
 
 
@@ -1018,36 +1093,47 @@ def oracle_rate(cls, frac, min_seconds, max_steps=None):
 
 
 def run_reference(args, cls, key, budget_s=90.0):
-    """The CPU oracle as the reference arm: rank 0 only, a row sample per step.
+    """The CPU oracle as the reference arm: rank 0 only, on all host threads.
 
-    The sample shrinks below the workload's default fraction when needed so
-    that warm-up plus timed steps take about ``budget_s`` seconds.
+    A step is one oracle step per host thread, all on the same row sample of
+    the workload, run concurrently (numpy releases the interpreter lock in
+    its array operations).  The sample shrinks below the workload's default
+    fraction when needed so that warm-up plus timed steps take about
+    ``budget_s`` seconds.
     """
+    from concurrent.futures import ThreadPoolExecutor
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    nthreads, cpu_model = host_cpu()
     frac = ORACLE_FRACTION[key]
-    t0 = time.perf_counter()
-    cls.oracle_step(cls.oracle_prepare(frac))
-    per_step = time.perf_counter() - t0
-    allowed = budget_s / max(1, args.steps + args.warmup)
-    if per_step > allowed:
-        frac *= allowed / per_step
-    prep = cls.oracle_prepare(frac)
-    for _ in range(args.warmup):
-        cls.oracle_step(prep)
-    t0 = time.perf_counter()
-    nbytes = 0
-    for _ in range(args.steps):
-        nbytes += cls.oracle_step(prep)
-    el = time.perf_counter() - t0
+    with ThreadPoolExecutor(max_workers=nthreads) as ex:
+        def par_step(prep):
+            return sum(ex.map(lambda _: cls.oracle_step(prep), range(nthreads)))
+
+        t0 = time.perf_counter()
+        par_step(cls.oracle_prepare(frac))
+        per_step = time.perf_counter() - t0
+        allowed = budget_s / max(1, args.steps + args.warmup)
+        if per_step > allowed:
+            frac *= allowed / per_step
+        prep = cls.oracle_prepare(frac)
+        for _ in range(args.warmup):
+            par_step(prep)
+        t0 = time.perf_counter()
+        nbytes = 0
+        for _ in range(args.steps):
+            nbytes += par_step(prep)
+        el = time.perf_counter() - t0
     gbs = nbytes / el / 1e9
-    sample = f"{frac:.4g} of each weight matrix's rows per step, full K, same seeds and distributions"
+    sample = (f"each step: {nthreads} host threads, each one oracle step on {frac:.4g} of each weight "
+              f"matrix's rows, full K, same seeds and distributions (numpy fp64)")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": cls.name, "oracle_row_fraction": frac},
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+                             "sample": sample, "cpu_model": cpu_model},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -1095,18 +1181,29 @@ def main(argv=None):
         for c in range(wl.copies):
             wl.step(c)
     stream.synchronize()
-    singles = [capture(lambda c=c: wl.step(c), stream) for c in range(wl.copies)]
-    cycle = capture(lambda: [wl.step(c) for c in range(wl.copies)], stream)
-    time_steps(cycle, singles, args.warmup, stream)
+    runner = StepRunner(wl, stream)
+    runner.prepare(args.warmup)
+    runner.prepare(args.steps)
+    time_steps(runner, args.warmup, stream)
 
-    barrier(device)
-    torch.cuda.synchronize(device)
+    # the timed region: exactly K steps, bracketed by a barrier and a device
+    # synchronise; repeated so that it spans enough wall time for the clock
+    # sampler (about 0.1 s), and the median region is reported
     clocks = ClockSampler(device)
     clocks.start()
-    ms = time_steps(cycle, singles, args.steps, stream)
-    torch.cuda.synchronize(device)
+    regions = []
+    while True:
+        barrier(device)
+        torch.cuda.synchronize(device)
+        regions.append(time_steps(runner, args.steps, stream))
+        torch.cuda.synchronize(device)
+        barrier(device)
+        # every rank stops after the same region (its decision taken from the slowest)
+        done = len(regions) >= 200 or (len(regions) >= 5 and sum(regions) >= 100.0)
+        if reduce_over_ranks(1.0 if done else 0.0, "max", device) > 0:
+            break
     clocks.stop()
-    barrier(device)
+    ms = statistics.median(regions)
     bytes_rank = wl.bytes_per_step() * args.steps
     gbs, ms_max = aggregate(bytes_rank, ms, device)
 
@@ -1116,9 +1213,9 @@ def main(argv=None):
     tot_b, tot_ms, launches = 0, 0.0, 0
     reps = max(3, min(20, 2000 // max(1, wl.copies)))
     for label, nbytes, fn in wl.kernel_calls():
-        gk = capture(lambda fn=fn: [fn(c) for c in range(wl.copies)], stream)
-        time_steps(gk, [gk], 2, stream)
-        t = time_steps(gk, [gk], reps, stream)
+        gk = _GraphRunner(capture(lambda fn=fn: [fn(c) for c in range(wl.copies)], stream))
+        time_steps(gk, 2, stream)
+        t = time_steps(gk, reps, stream)
         us = t * 1e3 / (reps * wl.copies)
         per_call[label] = {"us": round(us, 3), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
         tot_b += nbytes
@@ -1152,10 +1249,15 @@ def main(argv=None):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         frac = ORACLE_FRACTION[args.workload]
-        v, steps_done, el, _ = oracle_rate(cls, frac, 10.0, max_steps=200)
-        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{steps_done} oracle steps on {frac:.4g} of each weight matrix's rows "
-                         f"(full K, same seeds), {el:.1f} s, numpy fp64, one thread"}
+        nthreads, cpu_model = host_cpu()
+        v1, steps1, el1, _ = oracle_rate(cls, frac, 6.0, max_steps=200)
+        vn, stepsn, eln, _ = oracle_rate(cls, frac, 8.0, threads=nthreads)
+        cpu = {"value": vn, "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+               "sample": f"{stepsn} oracle steps over {nthreads} host threads, each on {frac:.4g} of "
+                         f"each weight matrix's rows (full K, same seeds), {eln:.1f} s, numpy fp64",
+               "one_core": {"value": v1, "unit": "GB/s", "cores": 1,
+                            "sample": f"{steps1} oracle steps, one thread, {el1:.1f} s"},
+               "nproc": nthreads, "cpu_model": cpu_model}
 
     if rank == 0:
         line = {
@@ -1181,6 +1283,11 @@ def main(argv=None):
                            "in a wobs.StepGraph and replayed every step: pinned H2D of the "
                            "activations, the step's launches, D2H of the outputs"},
             "gpu_launches": wl.launches_per_step * args.steps,
+            "timed_regions": {"count": len(regions), "ms_min": round(min(regions), 5),
+                              "ms_median": round(ms, 5), "ms_max": round(max(regions), 5),
+                              "how": "each region: exactly --steps steps between a barrier and "
+                                     "a device synchronise; value and ms_per_step use the median "
+                                     "region"},
             "clocks": clocks.report(),
         }
         print(json.dumps(line), flush=True)
