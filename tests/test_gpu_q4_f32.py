@@ -84,11 +84,14 @@ def test_fused_quantisation_edge_cases(variant):
 
 
 def _near_tie_vector(k, seed):
-    """Blocks whose quotients x / d sit on, or one float32 step either side
-    of, the half-integers where rounding to the nearest code changes: the
-    block maximum is 127 * 2^e (so d = 2^e exactly) and the other elements
-    are (j + 1/2) * 2^e, nudged by -1, 0 or +1 ulp, of both signs; every
-    fourth block is plain Gaussian."""
+    """Blocks whose quotients x / d sit on, or a few float32 steps either side
+    of, the half-integers where rounding to the nearest code changes.  Three
+    kinds of block in turn: the block maximum is 127 * 2^e (so d = 2^e
+    exactly) and the other elements are (j + 1/2) * 2^e, nudged by -1, 0 or
+    +1 ulp, of both signs; the block maximum is an arbitrary value (d not a
+    power of two) and the other elements are float32((j + 1/2) * d) nudged
+    by -3 ... +3 ulp, so the IEEE quotients land within a few ulp of the
+    half-integers on both sides; plain Gaussian blocks."""
     rng = np.random.default_rng(seed)
     x = np.empty(k, np.float32)
     for b in range(k // 32):
@@ -96,11 +99,22 @@ def _near_tie_vector(k, seed):
             x[32 * b:32 * b + 32] = rng.standard_normal(32).astype(np.float32)
             continue
         e = np.float32(2.0) ** int(rng.integers(-20, 5))   # d and s = d * sum(q) stay finite in fp16
-        half = (rng.integers(-127, 127, 31).astype(np.float32) + np.float32(0.5)) * e
-        nudge = rng.integers(-1, 2, 31)
-        half = np.where(nudge > 0, np.nextafter(half, np.float32(np.inf)),
-                        np.where(nudge < 0, np.nextafter(half, np.float32(-np.inf)), half))
-        blk = np.concatenate([[np.float32(127.0) * e * np.float32(rng.choice([-1, 1]))], half])
+        sign = np.float32(rng.choice([-1, 1]))
+        if b % 4 == 2:
+            amax = np.float32(127.0 * float(e) * (1.0 + 0.99 * rng.random()))
+            d = np.float32(amax) / np.float32(127.0)
+            half = ((rng.integers(-127, 127, 31) + 0.5) * np.float64(d)).astype(np.float32)
+            for _ in range(3):
+                step = rng.integers(-1, 2, 31)
+                half = np.where(step > 0, np.nextafter(half, np.float32(np.inf)),
+                                np.where(step < 0, np.nextafter(half, np.float32(-np.inf)), half))
+            blk = np.concatenate([[amax * sign], half])
+        else:
+            half = (rng.integers(-127, 127, 31).astype(np.float32) + np.float32(0.5)) * e
+            nudge = rng.integers(-1, 2, 31)
+            half = np.where(nudge > 0, np.nextafter(half, np.float32(np.inf)),
+                            np.where(nudge < 0, np.nextafter(half, np.float32(-np.inf)), half))
+            blk = np.concatenate([[np.float32(127.0) * e * sign], half])
         x[32 * b:32 * b + 32] = blk.astype(np.float32)[rng.permutation(32)]
     return x
 

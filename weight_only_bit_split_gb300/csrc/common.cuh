@@ -152,41 +152,110 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 
 // ------------------------------------------------ Q8_1 codes in a prologue
 
-// The IEEE float32 quotient, kept out of line: it is the rare fallback of
-// q8_1_codes and must not be evaluated (predicated) on the fast path.
-static __device__ __noinline__ float ieee_div(float x, float d) { return x / d; }
-
-// q = roundf(x / d) for four elements of one block, as the Q8_1 format
-// defines it (IEEE float32 quotient, then round half away from zero),
-// without a full division for almost every element.  For 2^-126 <= d <
-// 2^126, __fdividef(x, d) is within 2 ulp of the exact quotient (CUDA's
-// documented bound) and the IEEE quotient is within 0.5 ulp of it; with
-// |x / d| <= 127 (x is in the block whose maximum defines d) one ulp is at
-// most 2^-17, so both lie within 2^-14 of each other.  roundf changes value
-// only at the half-integers k + 1/2, so when the approximation is farther
-// than 2^-14 from the nearest one, both quotients round to the same
-// integer; otherwise (and for d outside the bound's range) the IEEE
-// division decides.
-__device__ __forceinline__ float q8_1_quotient(float x, float d, bool d_ok) {
-  const float t = __fdividef(x, d);
-  const float h = floorf(t) + 0.5f;
-  return (d_ok && fabsf(t - h) > 0x1p-14f) ? t : __int_as_float(0x7fc00000);   // NaN: decide exactly
+// TPB lanes per 32-element block (TPB = 2, 4 or 8 consecutive lanes; lane j
+// of the group holds elements 32/TPB * j ... 32/TPB * (j + 1) - 1), for the
+// quantising prologues.  The decisions are the Q8_1 format's: amax over the
+// block, d = amax / 127 as an IEEE float32 division, q = roundf(x / d) with
+// the IEEE quotient (0 when d = 0).  The quotient is formed as t = x * r
+// with r the hardware's approximate reciprocal of d (PTX rcp.approx: at most
+// 1 ulp from 1/d), so |t - x/d| <= |x/d| * (2^-23 + 2^-24) < 2^-15.4 for
+// |x/d| <= 127, while the IEEE quotient lies within half an ulp (<= 2^-18)
+// of x/d: the two are within 2^-15 of each other.  roundf changes value only
+// at the half-integers, so whenever t is farther than 2^-13 from every
+// half-integer, roundf(IEEE quotient) equals the nearest integer to t, which
+// is read off with the 1.5 * 2^23 addition (exact for |t| < 2^22: the sum's
+// low mantissa bits are the integer, its low byte the two's-complement
+// code).  Otherwise, and for d outside [2^-126, 2^126), the lane takes the
+// IEEE division for its elements.  No conversion-unit instruction
+// (float-to-int, rounding, division) is spent per element on the fast path.
+__device__ __forceinline__ float rcp_approx_ftz(float d) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+  return r;
 }
-__device__ __forceinline__ void q8_1_codes(const float4& v, float d, int& q0, int& q1, int& q2,
-                                           int& q3) {
+
+// Low bytes of four words, in order, as one word.
+__device__ __forceinline__ uint32_t pack_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
+template <int TPB>
+struct Q81Part {
+  static constexpr int kWords = 8 / TPB;   // code words (4 codes each) per lane
+  uint32_t codes[kWords];                  // this lane's codes in element order
+  float d;                                 // the block's scale (float32, before fp16 rounding)
+  int sum;                                 // exact sum of all 32 codes of the block
+};
+
+// All 32 lanes of the warp must call this (the group exchange is a
+// shuffle); lanes whose block does not exist pass zeros and discard the
+// result.
+template <int TPB>
+__device__ __forceinline__ Q81Part<TPB> q8_1_part_block(const float4 (&v)[8 / TPB]) {
+  constexpr int kW = 8 / TPB;
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kW; ++i)
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+#pragma unroll
+  for (int o = 1; o < TPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  Q81Part<TPB> h;
+  h.d = amax / 127.0f;
+  const float d = h.d;
   const bool d_ok = d >= 0x1p-126f && d < 0x1p126f;
-  float t0 = q8_1_quotient(v.x, d, d_ok), t1 = q8_1_quotient(v.y, d, d_ok);
-  float t2 = q8_1_quotient(v.z, d, d_ok), t3 = q8_1_quotient(v.w, d, d_ok);
-  if (__builtin_expect(isnan(t0) || isnan(t1) || isnan(t2) || isnan(t3), 0)) {
-    if (isnan(t0)) t0 = ieee_div(v.x, d);
-    if (isnan(t1)) t1 = ieee_div(v.y, d);
-    if (isnan(t2)) t2 = ieee_div(v.z, d);
-    if (isnan(t3)) t3 = ieee_div(v.w, d);
+  const float r = d_ok ? rcp_approx_ftz(d) : 0.0f;
+  constexpr float kRound = 12582912.0f;        // 1.5 * 2^23
+  float x[4 * kW];
+#pragma unroll
+  for (int i = 0; i < kW; ++i) {
+    x[4 * i] = v[i].x; x[4 * i + 1] = v[i].y; x[4 * i + 2] = v[i].z; x[4 * i + 3] = v[i].w;
   }
-  q0 = static_cast<int>(roundf(t0));
-  q1 = static_cast<int>(roundf(t1));
-  q2 = static_cast<int>(roundf(t2));
-  q3 = static_cast<int>(roundf(t3));
+  uint32_t bits[4 * kW];
+  bool ok = d_ok || d == 0.0f;                 // d == 0: r = 0, every code 0
+#pragma unroll
+  for (int i = 0; i < 4 * kW; ++i) {
+    const float t = __fmul_rn(x[i], r);
+    const float tm = __fadd_rn(t, kRound);
+    const float e = __fsub_rn(t, __fsub_rn(tm, kRound));
+    ok = ok && fabsf(e) < 0.5f - 0x1p-13f;
+    bits[i] = __float_as_uint(tm);
+  }
+  if (__builtin_expect(!ok, 0)) {
+#pragma unroll
+    for (int i = 0; i < 4 * kW; ++i)
+      bits[i] = static_cast<uint32_t>(d != 0.0f ? static_cast<int>(roundf(x[i] / d)) : 0);
+  }
+  int s = 0;
+#pragma unroll
+  for (int i = 0; i < kW; ++i) {
+    h.codes[i] = pack_low_bytes(bits[4 * i], bits[4 * i + 1], bits[4 * i + 2], bits[4 * i + 3]);
+    s = __dp4a(static_cast<int>(h.codes[i]), 0x01010101, s);
+  }
+#pragma unroll
+  for (int o = 1; o < TPB; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  h.sum = s;
+  return h;
+}
+
+// The lane group's share of the 36-byte Q8_1 block {fp16 d, fp16 d * sum,
+// int8 q[32]} (4-byte aligned stores); `j` is the lane's index in its group.
+template <int TPB>
+__device__ __forceinline__ void store_q8_1_part(uint8_t* blk, const Q81Part<TPB>& h, int j) {
+  constexpr int kW = 8 / TPB;
+  uint32_t* w = reinterpret_cast<uint32_t*>(blk + 4) + kW * j;
+#pragma unroll
+  for (int i = 0; i < kW; ++i) w[i] = h.codes[i];
+  if (j == 0)
+    *reinterpret_cast<__half2*>(blk) =
+        __halves2half2(__float2half_rn(h.d), __float2half_rn(h.d * static_cast<float>(h.sum)));
+}
+
+// Lanes per block for a prologue of NT threads over nb blocks: the most
+// lanes (shortest chain per lane) that still cover the vector in one pass,
+// two when no single pass does.
+template <int NT>
+__host__ __device__ constexpr int q8_1_lanes_per_block(int nb) {
+  return nb * 8 <= NT ? 8 : (nb * 4 <= NT ? 4 : 2);
 }
 
 // ------------------------------------------------------- argmax key

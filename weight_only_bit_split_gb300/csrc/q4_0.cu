@@ -228,62 +228,53 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 // Q8_1 quantisation of one fp32 activation vector straight into the
 // shared-memory planes of the M = 1 kernel (every CTA quantises the whole
-// vector).  The decisions are the quantiser's: eight threads per 32-block,
-// four elements each, amax over the block, d = amax / 127 in IEEE float32,
-// q = roundf(x / d) (q8_1_codes; 0 when d = 0), d widened back from its fp16
-// rounding, exact integer code sum -- so the planes hold exactly what
-// staging the stored Q8_1 blocks would.  Every thread of the CTA (NT of
-// them) calls this: the shuffles and the loop bounds are warp-uniform
-// because nb % 8 == 0 and a warp's four groups are consecutive.
+// vector).  The decisions are the quantiser's (q8_1_part_block: TPB lanes
+// per 32-block, amax, d = amax / 127 in IEEE float32, q = roundf(x / d), 0
+// when d = 0), d widened back from its fp16 rounding, exact integer code
+// sum -- so the planes hold exactly what staging the stored Q8_1 blocks
+// would.  Every thread of the CTA (NT of them) calls this with the same
+// trip count, so the group shuffles see whole warps.
+template <int NT, int TPB>
+__device__ __forceinline__ void q8_1_planes_tpb(const float* __restrict__ X, int nb, int4* x_lo,
+                                                int4* x_hi, float* x_d, int* x_s,
+                                                uint8_t* __restrict__ xq_out) {
+  constexpr int kPerPass = NT / TPB;           // blocks per pass
+  constexpr int kW = 8 / TPB;                  // code words per lane
+  const int j = threadIdx.x & (TPB - 1);
+  const int passes = (nb + kPerPass - 1) / kPerPass;
+  for (int p = 0; p < passes; ++p) {
+    const int b = p * kPerPass + static_cast<int>(threadIdx.x) / TPB;
+    const bool valid = b < nb;
+    float4 v[kW];
+    const float4* src = reinterpret_cast<const float4*>(X + 32 * b) + kW * j;
+#pragma unroll
+    for (int i = 0; i < kW; ++i) v[i] = valid ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const Q81Part<TPB> h = q8_1_part_block<TPB>(v);
+    if (!valid) continue;
+    // word w of the block's eight code words: words 0..3 in x_lo, 4..7 in x_hi
+#pragma unroll
+    for (int i = 0; i < kW; ++i) {
+      const int w = kW * j + i;
+      reinterpret_cast<uint32_t*>(w < 4 ? &x_lo[b] : &x_hi[b])[w & 3] = h.codes[i];
+    }
+    if (j == 0) {
+      x_d[b] = __half2float(__float2half_rn(h.d));
+      x_s[b] = h.sum;
+    }
+    // each 36-byte Q8_1 block written by one CTA
+    if (xq_out != nullptr && b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x))
+      store_q8_1_part<TPB>(xq_out + 36 * static_cast<int64_t>(b), h, j);
+  }
+}
+
 template <int NT>
 __device__ __forceinline__ void q8_1_planes_from_f32(const float* __restrict__ X, int nb, int4* x_lo,
                                                      int4* x_hi, float* x_d, int* x_s,
                                                      uint8_t* __restrict__ xq_out) {
-  constexpr int kGroups = NT / 8;
-  constexpr int kBatch = 4;                    // loads in flight per thread
-  const int g = threadIdx.x >> 3, j = threadIdx.x & 7;
-  for (int b0 = g; b0 < nb; b0 += kBatch * kGroups) {
-    float4 v[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int b = b0 + u * kGroups;
-      v[u] = b < nb ? *reinterpret_cast<const float4*>(X + 32 * b + 4 * j)
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int b = b0 + u * kGroups;
-      if (b >= nb) break;                      // warp-uniform
-      float amax = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float d = amax / 127.0f;
-      int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-      if (d != 0.0f) q8_1_codes(v[u], d, q0, q1, q2, q3);
-      int sum = q0 + q1 + q2 + q3;
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      const uint32_t packed = (static_cast<uint32_t>(q0) & 0xFFu) |
-                              ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
-                              ((static_cast<uint32_t>(q2) & 0xFFu) << 16) |
-                              (static_cast<uint32_t>(q3) << 24);
-      reinterpret_cast<int*>(j < 4 ? &x_lo[b] : &x_hi[b])[j & 3] = static_cast<int>(packed);
-      if (j == 0) {
-        x_d[b] = __half2float(__float2half_rn(d));
-        x_s[b] = sum;
-      }
-      // the 36-byte Q8_1 block {fp16 d, fp16 d * sum, codes}, each block
-      // written by one CTA
-      if (xq_out != nullptr && b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
-        uint8_t* blk = xq_out + 36 * static_cast<int64_t>(b);
-        *reinterpret_cast<uint32_t*>(blk + 4 + 4 * j) = packed;
-        if (j == 0) {
-          const float sd = d * static_cast<float>(sum);
-          *reinterpret_cast<__half2*>(blk) = __halves2half2(__float2half_rn(d), __float2half_rn(sd));
-        }
-      }
-    }
-  }
+  const int tpb = q8_1_lanes_per_block<NT>(nb);
+  if (tpb == 8) q8_1_planes_tpb<NT, 8>(X, nb, x_lo, x_hi, x_d, x_s, xq_out);
+  else if (tpb == 4) q8_1_planes_tpb<NT, 4>(X, nb, x_lo, x_hi, x_d, x_s, xq_out);
+  else q8_1_planes_tpb<NT, 2>(X, nb, x_lo, x_hi, x_d, x_s, xq_out);
 }
 
 // kF32X: xsrc is the fp32 activation vector, quantised to Q8_1 in the

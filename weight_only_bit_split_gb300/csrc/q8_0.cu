@@ -91,56 +91,43 @@ __device__ __forceinline__ int q8_dot16(uint4 w, int4 x) {
 
 // Q8_1 quantisation of one fp32 activation vector into this kernel's
 // planes (code chunks in block order, fp16-rounded scales), every CTA the
-// whole vector, taking the quantiser's decisions: eight threads per 32-block,
-// four elements each, amax, d = amax / 127 in IEEE float32, q = roundf(x / d)
-// (q8_1_codes; 0 when d = 0).  Block b's 36-byte Q8_1 block is also written
-// to xq_out (when given) by CTA b mod grid.  All NT threads call this; nb is
-// a multiple of 8, so the shuffles and loop bounds are warp-uniform.
+// whole vector, taking the quantiser's decisions (q8_1_part_block: TPB lanes
+// per 32-block, amax, d = amax / 127 in IEEE float32, q = roundf(x / d), 0
+// when d = 0).  Block b's 36-byte Q8_1 block is also written to xq_out (when
+// given) by CTA b mod grid.  All NT threads call this with the same trip
+// count, so the group shuffles see whole warps.
+template <int NT, int TPB>
+__device__ __forceinline__ void q8_planes_tpb(const float* __restrict__ X, int nb, int4* x_c,
+                                              float* x_d, uint8_t* __restrict__ xq_out) {
+  constexpr int kPerPass = NT / TPB;
+  constexpr int kW = 8 / TPB;
+  const int j = threadIdx.x & (TPB - 1);
+  const int passes = (nb + kPerPass - 1) / kPerPass;
+  for (int p = 0; p < passes; ++p) {
+    const int b = p * kPerPass + static_cast<int>(threadIdx.x) / TPB;
+    const bool valid = b < nb;
+    float4 v[kW];
+    const float4* src = reinterpret_cast<const float4*>(X + 32 * b) + kW * j;
+#pragma unroll
+    for (int i = 0; i < kW; ++i) v[i] = valid ? __ldg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const Q81Part<TPB> h = q8_1_part_block<TPB>(v);
+    if (!valid) continue;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(x_c) + 8 * b + kW * j;   // chunks 2b, 2b + 1
+#pragma unroll
+    for (int i = 0; i < kW; ++i) dst[i] = h.codes[i];
+    if (j == 0) x_d[b] = __half2float(__float2half_rn(h.d));
+    if (xq_out != nullptr && b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x))
+      store_q8_1_part<TPB>(xq_out + 36 * static_cast<int64_t>(b), h, j);
+  }
+}
+
 template <int NT>
 __device__ __forceinline__ void q8_planes_from_f32(const float* __restrict__ X, int nb, int4* x_c,
                                                    float* x_d, uint8_t* __restrict__ xq_out) {
-  constexpr int kGroups = NT / 8;
-  constexpr int kBatch = 4;
-  const int g = threadIdx.x >> 3, j = threadIdx.x & 7;
-  for (int b0 = g; b0 < nb; b0 += kBatch * kGroups) {
-    float4 v[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int b = b0 + u * kGroups;
-      v[u] = b < nb ? *reinterpret_cast<const float4*>(X + 32 * b + 4 * j)
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int b = b0 + u * kGroups;
-      if (b >= nb) break;                      // warp-uniform
-      float amax = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float d = amax / 127.0f;
-      int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-      if (d != 0.0f) q8_1_codes(v[u], d, q0, q1, q2, q3);
-      const uint32_t packed = (static_cast<uint32_t>(q0) & 0xFFu) |
-                              ((static_cast<uint32_t>(q1) & 0xFFu) << 8) |
-                              ((static_cast<uint32_t>(q2) & 0xFFu) << 16) |
-                              (static_cast<uint32_t>(q3) << 24);
-      reinterpret_cast<uint32_t*>(x_c)[8 * b + j] = packed;
-      if (j == 0) x_d[b] = __half2float(__float2half_rn(d));
-      if (xq_out != nullptr) {
-        int sum = q0 + q1 + q2 + q3;
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x)) {
-          uint8_t* blk = xq_out + 36 * static_cast<int64_t>(b);
-          *reinterpret_cast<uint32_t*>(blk + 4 + 4 * j) = packed;
-          if (j == 0) {
-            const float sd = d * static_cast<float>(sum);
-            *reinterpret_cast<__half2*>(blk) = __halves2half2(__float2half_rn(d), __float2half_rn(sd));
-          }
-        }
-      }
-    }
-  }
+  const int tpb = q8_1_lanes_per_block<NT>(nb);
+  if (tpb == 8) q8_planes_tpb<NT, 8>(X, nb, x_c, x_d, xq_out);
+  else if (tpb == 4) q8_planes_tpb<NT, 4>(X, nb, x_c, x_d, xq_out);
+  else q8_planes_tpb<NT, 2>(X, nb, x_c, x_d, xq_out);
 }
 
 // Columns [0, M) of this launch (M <= MC); xq, Y and the argmax state are
