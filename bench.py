@@ -735,6 +735,110 @@ class NF4:
         return rows * cls.k // 2 + 4 * rows * cls.k // 64 + 2 * cls.k + 2 * rows
 
 
+class NF4Sweep:
+    """NF4 28672x8192 with M in {1, 2, 4, 8, 16, 32} activation columns (the
+    bitsandbytes thread's 70B MLP matrix; M = 1 is the one-token decode, M > 1
+    a small decode batch), one wobs_gemv_nf4 per M per step.  The dequantise-
+    then-GEMM alternative (wobs_dequantize_nf4 into a bf16 matrix, then the
+    dense bf16 GEMV over 32 columns) is timed beside it as an extra call."""
+    name = "nf4_gemv_28672x8192_m_sweep"
+    n, k = 28672, 8192
+    Ms = (1, 2, 4, 8, 16, 32)
+    dtype = "f32"
+    kernel = "nf4_tc"
+    kernel_src = "nf4_tc.cu"
+    workload_id = 3
+    launches_per_step = len(Ms)
+
+    def __init__(self, device):
+        import weight_only_bit_split_gb300 as wobs
+        from weight_only_bit_split_gb300 import synth
+        from weight_only_bit_split_gb300.nf4_levels import normal_float_levels
+        self.wobs = wobs
+        self.cb = normal_float_levels().numpy()
+        self.copies = max(1, math.ceil(ROTATE_BYTES / self.gemv_bytes(1)))
+        self.planes = []
+        for c in range(self.copies):
+            w = synth.weights(self.workload_id, (self.n, self.k), copy=c, device=device, dtype=torch.bfloat16)
+            self.planes.append(wobs.wobs_quantize_nf4(w, self.cb))
+            del w
+        self.X_all, xs = packed([(m, self.k) for m in self.Ms], torch.bfloat16, device)
+        self.X = dict(zip(self.Ms, xs))
+        for m in self.Ms:
+            self.X[m].copy_(synth.activations(self.workload_id, (m, self.k), copy=m, device=device,
+                                              dtype=torch.bfloat16))
+        self.Y_all, ys = packed([(m, self.n) for m in self.Ms], torch.bfloat16, device)
+        self.Y = dict(zip(self.Ms, ys))
+        self.ws = {m: wobs.workspace(wobs.OP_GEMV_NF4, m, self.n, self.k, device) for m in self.Ms}
+        self.Wd = torch.empty(self.n, self.k, dtype=torch.bfloat16, device=device)
+        self.Ld = torch.empty(32, self.n, dtype=torch.float32, device=device)
+        torch.cuda.synchronize(device)
+
+    @classmethod
+    def gemv_bytes(cls, m):
+        return cls.n * cls.k // 2 + 4 * cls.n * cls.k // 64 + 2 * m * cls.k + 2 * m * cls.n
+
+    def bytes_per_step(self):
+        return sum(self.gemv_bytes(m) for m in self.Ms)
+
+    def _call(self, c, m):
+        qs, am = self.planes[c]
+        self.wobs.wobs_gemv_nf4(qs, am, self.cb, self.X[m], y=self.Y[m], ws=self.ws[m])
+
+    def step(self, c):
+        for m in self.Ms:
+            self._call(c, m)
+
+    def kernel_calls(self):
+        return [(f"M{m}", self.gemv_bytes(m), lambda c, m=m: self._call(c, m)) for m in self.Ms]
+
+    def extra_calls(self):
+        def dq(c):
+            qs, am = self.planes[c]
+            self.wobs.wobs_dequantize_nf4(qs, am, self.cb, W=self.Wd)
+            self.wobs.wobs_gemv_bf16(self.Wd, self.X[32], logits=self.Ld)
+        return [("dequant+gemm_M32", self.gemv_bytes(32), dq)]
+
+    def e2e_setup(self):
+        self.xh = self.X_all.cpu().pin_memory()
+        self.yh = torch.empty(self.Y_all.shape, dtype=self.Y_all.dtype).pin_memory()
+        return self.xh.numel() * 2, self.yh.numel() * 2
+
+    def e2e_step(self, c):
+        self.X_all.copy_(self.xh, non_blocking=True)
+        self.step(c)
+        self.yh.copy_(self.Y_all, non_blocking=True)
+
+    def config(self):
+        return {"workload": self.name, "shapes_NxK": [f"{self.n}x{self.k}"], "M": list(self.Ms),
+                "weight_copies": self.copies,
+                "working_set_gb": round(self.copies * self.gemv_bytes(1) / 1e9, 3),
+                "l2": "inputs larger than L2: rotated weight copies, working set above 1 GB"}
+
+    @classmethod
+    def oracle_prepare(cls, frac):
+        import oracle
+        from weight_only_bit_split_gb300 import synth
+        from weight_only_bit_split_gb300.nf4_levels import normal_float_levels
+        cb = normal_float_levels().numpy()
+        rows = max(1, int(round(cls.n * frac)))
+        w = synth.weights(cls.workload_id, (rows, cls.k), dtype=torch.bfloat16).float().numpy()
+        codes, absmax = oracle.quantize_nf4(w, cb)
+        xs = {m: synth.activations(cls.workload_id, (m, cls.k), copy=m, dtype=torch.bfloat16).float().numpy()
+              for m in cls.Ms}
+        return oracle.pack_nf4(codes), absmax, cb, xs, rows
+
+    @classmethod
+    def oracle_step(cls, prep):
+        import oracle
+        qs, absmax, cb, xs, rows = prep
+        nbytes = 0
+        for m in cls.Ms:
+            oracle.gemv_nf4(qs, absmax, cb, xs[m])
+            nbytes += rows * cls.k // 2 + 4 * rows * cls.k // 64 + 2 * m * cls.k + 2 * m * rows
+        return nbytes
+
+
 class LmHead:
     name = "bf16_lm_head_argmax_128000x4096"
     n, k = 128000, 4096
@@ -1030,9 +1134,11 @@ class ArgCmp:
 
 
 WORKLOADS = {"q4_m1": Q4M1Fused, "q4_m1_2call": Q4M1, "q4_m_sweep": Q4Sweep, "fp16_4096": DenseF16, "nf4": NF4,
+             "nf4_m_sweep": NF4Sweep,
              "lm_head": LmHead, "argcmp": ArgCmp, "q8_m1": Q8M1Fused, "q8_m1_2call": Q8M1}
 # oracle row fraction per step (bounds the CPU time of one oracle step)
 ORACLE_FRACTION = {"q4_m1": 0.125, "q4_m1_2call": 0.125, "q4_m_sweep": 1 / 64, "fp16_4096": 0.5, "nf4": 1 / 32,
+                   "nf4_m_sweep": 1 / 512,
                    "lm_head": 1 / 256, "argcmp": 1 / 4, "q8_m1": 1 / 16, "q8_m1_2call": 1 / 16}
 
 
@@ -1222,6 +1328,15 @@ def main(argv=None):
         tot_ms += us * 1e-3
         launches += 1
     achieved = tot_b / (tot_ms * 1e-3) / 1e9
+    # other ways of computing the same product, timed the same way, outside
+    # the roofline figure
+    for label, nbytes, fn in (wl.extra_calls() if hasattr(wl, "extra_calls") else []):
+        gk = _GraphRunner(capture(lambda fn=fn: [fn(c) for c in range(wl.copies)], stream))
+        time_steps(gk, 2, stream)
+        t = time_steps(gk, reps, stream)
+        us = t * 1e3 / (reps * wl.copies)
+        per_call[label] = {"us": round(us, 3), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                           "extra": True}
     peak, peak_kind = measured_peaks()
     traffic = traffic_record(cls.kernel if isinstance(cls.kernel, str) else None)
 

@@ -339,18 +339,39 @@ WOBS_API int wobs_gemv_q8_0_f32(const int8_t* qs, const void* d, const float* x,
                                 size_t ws_bytes, void* stream);
 
 /*
- * NF4 GEMV, M = 1 (bitsandbytes issue #1842: the fused 4-bit inference GEMV
- * for one decode token): y[n] = sum_b absmax[n][b] * sum_i codebook[code_i]
- * * x_i, fp32 accumulation, bf16 output (round to nearest even).  Optional
- * fused argmax over the bf16 outputs (as stored).
+ * NF4 GEMV for 1..32 activation columns (bitsandbytes issue #1842: the
+ * fused 4-bit inference GEMV; one decode token is M = 1, a small decode
+ * batch M > 1): Y[m][n] = sum_b absmax[n][b] * sum_i codebook[code_i] *
+ * X[m][i], fp32 accumulation, bf16 output (round to nearest even).
+ * Optional fused argmax per column over the bf16 outputs (as stored).
+ * M >= 2 runs on the tensor cores with every weight rounded once to f16
+ * (relative error <= 2^-11, inside the GEMV tolerance) where K is a multiple
+ * of 256 and the planes and activation rows are 16-byte aligned, else on
+ * the CUDA cores in fp32.
  *
  *   qs [N][K/2], absmax fp32 [N][K/64], codebook HOST pointer to 16 floats,
- *   x bf16 [K], y bf16 [N], argmax int64 [1] or NULL; K multiple of 64.
- *   ws  workspace (op WOBS_OP_GEMV_NF4).
+ *   X bf16 [M][ldx] (ldx >= K; ignored for M = 1), Y bf16 [M][N], argmax
+ *   int64 [M] or NULL; 1 <= M <= WOBS_MAX_M; K multiple of 64, at most
+ *   32768.  ws  workspace (op WOBS_OP_GEMV_NF4, with the same M).
  */
 WOBS_API int wobs_gemv_nf4(const uint8_t* qs, const float* absmax, const float* codebook,
-                           const void* x, void* y, int64_t* argmax, int N, int K, void* ws,
-                           size_t ws_bytes, void* stream);
+                           const void* X, int64_t ldx, int M, void* Y, int64_t* argmax, int N,
+                           int K, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * NF4 -> bf16 dequantisation, the first half of the dequantise-then-GEMM
+ * path (bitsandbytes issue #1842, "Benchmark Data": dequantise + bf16
+ * matrix product, the alternative the fused GEMV is measured against, which
+ * pays off when the dequantised matrix serves many activation columns):
+ * W[n][k] = bf16(absmax[n][k/64] * codebook[code(n, k)]), the product taken
+ * in IEEE float32 and rounded to nearest even.  Bit-exact with the
+ * definition.  The dense GEMV entry points (wobs_gemv_bf16) then take W.
+ *
+ *   qs [N][K/2], absmax fp32 [N][K/64], codebook HOST pointer to 16 floats,
+ *   W bf16 [N][ldw] (ldw >= K, even, 4-byte aligned); K multiple of 64.
+ */
+WOBS_API int wobs_dequantize_nf4(const uint8_t* qs, const float* absmax, const float* codebook,
+                                 int N, int K, void* W, int64_t ldw, void* stream);
 
 /*
  * Standalone ArgCompare over the rows of a matrix ("[WIP] ArgCompare

@@ -35,7 +35,7 @@ from .formats import (  # noqa: F401
     quantize_q8_1, pack_q8_1, unpack_q8_1,
     quantize_q4_0, pack_q4_0, unpack_q4_0, dequantize_q4_0,
     quantize_q8_0, dequantize_q8_0,
-    nf4_codebook, quantize_nf4, pack_nf4, unpack_nf4, dequantize_nf4,
+    nf4_codebook, quantize_nf4, pack_nf4, unpack_nf4, dequantize_nf4, dequantize_nf4_bf16,
 )
 from .gemv import (  # noqa: F401
     gemv_dense, abs_dot_dense, q4_0_q8_1_blockdots, gemv_q4_0_q8_1,

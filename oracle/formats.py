@@ -66,7 +66,7 @@ import math
 
 import numpy as np
 
-from .numerics import f16_rn, round_half_away
+from .numerics import bf16_rn_bits, f16_rn, round_half_away
 
 QK8_1 = 32
 QK4_0 = 32
@@ -309,3 +309,21 @@ def dequantize_nf4(qs, absmax, cb):
     lv = np.asarray(cb, np.float32).astype(np.float64)[c]
     a = np.asarray(absmax, np.float32).astype(np.float64).reshape(n, k // QK_NF4, 1)
     return (lv.reshape(n, k // QK_NF4, QK_NF4) * a).reshape(n, k)
+
+
+def dequantize_nf4_bf16(qs, absmax, cb):
+    """bf16 bit patterns (uint16, (N, K)) of the dequantised NF4 weights.
+
+    The dequantise-then-matrix-product path of bitsandbytes issue #1842
+    ("Benchmark Data": dequantise + bf16 mm) materialises the weights in the
+    model's bf16: each element is the IEEE float32 product absmax * cb[code]
+    (the format's scale and level, both float32), rounded to bfloat16 to
+    nearest even.
+    """
+    c = unpack_nf4(qs)
+    n, k = c.shape
+    lv = np.asarray(cb, np.float32)[c].reshape(n, k // QK_NF4, QK_NF4)
+    a = np.asarray(absmax, np.float32).reshape(n, k // QK_NF4, 1)
+    prod = (lv * a).astype(np.float32)          # float32 x float32 -> float32 (IEEE)
+    return bf16_rn_bits(prod.reshape(n, k))
+

@@ -72,8 +72,15 @@ def test_shape_checks():
     rc, _ = _status("wobs_quantize_q8_1", FAKE16, 48, 1, 48, FAKE16, None)
     assert rc == -3
     cb = (ctypes.c_float * 16)()
-    rc, _ = _status("wobs_gemv_nf4", FAKE16, FAKE16, cb, FAKE16, FAKE16, None, 8, 96, None, 0, None)
+    rc, _ = _status("wobs_gemv_nf4", FAKE16, FAKE16, cb, FAKE16, 96, 1, FAKE16, None, 8, 96, None, 0, None)
     assert rc == -3
+    rc, _ = _status("wobs_dequantize_nf4", FAKE16, FAKE16, cb, 8, 96, FAKE16, 96, None)
+    assert rc == -3
+    # NF4 columns: M outside 1..32, activation pitch below K
+    rc, _ = _status("wobs_gemv_nf4", FAKE16, FAKE16, cb, FAKE16, 128, 33, FAKE16, None, 8, 128, None, 0, None)
+    assert rc == -1
+    rc, _ = _status("wobs_gemv_nf4", FAKE16, FAKE16, cb, FAKE16, 64, 2, FAKE16, None, 8, 128, None, 0, None)
+    assert rc == -1
     rc, _ = _status("wobs_gemv_f16", FAKE16, 12, FAKE16, 12, 1, FAKE16, 8, 12, None, 0, None)
     assert rc == -3
     # M outside 1..32

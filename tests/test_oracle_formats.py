@@ -261,3 +261,44 @@ def test_q8_0_codes_equal_q8_1_codes():
     q0, d0 = oracle.quantize_q8_0(v)
     q1, d1, _ = oracle.quantize_q8_1(v)
     assert np.array_equal(q0, q1) and np.array_equal(d0.view(np.uint16), d1.view(np.uint16))
+
+
+# ------------------------------------------------- NF4 -> bf16 dequantisation
+
+def _bf16_bits_by_torch(v32):
+    """bf16 patterns of float32 values through torch's own conversion (RNE)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(v32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_nf4_bf16_dequant_h5_block_gives_the_levels_in_order():
+    # the H5 block (levels 0..15 in order, four times) with absmax 1: each
+    # element is bf16(level), in element order
+    cb = nf4_codebook_fixture()
+    qs = hexbytes(load("nf4_h5.json")["qs_hex"])[None, :]
+    bits = oracle.dequantize_nf4_bf16(qs, np.ones((1, 1), np.float32), cb)
+    assert np.array_equal(bits[0], np.tile(_bf16_bits_by_torch(cb), 4))
+
+
+def test_nf4_bf16_dequant_against_exact_products_and_library_rounding():
+    # two float32 factors have an exact float64 product (48 significant
+    # bits); numpy's float64 -> float32 is RNE, torch's float32 -> bf16 is RNE
+    cb = nf4_codebook_fixture()
+    rng = np.random.default_rng(77)
+    n, k = 6, 256
+    codes = rng.integers(0, 16, size=(n, k))
+    absmax = (rng.random((n, k // 64)) * np.exp(rng.uniform(-30, 30, (n, k // 64)))).astype(np.float32)
+    absmax[1, 2] = 0.0
+    bits = oracle.dequantize_nf4_bf16(oracle.pack_nf4(codes), absmax, cb)
+    exact = cb.astype(np.float64)[codes] * np.repeat(absmax.astype(np.float64), 64, axis=1)
+    want = _bf16_bits_by_torch(exact.astype(np.float32))
+    assert np.array_equal(bits, want)
+    # a power-of-two absmax scales the bf16 levels exactly
+    a2 = np.full((1, 1), np.float32(2.0 ** -7), np.float32)
+    b2 = oracle.dequantize_nf4_bf16(oracle.pack_nf4(np.arange(64)[None, :] % 16), a2, cb)
+    lv = oracle.bf16_bits_to_f32(_bf16_bits_by_torch(cb)).astype(np.float64) * 2.0 ** -7
+    assert np.array_equal(oracle.bf16_bits_to_f32(b2[0]).astype(np.float64), np.tile(lv, 4))
+    # truncating instead of rounding to nearest would change some of them
+    trunc = (exact.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert not np.array_equal(bits, trunc)

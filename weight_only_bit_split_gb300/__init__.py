@@ -423,27 +423,70 @@ def wobs_gemv_q8_0_f32(qs, d, x, y=None, argmax=None, want_argmax=False, ws=None
 
 
 def wobs_gemv_nf4(qs, absmax, codebook, x, y=None, argmax=None, want_argmax=False, ws=None):
-    """y[N] (bf16) from NF4 planes (qs [N, K/2], absmax [N, K/64]) and bf16 x[K]."""
+    """NF4 GEMV: bf16 y from NF4 planes (qs [N, K/2], absmax [N, K/64]).
+
+    ``x`` is bf16 [K] (one column; y is [N]) or [M, K] (M columns, 1 <= M <=
+    32; y is [M, N]); ``argmax`` is int64 [M].
+    """
     lib = _lib.get()
     _need(qs, "qs", torch.uint8, 2)
     _need(absmax, "absmax", torch.float32, 2, qs.device)
-    x1 = x.reshape(-1)
-    _need(x1, "x", torch.bfloat16, 1, qs.device)
+    one = x.dim() == 1
+    X2 = x.view(1, -1) if one else x
+    _need(X2, "x", torch.bfloat16, 2, qs.device)
     N, K = qs.shape[0], qs.shape[1] * 2
-    if x1.numel() != K or not (qs.is_contiguous() and absmax.is_contiguous()):
-        raise ValueError("x must have K elements; planes must be contiguous")
+    M = X2.shape[0]
+    if X2.shape[1] != K or not (qs.is_contiguous() and absmax.is_contiguous()):
+        raise ValueError("x must have K elements per column; planes must be contiguous")
     if y is None:
-        y = torch.empty(N, dtype=torch.bfloat16, device=qs.device)
+        y = torch.empty((N,) if one else (M, N), dtype=torch.bfloat16, device=qs.device)
     _need(y, "y", torch.bfloat16, None, qs.device)
+    if y.numel() != M * N or not y.is_contiguous():
+        raise ValueError("y must be a contiguous [M, N] bf16 tensor")
     if argmax is None and want_argmax:
-        argmax = torch.empty(1, dtype=torch.int64, device=qs.device)
+        argmax = torch.empty(M, dtype=torch.int64, device=qs.device)
     if ws is None:
-        ws = _auto_ws(OP_GEMV_NF4, 1, N, K, qs.device, argmax)
-    rc = lib.wobs_gemv_nf4(_ptr(qs), _ptr(absmax), _codebook(codebook), _ptr(x1), _ptr(y),
-                           _ptr(argmax), N, K, _ptr(ws), ws.numel() if ws is not None else 0,
+        ws = _auto_ws(OP_GEMV_NF4, M, N, K, qs.device, argmax)
+    rc = lib.wobs_gemv_nf4(_ptr(qs), _ptr(absmax), _codebook(codebook), _ptr(X2), _rows(X2), M,
+                           _ptr(y), _ptr(argmax), N, K, _ptr(ws), ws.numel() if ws is not None else 0,
                            _stream(qs.device))
     _check(rc, lib)
     return y, argmax
+
+
+def wobs_dequantize_nf4(qs, absmax, codebook, W=None):
+    """bf16 W [N, K] = absmax * codebook[code] (fp32 product, rounded to bf16)."""
+    lib = _lib.get()
+    _need(qs, "qs", torch.uint8, 2)
+    _need(absmax, "absmax", torch.float32, 2, qs.device)
+    N, K = qs.shape[0], qs.shape[1] * 2
+    if not (qs.is_contiguous() and absmax.is_contiguous()):
+        raise ValueError("planes must be contiguous")
+    if W is None:
+        W = torch.empty(N, K, dtype=torch.bfloat16, device=qs.device)
+    _need(W, "W", torch.bfloat16, 2, qs.device)
+    rc = lib.wobs_dequantize_nf4(_ptr(qs), _ptr(absmax), _codebook(codebook), N, K, _ptr(W), _rows(W),
+                                 _stream(qs.device))
+    _check(rc, lib)
+    return W
+
+
+def nf4_dequant_gemm(qs, absmax, codebook, X, W=None, logits=None):
+    """The dequantise-then-GEMM path: wobs_dequantize_nf4 into ``W`` (bf16
+    [N, K], allocated if not given), then the dense bf16 GEMV
+    (wobs_gemv_bf16) over the columns of X (bf16 [M, K]) in calls of at most
+    32 columns.  Returns fp32 logits [M, N] and W."""
+    W = wobs_dequantize_nf4(qs, absmax, codebook, W)
+    X2 = X.view(1, -1) if X.dim() == 1 else X
+    _need(X2, "X", torch.bfloat16, 2, qs.device)
+    M = X2.shape[0]
+    N = W.shape[0]
+    if logits is None:
+        logits = torch.empty(M, N, dtype=torch.float32, device=qs.device)
+    for m0 in range(0, M, MAX_M):
+        m1 = min(M, m0 + MAX_M)
+        wobs_gemv_bf16(W, X2[m0:m1], logits=logits[m0:m1])
+    return logits, W
 
 
 def _argcmp(name, X, out, ws):

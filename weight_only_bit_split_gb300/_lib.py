@@ -41,8 +41,10 @@ SIGNATURES = {
     "wobs_quantize_q8_0": (c_int, [c_void_p, c_int64, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "wobs_gemv_q8_0_q8_1": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
                                     c_int, c_void_p, c_size_t, c_void_p]),
-    "wobs_gemv_nf4": (c_int, [c_void_p, c_void_p, c_float_p, c_void_p, c_void_p, c_void_p, c_int,
-                              c_int, c_void_p, c_size_t, c_void_p]),
+    "wobs_gemv_nf4": (c_int, [c_void_p, c_void_p, c_float_p, c_void_p, c_int64, c_int, c_void_p,
+                              c_void_p, c_int, c_int, c_void_p, c_size_t, c_void_p]),
+    "wobs_dequantize_nf4": (c_int, [c_void_p, c_void_p, c_float_p, c_int, c_int, c_void_p, c_int64,
+                                    c_void_p]),
     "wobs_argmax": (c_int, [c_int, c_void_p, c_int64, c_int, c_int, c_void_p, c_void_p, c_size_t,
                             c_void_p]),
     "wobs_argmin": (c_int, [c_int, c_void_p, c_int64, c_int, c_int, c_void_p, c_void_p, c_size_t,

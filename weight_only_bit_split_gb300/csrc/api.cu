@@ -83,6 +83,10 @@ WsLayout ws_layout(int op, int M, int N, int K) {
       const size_t tb = 4ull * L.splits * ((N + 255) / 256) * 256 * (8 * ((M + 7) / 8));
       if (tb > pb) pb = tb;
     }
+    if (op == WOBS_OP_GEMV_NF4 && M >= 2) {
+      const size_t tb = wobs::nf4_tc_partial_bytes(M, N, K);
+      if (tb > pb) pb = tb;
+    }
     if (op == WOBS_OP_GEMV_Q4_0_Q8_1 && M >= 2 && K % 256 == 0) {
       size_t tb = wobs::q4_mma_partial_bytes(M, N, K, env_splits());
       if (!env_splits() && M >= 5 && wobs::q4_tc_enabled()) {
@@ -237,6 +241,13 @@ int choose_splits(int op, int M, int N, int K) {
       }
       if (s < smin) s = smin;
       return s < 1 ? 1 : s;
+    }
+    case WOBS_OP_GEMV_NF4: {
+      // several columns: the tensor-memory kernel's own K split (the
+      // CUDA-core fallback takes none)
+      if (M < 2 || nf4_cp_forced()) return 1;
+      const Nf4TcPlan p = nf4_tc_plan(M, N, K);
+      return p.ok ? p.splits : 1;
     }
     default:
       return 1;
@@ -498,26 +509,43 @@ int wobs_gemv_q8_0_q8_1(const int8_t* qs, const void* d, const void* xq, int M, 
   return finish_launch(e, "gemv_q8_0_q8_1", M, N, K, L, 1);
 }
 
-int wobs_gemv_nf4(const uint8_t* qs, const float* absmax, const float* codebook, const void* x,
-                  void* y, int64_t* argmax, int N, int K, void* ws, size_t ws_bytes,
-                  void* stream) {
-  if (!qs || !absmax || !codebook || !x || !y) return fail(WOBS_ERR_INVALID_ARG, "gemv_nf4: null pointer");
+int wobs_gemv_nf4(const uint8_t* qs, const float* absmax, const float* codebook, const void* X,
+                  int64_t ldx, int M, void* Y, int64_t* argmax, int N, int K, void* ws,
+                  size_t ws_bytes, void* stream) {
+  if (!qs || !absmax || !codebook || !X || !Y) return fail(WOBS_ERR_INVALID_ARG, "gemv_nf4: null pointer");
+  if (M < 1 || M > WOBS_MAX_M) return fail(WOBS_ERR_INVALID_ARG, "gemv_nf4: M=%d outside 1..%d", M, WOBS_MAX_M);
   if (N < 1 || K < 64 || (K % 64) || K > 32768)
     return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "gemv_nf4: N=%d K=%d (K a multiple of 64, at most 32768)", N, K);
-  if (!aligned16(qs) || !aligned4(absmax) || (reinterpret_cast<uintptr_t>(x) & 1u) ||
-      (reinterpret_cast<uintptr_t>(y) & 1u))
+  if (M > 1 && ldx < K) return fail(WOBS_ERR_INVALID_ARG, "gemv_nf4: ldx < K");
+  if (!aligned16(qs) || !aligned4(absmax) || (reinterpret_cast<uintptr_t>(X) & 1u) ||
+      (reinterpret_cast<uintptr_t>(Y) & 1u))
     return fail(WOBS_ERR_MISALIGNED, "gemv_nf4: misaligned pointer");
   if (argmax && (reinterpret_cast<uintptr_t>(argmax) & 7u))
     return fail(WOBS_ERR_MISALIGNED, "gemv_nf4: argmax not 8-byte aligned");
   Prepared p;
-  int rc = prepare_ws(WOBS_OP_GEMV_NF4, 1, N, K, argmax, ws, ws_bytes, &p);
+  int rc = prepare_ws(WOBS_OP_GEMV_NF4, M, N, K, argmax, ws, ws_bytes, &p);
   if (rc) return rc;
   wobs::Codebook16 cb;
   std::memcpy(cb.v, codebook, sizeof(cb.v));
   wobs::Launch L;
-  cudaError_t e = wobs::launch_gemv_nf4(qs, absmax, cb, x, y, N, K, p.am,
-                                        static_cast<cudaStream_t>(stream), &L);
-  return finish_launch(e, "gemv_nf4", 1, N, K, L, 1);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = M == 1 ? wobs::launch_gemv_nf4(qs, absmax, cb, X, Y, N, K, p.am, st, &L)
+                         : wobs::launch_gemv_nf4_mc(qs, absmax, cb, X, M > 1 ? ldx : K, M, Y, N, K, p.sk,
+                                                    p.am, st, &L);
+  return finish_launch(e, "gemv_nf4", M, N, K, L, p.sk.splits);
+}
+
+int wobs_dequantize_nf4(const uint8_t* qs, const float* absmax, const float* codebook, int N, int K,
+                        void* W, int64_t ldw, void* stream) {
+  if (!qs || !absmax || !codebook || !W) return fail(WOBS_ERR_INVALID_ARG, "dequantize_nf4: null pointer");
+  if (N < 1 || K < 64 || (K % 64)) return fail(WOBS_ERR_UNSUPPORTED_SHAPE, "dequantize_nf4: N=%d K=%d", N, K);
+  if (ldw < K || (ldw % 2)) return fail(WOBS_ERR_INVALID_ARG, "dequantize_nf4: ldw");
+  if (!aligned4(absmax) || !aligned4(W)) return fail(WOBS_ERR_MISALIGNED, "dequantize_nf4: misaligned pointer");
+  wobs::Codebook16 cb;
+  std::memcpy(cb.v, codebook, sizeof(cb.v));
+  wobs::Launch L;
+  cudaError_t e = wobs::launch_dequantize_nf4(qs, absmax, cb, N, K, W, ldw, static_cast<cudaStream_t>(stream), &L);
+  return finish_launch(e, "dequantize_nf4", 0, N, K, L, 1);
 }
 
 static int argcmp(const char* op, bool is_min, int dtype, const void* X, int64_t ldx, int M, int N,

@@ -112,6 +112,26 @@ int q8_0_columns_per_launch(int K);
 cudaError_t launch_gemv_nf4(const uint8_t* qs, const float* absmax, const Codebook16& cb,
                             const void* x, void* y, int N, int K, const ArgmaxArgs& am,
                             cudaStream_t st, Launch* info);
+// NF4 with 2..32 activation columns (X bf16 [M][ldx], Y bf16 [M][N]): the
+// tcgen05 kernel (K % 256 == 0, 16-byte aligned planes and activation rows;
+// its plan fixes the K split, which must equal sk.splits) or the CUDA-core
+// kernel (no split).
+struct Nf4TcPlan {
+  bool ok = false;
+  int range = 0, splits = 1, grid = 0;
+};
+Nf4TcPlan nf4_tc_plan(int M, int N, int K);
+size_t nf4_tc_partial_bytes(int M, int N, int K);
+cudaError_t launch_nf4_tc(const uint8_t* qs, const float* absmax, const Codebook16& cb, const void* X,
+                          int64_t ldx, int M, void* Y, int N, int K, const SplitArgs& sk,
+                          const ArgmaxArgs& am, cudaStream_t st, Launch* info);
+cudaError_t launch_gemv_nf4_mc(const uint8_t* qs, const float* absmax, const Codebook16& cb,
+                               const void* X, int64_t ldx, int M, void* Y, int N, int K,
+                               const SplitArgs& sk, const ArgmaxArgs& am, cudaStream_t st,
+                               Launch* info);
+// NF4 -> bf16 dequantisation: W[n][k] = bf16(absmax[n][k/64] * codebook[code])
+cudaError_t launch_dequantize_nf4(const uint8_t* qs, const float* absmax, const Codebook16& cb, int N,
+                                  int K, void* W, int64_t ldw, cudaStream_t st, Launch* info);
 
 // Standalone argmax / argmin over the rows of [M][N] (dtype 1 fp16, 2 bf16,
 // 3 fp32).  warp_rows: one warp per row, no workspace; otherwise one CTA per

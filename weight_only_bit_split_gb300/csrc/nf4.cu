@@ -391,7 +391,124 @@ cudaError_t run(const uint8_t* qs, const float* absmax, const Codebook16& cb, co
                   am);
 }
 
+// ------------------------------------------------- 2..32 columns, CUDA cores
+
+// The fallback for several activation columns where the tensor-memory kernel
+// does not apply (K not a multiple of 256, unaligned planes or activations):
+// one thread per weight row, K in chunks of 256 whose activations (all
+// columns, fp32) sit in shared memory; per 64-block the code sums
+// sum_i codebook[c_i] * x_i of every column, then times the block's absmax,
+// as the format defines the product.
+constexpr int kMnChunk = 256;
+
+template <int MC, bool kArgmax>
+__global__ void __launch_bounds__(kThreads) nf4_mn_kernel(const uint8_t* __restrict__ qs,
+                                                           const float* __restrict__ absmax,
+                                                           Codebook16 cb,
+                                                           const __nv_bfloat16* __restrict__ X,
+                                                           int64_t ldx, int M,
+                                                           __nv_bfloat16* __restrict__ Y, int N,
+                                                           int K, ArgmaxArgs am) {
+  __shared__ float xs[MC][kMnChunk];
+  __shared__ float lv[16];
+  const int row = blockIdx.x * kThreads + threadIdx.x;
+  const bool valid = row < N;
+  const int nb = K >> 6;
+  if (threadIdx.x < 16) lv[threadIdx.x] = cb.v[threadIdx.x];
+  pdl_launch_dependents();
+  pdl_wait();
+  float acc[MC];
+#pragma unroll
+  for (int m = 0; m < MC; ++m) acc[m] = 0.f;
+  const uint8_t* qrow = qs + static_cast<int64_t>(valid ? row : 0) * (K >> 1);
+  const float* arow = absmax + static_cast<int64_t>(valid ? row : 0) * nb;
+  for (int k0 = 0; k0 < K; k0 += kMnChunk) {
+    const int kc = min(kMnChunk, K - k0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < MC * kMnChunk; i += kThreads) {
+      const int m = i / kMnChunk, k = i - m * kMnChunk;
+      xs[m][k] = (m < M && k < kc) ? __bfloat162float(X[m * ldx + k0 + k]) : 0.f;
+    }
+    __syncthreads();
+    if (valid) {
+      for (int b = 0; b < (kc >> 6); ++b) {
+        const int gb = (k0 >> 6) + b;
+        const float a = __ldg(arow + gb);
+        float inner[MC];
+#pragma unroll
+        for (int m = 0; m < MC; ++m) inner[m] = 0.f;
+        for (int by = 0; by < 32; ++by) {
+          const uint32_t c = __ldg(qrow + 32 * gb + by);
+          const float w0 = lv[c >> 4], w1 = lv[c & 15u];   // elements 2 by, 2 by + 1
+          const int k = 64 * b + 2 * by;
+#pragma unroll
+          for (int m = 0; m < MC; ++m) inner[m] = fmaf(w1, xs[m][k + 1], fmaf(w0, xs[m][k], inner[m]));
+        }
+#pragma unroll
+        for (int m = 0; m < MC; ++m) acc[m] = fmaf(a, inner[m], acc[m]);
+      }
+    }
+  }
+  __shared__ uint64_t s_key[kWarps][MC];
+  __shared__ uint64_t s_cta[MC];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int m = 0; m < MC; ++m) {
+    const __nv_bfloat16 o = __float2bfloat16_rn(acc[m]);
+    if (valid && m < M) Y[static_cast<int64_t>(m) * N + row] = o;
+    if (kArgmax) {
+      uint64_t k = (valid && m < M) ? argmax_key(__bfloat162float(o), static_cast<uint32_t>(row)) : 0ull;
+      k = warp_max_u64(k);
+      if (lane == 0) s_key[warp][m] = k;
+    }
+  }
+  if (kArgmax) {
+    __syncthreads();
+    if (threadIdx.x < MC) {
+      uint64_t bk = 0;
+      for (int w = 0; w < kWarps; ++w) bk = s_key[w][threadIdx.x] > bk ? s_key[w][threadIdx.x] : bk;
+      s_cta[threadIdx.x] = bk;
+    }
+    __syncthreads();
+    argmax_publish(s_cta, M, am, gridDim.x);
+  }
+}
+
+template <int MC>
+cudaError_t run_mn(const uint8_t* qs, const float* absmax, const Codebook16& cb, const void* X,
+                   int64_t ldx, int M, void* Y, int N, int K, const ArgmaxArgs& am, cudaStream_t st,
+                   Launch* info) {
+  const int grid = (N + kThreads - 1) / kThreads;
+  info->grid_x = grid;
+  info->block = kThreads;
+  info->kernel = "nf4_mn";
+  if (am.out)
+    return launch_k(nf4_mn_kernel<MC, true>, dim3(grid), dim3(kThreads), 0, st, true, qs, absmax, cb,
+                    static_cast<const __nv_bfloat16*>(X), ldx, M, static_cast<__nv_bfloat16*>(Y), N, K, am);
+  return launch_k(nf4_mn_kernel<MC, false>, dim3(grid), dim3(kThreads), 0, st, true, qs, absmax, cb,
+                  static_cast<const __nv_bfloat16*>(X), ldx, M, static_cast<__nv_bfloat16*>(Y), N, K, am);
+}
+
 }  // namespace
+
+// Several activation columns: the tensor-memory kernel where it applies,
+// otherwise the CUDA-core kernel above (which takes no K split).
+cudaError_t launch_gemv_nf4_mc(const uint8_t* qs, const float* absmax, const Codebook16& cb,
+                               const void* X, int64_t ldx, int M, void* Y, int N, int K,
+                               const SplitArgs& sk, const ArgmaxArgs& am, cudaStream_t st,
+                               Launch* info) {
+  if (!nf4_cp_forced()) {
+    cudaError_t e = launch_nf4_tc(qs, absmax, cb, X, ldx, M, Y, N, K, sk, am, st, info);
+    if (e != cudaErrorNotSupported) return e;
+    cudaGetLastError();
+  }
+  if (M <= 2) return run_mn<2>(qs, absmax, cb, X, ldx, M, Y, N, K, am, st, info);
+  if (M <= 4) return run_mn<4>(qs, absmax, cb, X, ldx, M, Y, N, K, am, st, info);
+  if (M <= 8) return run_mn<8>(qs, absmax, cb, X, ldx, M, Y, N, K, am, st, info);
+  if (M <= 16) return run_mn<16>(qs, absmax, cb, X, ldx, M, Y, N, K, am, st, info);
+  return run_mn<32>(qs, absmax, cb, X, ldx, M, Y, N, K, am, st, info);
+}
+
 
 cudaError_t launch_gemv_nf4(const uint8_t* qs, const float* absmax, const Codebook16& cb,
                             const void* x, void* y, int N, int K, const ArgmaxArgs& am,

@@ -43,6 +43,7 @@
 #include <cstdlib>
 
 #include "common.cuh"
+#include "nf4_decode.cuh"
 #include "tcgen05.cuh"
 
 namespace wobs {
@@ -64,13 +65,6 @@ constexpr int kKS = 1024;                    // codes per row per stage
 constexpr int kStage = 4 * 8192 + kRB * 64;  // 36864 bytes, a multiple of 1024
 constexpr uint32_t kStageTx = kStage;
 
-// PTX prmt, default mode: selector nibble bits 0-2 pick one of the eight
-// source bytes, bit 3 replicates that byte's sign bit over the result byte.
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
 // Shared loads as pure functions of their address, so the compiler may
 // interleave them with the MMAs.  Stage reads stay between the stage's full
 // wait and its release because their addresses come from a value produced
@@ -130,12 +124,6 @@ __device__ __forceinline__ void mbar_arrive_after(uint64_t* bar, float d0, float
                :: "r"(smem_addr(bar)), "f"(d0), "f"(d1), "f"(d2), "f"(d3) : "memory");
 }
 
-// Codebook held as byte planes: lo/hi bytes of the f16 entries 0..7 (A) and
-// 8..15 (B), two registers each.
-struct Planes {
-  uint32_t la0, la1, lb0, lb1, ha0, ha1, hb0, hb1;
-};
-
 // One code word (4 bytes, 8 codes; byte j = element 2j in its high nibble,
 // element 2j + 1 in its low nibble) -> four f16 pairs, low half = the even
 // element.  Table variant: one lookup per byte.
@@ -144,25 +132,6 @@ struct Planes {
 __device__ __forceinline__ void decode_table(uint32_t w, uint32_t tl, uint32_t (&r)[4]) {
 #pragma unroll
   for (int j = 0; j < 4; ++j) r[j] = lds32(prmt(w, tl, 0x7604u | (j << 4)));
-}
-
-// Register variant: the low 3 bits of each code select a byte in the A and B
-// planes, the high bit (spread to a byte mask by sign replication) picks A or
-// B, and byte permutes pair the low and high bytes into f16 values.
-__device__ __forceinline__ void decode_planes(uint32_t w, const Planes& p, uint32_t (&r)[4]) {
-  const uint32_t s = w & 0x77777777u;
-  const uint32_t w4 = w << 4;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t sel = h ? (s >> 16) : s;
-    const uint32_t m = prmt(w4, w, h ? 0xFBEAu : 0xD9C8u);   // byte i = 0xFF where code i >= 8
-    const uint32_t la = prmt(p.la0, p.la1, sel), lb = prmt(p.lb0, p.lb1, sel);
-    const uint32_t ha = prmt(p.ha0, p.ha1, sel), hb = prmt(p.hb0, p.hb1, sel);
-    const uint32_t lo = (la & ~m) | (lb & m);
-    const uint32_t hi = (ha & ~m) | (hb & m);
-    r[2 * h] = prmt(lo, hi, 0x4051u);
-    r[2 * h + 1] = prmt(lo, hi, 0x6273u);
-  }
 }
 
 // Power-of-two scale 2^(141 - E) for a positive float with biased exponent E

@@ -116,6 +116,32 @@ __global__ void __launch_bounds__(kThreads) nf4_quant_kernel(const __nv_bfloat16
   if (lane == 0) absmax[static_cast<int64_t>(n) * nb + b] = amax;
 }
 
+// ------------------------------------------------------ NF4 -> bf16
+// Dequantisation for the dequantise-then-GEMM path (bitsandbytes issue
+// #1842, "Benchmark Data": the dequantise + bf16 matrix-product row): one
+// thread per code byte, w = absmax * codebook[code] as an fp32 product,
+// rounded to bf16 (nearest even); element 2j from the high nibble.
+__global__ void __launch_bounds__(kThreads) nf4_dequant_kernel(const uint8_t* __restrict__ qs,
+                                                                const float* __restrict__ absmax,
+                                                                Codebook16 cb, int N, int K,
+                                                                __nv_bfloat16* __restrict__ W,
+                                                                int64_t ldw) {
+  __shared__ float lv[16];
+  if (threadIdx.x < 16) lv[threadIdx.x] = cb.v[threadIdx.x];
+  __syncthreads();
+  const int kh = K >> 1;
+  const int64_t total = static_cast<int64_t>(N) * kh;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int n = static_cast<int>(t / kh);
+    const int j = static_cast<int>(t - static_cast<int64_t>(n) * kh);
+    const uint32_t c = qs[t];
+    const float a = absmax[static_cast<int64_t>(n) * (K >> 6) + (j >> 5)];
+    const __nv_bfloat162 o = __floats2bfloat162_rn(__fmul_rn(a, lv[c >> 4]), __fmul_rn(a, lv[c & 15u]));
+    *reinterpret_cast<__nv_bfloat162*>(W + static_cast<int64_t>(n) * ldw + 2 * j) = o;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_q8_1(const float* X, int64_t ldx, int M, int K, void* xq,
@@ -150,6 +176,20 @@ cudaError_t launch_quantize_nf4(const void* W, int64_t ldw, int N, int K, const 
   info->kernel = "quantize_nf4";
   nf4_quant_kernel<<<static_cast<unsigned>(grid), kThreads, 0, st>>>(
       static_cast<const __nv_bfloat16*>(W), ldw, N, K, cb, qs, absmax);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize_nf4(const uint8_t* qs, const float* absmax, const Codebook16& cb, int N,
+                                  int K, void* W, int64_t ldw, cudaStream_t st, Launch* info) {
+  const int64_t total = static_cast<int64_t>(N) * (K / 2);
+  int64_t grid = (total + kThreads - 1) / kThreads;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+  if (grid > cap) grid = cap;
+  info->grid_x = static_cast<int>(grid);
+  info->block = kThreads;
+  info->kernel = "dequantize_nf4";
+  nf4_dequant_kernel<<<static_cast<unsigned>(grid), kThreads, 0, st>>>(qs, absmax, cb, N, K,
+                                                                       static_cast<__nv_bfloat16*>(W), ldw);
   return cudaGetLastError();
 }
 
