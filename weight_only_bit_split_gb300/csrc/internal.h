@@ -116,6 +116,10 @@ cudaError_t launch_gemv_nf4(const uint8_t* qs, const float* absmax, const Codebo
 // tcgen05 kernel (K % 256 == 0, 16-byte aligned planes and activation rows;
 // its plan fixes the K split, which must equal sk.splits) or the CUDA-core
 // kernel (no split).
+// The codebook scaled by a power of two into f16 normal numbers (largest
+// magnitude in [2^14, 2^15)); false when an entry is not finite or a nonzero
+// entry would fall below the f16 normal range.
+bool nf4_codebook_scale(const Codebook16& cb, float* scale, float* inv);
 struct Nf4TcPlan {
   bool ok = false;
   int range = 0, splits = 1, grid = 0;
