@@ -55,8 +55,10 @@
  *     ring (all three for measurements).  WOBS_Q4TC=1 takes Q4_0 calls with
  *     5..16 columns to the tcgen05 kernel as well (17..32 take it by
  *     default where its plan fills the GPU), WOBS_Q4TC=0 keeps every Q4_0
- *     call off it; WOBS_Q4F32=16 runs the fused quantise-and-GEMV kernel
- *     with 16 warps and two CTAs per SM (testing only).
+ *     call off it; WOBS_Q4F32=16 or 32 runs the fused quantise-and-GEMV
+ *     kernel with 16 warps and two CTAs per SM or 32 warps and one (the
+ *     default picks by shape; testing only).  WOBS_NF4_P=0..3 also applies
+ *     to the NF4 tensor-memory kernel for several columns.
  */
 #ifndef WOBS_H
 #define WOBS_H

@@ -15,11 +15,11 @@ from test_gpu_canaries import check_guards, guarded
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["32", "16"])
+@pytest.fixture(params=["32", "16", "auto"])
 def variant(request, monkeypatch):
-    """Both prologue shapes: 32 warps and one CTA per SM (the default), 16
-    warps and two CTAs per SM (forced)."""
-    if request.param == "32":
+    """Both prologue shapes, forced: 32 warps and one CTA per SM, 16 warps
+    and two CTAs per SM; and the library's own choice by shape."""
+    if request.param == "auto":
         monkeypatch.delenv("WOBS_Q4F32", raising=False)
     else:
         monkeypatch.setenv("WOBS_Q4F32", request.param)

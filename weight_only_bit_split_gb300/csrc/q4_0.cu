@@ -830,16 +830,22 @@ cudaError_t run_m1_local_t(const uint8_t* qs, const void* d, const float* x, uin
                   xq_out);
 }
 
-// 32 warps and one CTA per SM (each SM quantises x once) when the ring and
-// planes fit, else 16 warps and two CTAs per SM; WOBS_Q4F32=16 forces the
-// latter.
+// 32 warps and one CTA per SM (each SM quantises x once) for long vectors
+// or few rows; 16 warps and two CTAs per SM for K <= 4096 with at least
+// 4096 rows, where the prologue is short and a CTA that finishes early
+// hands its SM half to the next kernel sooner (GB300, per call back to
+// back: 4096^2 3.83 against 3.96 us, 14336x4096 6.90 against 7.30 us;
+// 1024x4096 and 4096x14336 are faster with 32 warps).  WOBS_Q4F32=16 or 32
+// forces one of them.
 template <bool kArgmax>
 cudaError_t run_m1_fused(const uint8_t* qs, const void* d, const float* x, uint8_t* xq_out, float* y,
                          int N, int K, const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   const char* v = std::getenv("WOBS_Q4F32");
-  const bool force16 = v && std::strcmp(v, "16") == 0;
   const bool fits32 = 32 * kRing * kSegBytes + (K / 32) * 40 <= 220 * 1024;
-  if (fits32 && !force16) return run_m1_local_t<kArgmax, 32>(qs, d, x, xq_out, y, N, K, am, st, info);
+  bool use32 = fits32 && !(K <= 4096 && N >= 4096);
+  if (v && std::strcmp(v, "16") == 0) use32 = false;
+  if (v && std::strcmp(v, "32") == 0 && fits32) use32 = true;
+  if (use32) return run_m1_local_t<kArgmax, 32>(qs, d, x, xq_out, y, N, K, am, st, info);
   return run_m1_local_t<kArgmax, 16>(qs, d, x, xq_out, y, N, K, am, st, info);
 }
 
