@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_tc_kernel(const __grid_consta
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ int s_last;                         // the epilogue's unit completed its tile
+  __shared__ volatile int s_evote[2];            // epilogue warps' abort vote, per step parity
   __shared__ uint16_t s_cbh[16];                 // codebook * 2^g in f16
   __shared__ unsigned s_colmax[32];              // max |x| per column (float bits)
   __shared__ float s_colinv[32];                 // per column: 2^-t of the activations
@@ -212,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_tc_kernel(const __grid_consta
     mbar_init(&bready, 8);
     mbar_init(&done, 1);
     s_abort = 0;
+    s_evote[0] = s_evote[1] = 0;
     for (int c = 0; c < 16; ++c) s_cbh[c] = __half_as_ushort(__float2half_rn(cb.v[c] * cb_scale));
     for (int c = 0; c < 32; ++c) {
       s_colmax[c] = 0u;
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_tc_kernel(const __grid_consta
     const int q = warp & 3, lr = 32 * q + lane;
     pdl_wait();
     uint64_t mybest = 0;
-    if (!__all_sync(0xffffffffu, mbar_wait(&bready, 0))) s_abort = 1;
+    const bool ready = __all_sync(0xffffffffu, mbar_wait(&bready, 0));
     float cinv[BN], acc[BN];
 #pragma unroll
     for (int c = 0; c < BN; ++c) {
@@ -414,12 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_tc_kernel(const __grid_consta
       acc[c] = 0.f;
     }
     const int64_t sstride = static_cast<int64_t>(ntiles) * (BN * kRows);
-    for (int i = 0; i < total && !s_abort; ++i) {
+    for (int i = 0; i < total; ++i) {
       const int u = i / su, j = i % su, db = i & 1, s = i % NS;
-      bool ok = mbar_wait(&dfull[db], (i >> 1) & 1);
+      bool ok = ready && mbar_wait(&dfull[db], (i >> 1) & 1);
       ok = ok && mbar_wait(&full[s], (i / NS) & 1);      // the stage's absmax has landed
-      if (!__all_sync(0xffffffffu, ok)) { s_abort = 1; break; }
-      if (s_abort) break;
+      // the four warps leave together (they meet at named barriers below):
+      // a vote per step, in a slot that is not rewritten before every warp
+      // has read it
+      if (!__all_sync(0xffffffffu, ok) && lane == 0) s_evote[i & 1] = 1;
+      epilogue_sync();
+      if (s_evote[i & 1]) { s_abort = 1; break; }
       tc_fence_after();
       // this row's absmax of the stage's four blocks
       const float4 a4 = *reinterpret_cast<const float4*>(gen(slot_addr(L, s)) + kStageBytes + 16 * lr);
