@@ -1361,6 +1361,28 @@ def main(argv=None):
     e2e_gbs = wl.bytes_per_step() / (e2e_ms * 1e-3) / 1e9
     e2e_gbs = reduce_over_ranks(e2e_gbs, "sum", device) if world > 1 else e2e_gbs
 
+    # the same graphs with the launches left out: what the step's two pinned
+    # copies cost on their own (latency of a host<->device round trip, not
+    # bandwidth: the step moves a few hundred KB)
+    shadow = [n for n in ("step", "_call") if hasattr(wl, n)]
+    for n in shadow:
+        setattr(wl, n, lambda *a, **k: None)
+    try:
+        copy_graphs = [wobs.StepGraph(lambda c=c: wl.e2e_step(c), stream) for c in range(min(4, wl.copies))]
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                copy_graphs[i % len(copy_graphs)].replay()
+            stream.synchronize()
+            e0.record(stream)
+            for i in range(e2e_steps):
+                copy_graphs[i % len(copy_graphs)].replay()
+            e1.record(stream)
+        e1.synchronize()
+        copies_ms = e0.elapsed_time(e1) / e2e_steps
+    finally:
+        for n in shadow:
+            delattr(wl, n)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         frac = ORACLE_FRACTION[args.workload]
@@ -1394,9 +1416,12 @@ def main(argv=None):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
+                    "us_per_step": round(e2e_ms * 1e3, 3),
+                    "copies_only_us_per_step": round(copies_ms * 1e3, 3),
                     "how": "public Python API calls of one step captured once per weight copy "
                            "in a wobs.StepGraph and replayed every step: pinned H2D of the "
-                           "activations, the step's launches, D2H of the outputs"},
+                           "activations, the step's launches, D2H of the outputs; "
+                           "copies_only: the same graphs without the launches"},
             "gpu_launches": wl.launches_per_step * args.steps,
             "timed_regions": {"count": len(regions), "ms_min": round(min(regions), 5),
                               "ms_median": round(ms, 5), "ms_max": round(max(regions), 5),

@@ -97,17 +97,29 @@ __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
 // Four code bytes of a block (bytes 4i..4i+3: elements 4i..4i+3 in the low
 // nibbles, 4i+16..4i+19 in the high ones) -> four f16 pairs (q - 8) * d4 in
 // the kernel's K order: (4i, 4i+2), (4i+16, 4i+18), (4i+1, 4i+3),
-// (4i+17, 4i+19).  1024 + q is exact in f16 (q OR-ed into the mantissa of
-// 1024), so is (1024 + q) - 1032; the multiply rounds once.
+// (4i+17, 4i+19).  A low nibble OR-ed into the mantissa of 1024 gives the
+// f16 value 1024 + q, and (1024 + q) - 1032 = q - 8 exactly; a high nibble
+// left in place gives 1024 + 16 q, and (1024 + 16 q) / 16 - 72 = q - 8
+// exactly (one fused multiply-add).  The multiply by d4 rounds once.
 __device__ __forceinline__ void decode_word(uint32_t w, uint32_t dd, uint32_t* out) {
+  const uint32_t kMagic = 0x64006400u;         // 1024, 1024
   const uint32_t kBias = 0x64086408u;          // 1032, 1032
-  out[0] = h2_mul(h2_sub((w & 0x000F000Fu) | 0x64006400u, kBias), dd);
-  out[1] = h2_mul(h2_sub(((w >> 4) & 0x000F000Fu) | 0x64006400u, kBias), dd);
-  out[2] = h2_mul(h2_sub(((w >> 8) & 0x000F000Fu) | 0x64006400u, kBias), dd);
-  out[3] = h2_mul(h2_sub(((w >> 12) & 0x000F000Fu) | 0x64006400u, kBias), dd);
+  const uint32_t kSixteenth = 0x2C002C00u;     // 1/16, 1/16
+  const uint32_t kHiBias = 0xD480D480u;        // -72, -72
+  const uint32_t w8 = w >> 8;
+  out[0] = h2_mul(h2_sub((w & 0x000F000Fu) | kMagic, kBias), dd);
+  out[1] = h2_mul(h2_fma((w & 0x00F000F0u) | kMagic, kSixteenth, kHiBias), dd);
+  out[2] = h2_mul(h2_sub((w8 & 0x000F000Fu) | kMagic, kBias), dd);
+  out[3] = h2_mul(h2_fma((w8 & 0x00F000F0u) | kMagic, kSixteenth, kHiBias), dd);
 }
 
 // Named barrier of the four epilogue warps.
@@ -288,11 +300,15 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
           const int i = u * su + j, a = i % kAbufs;
           if (!mbar_wait(&afull[a], (i / kAbufs) & 1)) { s_abort = 1; break; }
           tc_fence_after();
+          // descriptors of the step computed once: B box kk / 4 of the step
+          // (kBoxBytes apart), its 32-byte K slice kk % 4 (the start address
+          // field counts 16 bytes and cannot overflow inside shared memory)
+          const uint64_t bd0 = sw128_desc(bbase + j * (kSK / 64) * Sh::kBoxBytes);
+          const uint32_t at0 = tmem + a * kAcols;
 #pragma unroll
           for (int kk = 0; kk < kSK / 16; ++kk) {
-            const int k = j * kSK + 16 * kk;     // K offset inside the unit
-            const uint64_t bd = sw128_desc(bbase + (k >> 6) * Sh::kBoxBytes) + 2 * ((k & 63) >> 4);
-            tc_mma_ta(d, tmem + a * kAcols + 8 * kk, bd, idesc, (j | kk) != 0);
+            const uint64_t bd = bd0 + static_cast<uint64_t>(((kk >> 2) * Sh::kBoxBytes >> 4) + 2 * (kk & 3));
+            tc_mma_ta(d, at0 + 8 * kk, bd, idesc, (j | kk) != 0);
           }
           tc_commit(&aempty[a]);
           issued = true;
