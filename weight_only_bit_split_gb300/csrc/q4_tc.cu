@@ -19,27 +19,21 @@
 // |w_i x_i|, inside the GEMV tolerance of 1e-3 * sum |w_i x_i|.
 //
 // Pipeline (one CTA per SM, warp-specialised):
-//   * warp 0, one thread: 2-D TMA copies of 128 rows x 512 codes (two
-//     128-byte boxes side by side, 128-byte swizzle) into a 4-stage ring,
-//     and of the unit's scales (128 rows x R / 32) into one of two scale
-//     buffers;
+//   * warp 0, one thread: 2-D TMA copies of 128 rows x 256 codes (128-byte
+//     swizzle) into an 8-stage ring, and of the unit's scales (128 rows x
+//     R / 32) into one of two scale buffers;
 //   * warps 2..9: each thread owns one weight row (its tensor-memory lane);
 //     it reads its codes and scales from the stage, decodes four blocks into
-//     f16 pairs and stores them into tensor memory (three A buffers of 256 K).
-//     They touch weights only, so they start before the previous kernel on
-//     the stream has finished;
+//     f16 pairs and stores them into tensor memory (three A buffers of 256 K);
 //   * warp 1, one thread: tcgen05.mma with A read from tensor memory and B
-//     (the activations) from shared memory, fp32 accumulators in tensor
-//     memory (two buffers);
-//   * warps 10..13 (with the decoders once these have filled the three A
-//     buffers): after the dependency wait, convert the activations of the
-//     CTA's K range once into the 128-byte swizzle layout; then per unit
-//     read the accumulator (one row per thread), write y or the split-K
-//     partial, fold the greedy argmax.
+//     (the activations, converted once per CTA for its K range into the
+//     128-byte swizzle layout) from shared memory, fp32 accumulators in
+//     tensor memory (two buffers);
+//   * warps 10..13: read the accumulator (one row per thread), write y or
+//     the split-K partials, fold the greedy argmax.
 // Work units are (128-row tile, K range); every CTA keeps one K range, so
 // its activation tile is converted once.  Split K ranges are added in split
-// order, right after the unit, by the CTA that finishes a tile last (its
-// tensor cores meanwhile run the next unit).  The K order inside each
+// order by the CTA that finishes a tile last.  The K order inside each
 // 32-block is permuted identically on both operands so that the decode is
 // four mask-or operations per code word.  Every wait is bounded: on expiry
 // the CTA records the error word and stops.
@@ -54,9 +48,10 @@ namespace wobs {
 namespace {
 
 constexpr int kRows = 128;                       // weight rows per tile (MMA M)
-constexpr int kSK = 256;                         // K elements per tensor-memory A buffer (8 blocks)
-constexpr int kCodeBytes = kRows * kSK / 2;      // 16384: one 128-byte x 128-row copy box
-constexpr int kStageBytes = 2 * kCodeBytes;      // a copy stage: two boxes side by side along K
+constexpr int kSK = 256;                         // K elements per TMA stage (8 blocks)
+constexpr int kCodeBytes = kRows * kSK / 2;      // 16384
+constexpr int kStageBytes = kCodeBytes;
+constexpr int kMaxUnits = 256;                   // work units of one CTA at most
 constexpr int kThreads = 448;                    // TMA, MMA, 8 decoder, 4 epilogue warps
 constexpr int kAcols = kSK / 2;                  // tensor-memory columns of one A buffer
 constexpr int kAbufs = 3;                        // A buffers in tensor memory
@@ -72,7 +67,7 @@ static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignm
 template <int BN>
 struct TcQ {
   static constexpr int kMaxR = 1024;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 8;
   static constexpr int kSBuf = kRows * (kMaxR / 16);   // fp16 per block and row
   static constexpr int kBoxBytes = BN * 128;     // one 64-element K box of B
   static constexpr int kBBytes = (kMaxR / 64) * kBoxBytes;
@@ -97,89 +92,22 @@ __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
   return r;
 }
 
-__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t r;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-  return r;
-}
-
 // Four code bytes of a block (bytes 4i..4i+3: elements 4i..4i+3 in the low
 // nibbles, 4i+16..4i+19 in the high ones) -> four f16 pairs (q - 8) * d4 in
 // the kernel's K order: (4i, 4i+2), (4i+16, 4i+18), (4i+1, 4i+3),
-// (4i+17, 4i+19).  A low nibble OR-ed into the mantissa of 1024 gives the
-// f16 value 1024 + q, and (1024 + q) - 1032 = q - 8 exactly; a high nibble
-// left in place gives 1024 + 16 q, and (1024 + 16 q) / 16 - 72 = q - 8
-// exactly (one fused multiply-add).  The multiply by d4 rounds once.
+// (4i+17, 4i+19).  1024 + q is exact in f16 (q OR-ed into the mantissa of
+// 1024), so is (1024 + q) - 1032; the multiply rounds once.
 __device__ __forceinline__ void decode_word(uint32_t w, uint32_t dd, uint32_t* out) {
-  const uint32_t kMagic = 0x64006400u;         // 1024, 1024
   const uint32_t kBias = 0x64086408u;          // 1032, 1032
-  const uint32_t kSixteenth = 0x2C002C00u;     // 1/16, 1/16
-  const uint32_t kHiBias = 0xD480D480u;        // -72, -72
-  const uint32_t w8 = w >> 8;
-  out[0] = h2_mul(h2_sub((w & 0x000F000Fu) | kMagic, kBias), dd);
-  out[1] = h2_mul(h2_fma((w & 0x00F000F0u) | kMagic, kSixteenth, kHiBias), dd);
-  out[2] = h2_mul(h2_sub((w8 & 0x000F000Fu) | kMagic, kBias), dd);
-  out[3] = h2_mul(h2_fma((w8 & 0x00F000F0u) | kMagic, kSixteenth, kHiBias), dd);
-}
-
-// Named barrier of the four epilogue warps.
-__device__ __forceinline__ void epilogue_sync() {
-  asm volatile("bar.sync 2, 128;" ::: "memory");
+  out[0] = h2_mul(h2_sub((w & 0x000F000Fu) | 0x64006400u, kBias), dd);
+  out[1] = h2_mul(h2_sub(((w >> 4) & 0x000F000Fu) | 0x64006400u, kBias), dd);
+  out[2] = h2_mul(h2_sub(((w >> 8) & 0x000F000Fu) | 0x64006400u, kBias), dd);
+  out[3] = h2_mul(h2_sub(((w >> 12) & 0x000F000Fu) | 0x64006400u, kBias), dd);
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Activations of a CTA's K range (R elements from block kb0) -> f16
-// d8 * q8 in the 128-byte swizzle layout of the B operand (one 64-element
-// box of BN rows per BN * 128 bytes), K order as the weights'.  Thread t of
-// the nt converting threads takes items t, t + nt, ...; an item is four
-// consecutive codes of one column.  All loads of a batch are issued before
-// any is used, so a batch costs one L2 round trip.
-template <int BN>
-__device__ __forceinline__ void convert_b(const uint8_t* __restrict__ xq, int M, int nb, int kb0, int R,
-                                          int t, int nt, uint8_t* bdst) {
-  constexpr int kIt = 11;
-  constexpr int kBoxBytes = BN * 128;
-  const int nbr = R >> 5;
-  const int items = BN * nbr * 4;
-  for (int it0 = 0; it0 < items; it0 += nt * kIt) {
-    uint32_t w[kIt][3];
-#pragma unroll
-    for (int j = 0; j < kIt; ++j) {
-      const int it = it0 + t + nt * j;
-      const int m = it / (nbr * 4), rem = it - m * (nbr * 4);
-      const int bl = rem >> 2, i = rem & 3;
-      w[j][0] = w[j][1] = w[j][2] = 0u;
-      if (it < items && m < M) {
-        const uint32_t* blk =
-            reinterpret_cast<const uint32_t*>(xq + (static_cast<int64_t>(m) * nb + kb0 + bl) * 36);
-        w[j][0] = __ldg(blk);
-        w[j][1] = __ldg(blk + 1 + i);
-        w[j][2] = __ldg(blk + 5 + i);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kIt; ++j) {
-      const int it = it0 + t + nt * j;
-      if (it >= items) break;
-      const int m = it / (nbr * 4), rem = it - m * (nbr * 4);
-      const int bl = rem >> 2, i = rem & 3;
-      const float d8 = __half2float(__ushort_as_half(static_cast<unsigned short>(w[j][0] & 0xFFFFu)));
-      const uint32_t lo = w[j][1], hi = w[j][2];
-      auto c = [](uint32_t v, int b) { return static_cast<float>(static_cast<int8_t>((v >> (8 * b)) & 0xFFu)); };
-      uint4 v;
-      v.x = pack_h2(d8 * c(lo, 0), d8 * c(lo, 2));
-      v.y = pack_h2(d8 * c(hi, 0), d8 * c(hi, 2));
-      v.z = pack_h2(d8 * c(lo, 1), d8 * c(lo, 3));
-      v.w = pack_h2(d8 * c(hi, 1), d8 * c(hi, 3));
-      const int chunk = 4 * (bl & 1) + i;
-      *reinterpret_cast<uint4*>(bdst + (bl >> 1) * kBoxBytes + m * 128 + ((chunk ^ (m & 7)) << 4)) = v;
-    }
-  }
-  fence_proxy_async_smem();
 }
 
 template <int BN, bool kArgmax>
@@ -197,9 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
       tempty[2], sfull[2], sempty[2], bready, done;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ int s_last;                         // the epilogue's unit completed its tile
-  __shared__ volatile int s_evote[2];            // epilogue warps' abort vote, per unit parity
+  __shared__ unsigned char s_lastu[kMaxUnits];   // per unit: this CTA completed the tile
   __shared__ uint64_t s_key[4][32];
+  __shared__ uint64_t s_kc[32];                 // split-K argmax keys per column
   __shared__ uint64_t s_cta[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -211,8 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
   const int split = static_cast<int>(blockIdx.x) % S;
   const int tile0 = static_cast<int>(blockIdx.x) / S, tstep = static_cast<int>(gridDim.x) / S;
   const int my_units = tile0 < ntiles ? (ntiles - 1 - tile0) / tstep + 1 : 0;
-  const int su = R / kSK;                        // A buffers (K steps of 256) per unit
-  const int spu = (su + 1) >> 1;                 // copy stages per unit (the last may hold one box)
+  const int su = R / kSK;                        // stages per unit
   const int total = my_units * su;
   const int kb0 = split * (R >> 5);              // first block of this CTA's K range
 
@@ -231,12 +158,13 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
       mbar_init(&sfull[a], 1);
       mbar_init(&sempty[a], 8);
     }
-    mbar_init(&bready, 12);
+    mbar_init(&bready, 8);
     mbar_init(&done, 1);
     s_abort = 0;
-    s_evote[0] = s_evote[1] = 0;
-    for (int c = 0; c < 32; ++c)
+    for (int c = 0; c < 32; ++c) {
+      s_kc[c] = 0ull;
       for (int w = 0; w < 4; ++w) s_key[w][c] = 0ull;
+    }
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -254,10 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
     // ---------------- weight copies (weights are never written by a decode kernel)
     if (lane == 0) {
       int issued = 0, sissued = 0;
-      for (int i = 0; i < my_units * spu; ++i) {
+      for (int i = 0; i < total; ++i) {
         const int s = i % kStages;
-        const int u = i / spu, js = i - u * spu, tile = tile0 + u * tstep;
-        if (js == 0) {
+        const int u = i / su, tile = tile0 + u * tstep;
+        if (i % su == 0) {
           // the unit's scales (the scale plane as bytes: block b at 2 b)
           const int sb = u & 1;
           if (u >= 2 && !mbar_wait(&sempty[sb], ((u >> 1) & 1) ^ 1)) { s_abort = 1; break; }
@@ -267,14 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
         }
         if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) & 1) ^ 1)) { s_abort = 1; break; }
         if (s_abort) break;
-        // two 128-byte boxes per row (256 contiguous code bytes): one box per
-        // stage streamed at about 5.2 TB/s on GB300, two at 6.4-6.6 TB/s
-        const int k0 = split * R + js * 2 * kSK;
-        const int nbox = 2 * js + 1 < su ? 2 : 1;
-        mbar_expect_tx(&full[s], nbox * kCodeBytes);
+        const int k0 = split * R + (i % su) * kSK;
+        mbar_expect_tx(&full[s], kStageBytes);
         tma_load_2d(base + s * kStageBytes, &tq, k0 >> 1, tile * kRows, &full[s]);
-        if (nbox == 2)
-          tma_load_2d(base + s * kStageBytes + kCodeBytes, &tq, (k0 >> 1) + kSK / 2, tile * kRows, &full[s]);
         issued = i + 1;
       }
       if (s_abort) {
@@ -300,15 +223,11 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
           const int i = u * su + j, a = i % kAbufs;
           if (!mbar_wait(&afull[a], (i / kAbufs) & 1)) { s_abort = 1; break; }
           tc_fence_after();
-          // descriptors of the step computed once: B box kk / 4 of the step
-          // (kBoxBytes apart), its 32-byte K slice kk % 4 (the start address
-          // field counts 16 bytes and cannot overflow inside shared memory)
-          const uint64_t bd0 = sw128_desc(bbase + j * (kSK / 64) * Sh::kBoxBytes);
-          const uint32_t at0 = tmem + a * kAcols;
 #pragma unroll
           for (int kk = 0; kk < kSK / 16; ++kk) {
-            const uint64_t bd = bd0 + static_cast<uint64_t>(((kk >> 2) * Sh::kBoxBytes >> 4) + 2 * (kk & 3));
-            tc_mma_ta(d, at0 + 8 * kk, bd, idesc, (j | kk) != 0);
+            const int k = j * kSK + 16 * kk;     // K offset inside the unit
+            const uint64_t bd = sw128_desc(bbase + (k >> 6) * Sh::kBoxBytes) + 2 * ((k & 63) >> 4);
+            tc_mma_ta(d, tmem + a * kAcols + 8 * kk, bd, idesc, (j | kk) != 0);
           }
           tc_commit(&aempty[a]);
           issued = true;
@@ -326,30 +245,65 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
     // ---------------- decoders: thread = weight row = tensor-memory lane
     const int dw = warp - 2, q = warp & 3, h = dw >> 2;
     const int r = 32 * q + lane;
-    // weights and scales only: decoding starts before the previous kernel
-    // on the stream has finished.  Once the three A buffers are filled the
-    // decoders wait for it and take 2/3 of the activation conversion
-    // (the epilogue warps the rest): one L2 round trip instead of two.
-    bool converted = false;
-    auto convert = [&]() {
-      pdl_wait();
-      convert_b<BN>(xq, M, nb, kb0, R, dw * 32 + lane, 384, gbase + (bbase - base));
+    pdl_wait();
+    // activations of this CTA's K range -> f16 d8 * q8 in the 128-byte
+    // swizzle layout (one 64-element box of BN rows per 4 KB), K order as
+    // the weights'
+    {
+      // batches of eight items per thread: every load of a batch is issued
+      // before any is used, so a batch costs one L2 round trip
+      constexpr int kIt = 8;
+      const int nbr = R >> 5;
+      const int items = BN * nbr * 4;
+      for (int it0 = 0; it0 < items; it0 += 256 * kIt) {
+      uint32_t w[kIt][3];
+#pragma unroll
+      for (int j = 0; j < kIt; ++j) {
+        const int it = it0 + dw * 32 + lane + 256 * j;
+        const int m = it / (nbr * 4), rem = it - m * (nbr * 4);
+        const int bl = rem >> 2, i = rem & 3;
+        w[j][0] = w[j][1] = w[j][2] = 0u;
+        if (it < items && m < M) {
+          const uint32_t* blk =
+              reinterpret_cast<const uint32_t*>(xq + (static_cast<int64_t>(m) * nb + kb0 + bl) * 36);
+          w[j][0] = __ldg(blk);
+          w[j][1] = __ldg(blk + 1 + i);
+          w[j][2] = __ldg(blk + 5 + i);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kIt; ++j) {
+        const int it = it0 + dw * 32 + lane + 256 * j;
+        if (it >= items) break;
+        const int m = it / (nbr * 4), rem = it - m * (nbr * 4);
+        const int bl = rem >> 2, i = rem & 3;
+        const float d8 = __half2float(__ushort_as_half(static_cast<unsigned short>(w[j][0] & 0xFFFFu)));
+        const uint32_t lo = w[j][1], hi = w[j][2];
+        auto c = [](uint32_t v, int b) { return static_cast<float>(static_cast<int8_t>((v >> (8 * b)) & 0xFFu)); };
+        uint4 v;
+        v.x = pack_h2(d8 * c(lo, 0), d8 * c(lo, 2));
+        v.y = pack_h2(d8 * c(hi, 0), d8 * c(hi, 2));
+        v.z = pack_h2(d8 * c(lo, 1), d8 * c(lo, 3));
+        v.w = pack_h2(d8 * c(hi, 1), d8 * c(hi, 3));
+        const int chunk = 4 * (bl & 1) + i;
+        *reinterpret_cast<uint4*>(gbase + (bbase - base) + (bl >> 1) * Sh::kBoxBytes + m * 128 +
+                                  ((chunk ^ (m & 7)) << 4)) = v;
+      }
+      }
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bready);
-      converted = true;
-    };
+    }
     for (int i = 0; i < total; ++i) {
-      if (i == kAbufs) convert();
-      const int a = i % kAbufs;
+      const int s = i % kStages, a = i % kAbufs;
       const int u = i / su, j = i % su, sb = u & 1;
-      const int g = u * spu + (j >> 1), s = g % kStages, half = j & 1;   // copy stage, box
-      bool ok = mbar_wait(&full[s], (g / kStages) & 1);
+      bool ok = mbar_wait(&full[s], (i / kStages) & 1);
       ok = ok && mbar_wait(&aempty[a], ((i / kAbufs) & 1) ^ 1);
       if (j == 0) ok = ok && mbar_wait(&sfull[sb], (u >> 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) { s_abort = 1; break; }
       if (s_abort) break;
       tc_fence_after();
-      const uint8_t* st = gbase + s * kStageBytes + half * kCodeBytes;
+      const uint8_t* st = gbase + s * kStageBytes;
       // this warp's four scales of stage j: blocks 8j + 4h .. 8j + 4h + 3 of
       // the unit, two fp16 per 32-bit word (rows R / 16 bytes apart)
       const uint2 sc = *reinterpret_cast<const uint2*>(gbase + (sbase - base) + sb * kSBuf +
@@ -373,30 +327,32 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&afull[a]);
-        if (half == 1 || j == su - 1) mbar_arrive(&empty[s]);
+        mbar_arrive(&empty[s]);
         if (j == su - 1) mbar_arrive(&sempty[sb]);
       }
     }
-    if (!converted) convert();
   } else {
     // ---------------- epilogue: tensor-memory lanes 32q..32q+31 belong to warp q (mod 4)
     const int q = warp & 3, et = threadIdx.x - 320, lr = 32 * q + lane;
     pdl_wait();
-    // its share of the activation conversion (with the decoders)
-    convert_b<BN>(xq, M, nb, kb0, R, 256 + et, 384, gbase + (bbase - base));
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bready);
     uint64_t mybest = 0;
-    const int64_t sstride = static_cast<int64_t>(ntiles) * (BN * kRows);
+    auto emit = [&](int tile, const float (&v)[BN]) {
+      const int row = tile * kRows + lr;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        if (c < M && row < N) Y[static_cast<int64_t>(c) * N + row] = v[c];
+        if (kArgmax) {
+          uint64_t k = (c < M && row < N) ? argmax_key(v[c], static_cast<uint32_t>(row)) : 0ull;
+          k = warp_max_u64(k);
+          if (lane == c) mybest = k > mybest ? k : mybest;
+        }
+      }
+    };
     for (int u = 0; u < my_units; ++u) {
       const int acc = u & 1;
-      // the four warps leave together (they meet at named barriers below):
-      // a vote per unit, in a slot that is not rewritten before every warp
-      // has read it
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], (u >> 1) & 1));
-      if (!ok && lane == 0) s_evote[u & 1] = 1;
-      epilogue_sync();
-      if (s_evote[u & 1]) { s_abort = 1; break; }
+      if (!ok) { s_abort = 1; break; }
+      if (s_abort) break;
       tc_fence_after();
       float v[BN];
       tmem_load_row<BN>(tmem + (static_cast<uint32_t>(32 * q) << 16) + kDcol0 + acc * BN, v);
@@ -404,66 +360,78 @@ __global__ void __launch_bounds__(kThreads, 1) q4_tc_kernel(const __grid_constan
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
       const int tile = tile0 + u * tstep;
-      const int row = tile * kRows + lr;
-      bool emit = true;
-      if (S > 1) {
-        // split K: leave this range's partial, count the arrival; the CTA
-        // that completes the tile adds the ranges in split order while the
-        // tensor cores run the next unit
-        float* pt = sk.partials + static_cast<int64_t>(tile) * (BN * kRows) + lr;
+      if (S == 1) {
+        emit(tile, v);
+      } else {
+        float* pp = sk.partials + static_cast<int64_t>(split * ntiles + tile) * (BN * kRows) + lr;
 #pragma unroll
         for (int c = 0; c < BN; ++c)
-          if (c < M) __stcg(pt + split * sstride + c * kRows, v[c]);
-        epilogue_sync();
-        if (lr == 0) {
-          __threadfence();
-          const unsigned prev = atomicAdd(sk.counters + tile, 1u);
-          s_last = prev == static_cast<unsigned>(S) - 1u;
-          if (s_last) sk.counters[tile] = 0u;
-        }
-        epilogue_sync();
-        emit = s_last != 0;
-        if (emit) {
-          __threadfence();
-#pragma unroll
-          for (int c = 0; c < BN; ++c) v[c] = 0.f;
-          constexpr int kG = BN <= 16 ? 4 : 2;    // splits whose loads are in flight together
-          for (int sp0 = 0; sp0 < S; sp0 += kG) {
-            float t[kG][BN];
-#pragma unroll
-            for (int g = 0; g < kG; ++g)
-#pragma unroll
-              for (int c = 0; c < BN; ++c)
-                t[g][c] = (sp0 + g < S && c < M) ? __ldcg(pt + (sp0 + g) * sstride + c * kRows) : 0.f;
-#pragma unroll
-            for (int g = 0; g < kG; ++g)
-#pragma unroll
-              for (int c = 0; c < BN; ++c) v[c] += t[g][c];
-          }
-        }
-        epilogue_sync();                         // s_last is read before the next unit writes it
-      }
-      if (emit) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          if (c < M && row < N) Y[static_cast<int64_t>(c) * N + row] = v[c];
-          if (kArgmax) {
-            uint64_t k = (c < M && row < N) ? argmax_key(v[c], static_cast<uint32_t>(row)) : 0ull;
-            k = warp_max_u64(k);
-            if (lane == c) mybest = k > mybest ? k : mybest;
-          }
-        }
+          if (c < M) __stcg(pp + c * kRows, v[c]);
       }
     }
+    if (S > 1) __threadfence();                 // partials before the arrivals below
     if (kArgmax) s_key[q][lane] = mybest;
   }
 
   __syncthreads();
+  if (S > 1 && !s_abort) {
+    // Split K: one arrival per unit; the CTA that completes a tile adds its
+    // splits in split order, all 448 threads over the tile's M x 128
+    // outputs (each with its splits' loads in flight).  The partials are
+    // scratch (written before they are read, never taken for counters), so
+    // they are not cleared.  s_abort no longer changes: every role is done.
+    for (int u = threadIdx.x; u < my_units; u += kThreads) {
+      const int tile = tile0 + u * tstep;
+      const unsigned prev = atomicAdd(sk.counters + tile, 1u);
+      const bool last = prev == static_cast<unsigned>(S) - 1u;
+      if (last) sk.counters[tile] = 0u;
+      s_lastu[u] = last ? 1 : 0;
+    }
+    __syncthreads();
+    __threadfence();
+    // per thread at most kE outputs of a tile; loads of four splits of all
+    // of them are in flight together, then the outputs
+    constexpr int kE = (BN * kRows + kThreads - 1) / kThreads;
+    const int64_t sstride = static_cast<int64_t>(ntiles) * (BN * kRows);
+    for (int u = 0; u < my_units; ++u) {
+      if (!s_lastu[u]) continue;
+      const int tile = tile0 + u * tstep;
+      const float* pt = sk.partials + static_cast<int64_t>(tile) * (BN * kRows);
+      float v[kE];
+#pragma unroll
+      for (int i = 0; i < kE; ++i) v[i] = 0.f;
+      for (int sp0 = 0; sp0 < S; sp0 += 4) {
+        float t[4][kE];
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+          for (int i = 0; i < kE; ++i) {
+            const int e = threadIdx.x + i * kThreads;
+            t[b][i] = (sp0 + b < S && e < M * kRows) ? __ldcg(pt + (sp0 + b) * sstride + e) : 0.f;
+          }
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+          for (int i = 0; i < kE; ++i) v[i] += t[b][i];
+      }
+#pragma unroll
+      for (int i = 0; i < kE; ++i) {
+        const int e = threadIdx.x + i * kThreads;
+        const int c = e / kRows, row = tile * kRows + (e - c * kRows);
+        if (e < M * kRows && row < N) {
+          Y[static_cast<int64_t>(c) * N + row] = v[i];
+          if (kArgmax)
+            atomicMax(reinterpret_cast<unsigned long long*>(&s_kc[c]),
+                      static_cast<unsigned long long>(argmax_key(v[i], static_cast<uint32_t>(row))));
+        }
+      }
+    }
+  }
   if (s_abort && threadIdx.x == 0 && err) atomicExch(err, kErrGemvWait);
   if (kArgmax) {
     __syncthreads();
     if (threadIdx.x < 32) {
-      uint64_t k = 0ull;
+      uint64_t k = s_kc[threadIdx.x];
       if (static_cast<int>(threadIdx.x) < BN)
         for (int w = 0; w < 4; ++w) k = s_key[w][threadIdx.x] > k ? s_key[w][threadIdx.x] : k;
       s_cta[threadIdx.x] = k;
@@ -550,6 +518,7 @@ Q4TcPlan q4_tc_plan(int M, int N, int K) {
   const int per_split = sms / p.splits;
   const int groups = ntiles < per_split ? ntiles : per_split;
   p.grid = groups * p.splits;
+  if ((ntiles + groups - 1) / groups > kMaxUnits) return Q4TcPlan{};
   p.ok = q4_tc_forced() || (M > 16 && 2 * ntiles * p.splits >= sms);
   return p;
 }
