@@ -505,8 +505,15 @@ class Q4Sweep(Q4M1):
     name = "q4_0_q8_1_m_sweep"
     shapes = [(4096, 4096), (14336, 4096)]
     Ms = (1, 2, 4, 8, 12, 16, 24, 32)
-    kernel = "q4_0_q8_1 (m1_cp / mc_cp / mma)"
+    # the roofline figure is the dominant kernel's: the mma.sync kernel
+    # (M = 5..16) takes the largest share of the step
+    kernel = "q4_0_q8_1_mma"
+    kernel_src = "q4_mma.cu"
     workload_id = 4
+
+    @classmethod
+    def roofline_call(cls, label):
+        return int(label[1:].split("_")[0]) in (8, 12, 16)
 
     def __init__(self, device):
         super().__init__(device)
@@ -749,6 +756,10 @@ class NF4Sweep:
     kernel_src = "nf4_tc.cu"
     workload_id = 3
     launches_per_step = len(Ms)
+
+    @classmethod
+    def roofline_call(cls, label):
+        return label != "M1"                     # M = 1 runs nf4_mma
 
     def __init__(self, device):
         import weight_only_bit_split_gb300 as wobs
@@ -1324,6 +1335,8 @@ def main(argv=None):
         t = time_steps(gk, reps, stream)
         us = t * 1e3 / (reps * wl.copies)
         per_call[label] = {"us": round(us, 3), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+        if hasattr(wl, "roofline_call") and not wl.roofline_call(label):
+            continue                               # another kernel than the dominant one
         tot_b += nbytes
         tot_ms += us * 1e-3
         launches += 1
