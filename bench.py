@@ -258,6 +258,30 @@ class _GraphRunner:
             self.g.replay()
 
 
+def time_call_site(wl, fn, stream, reps):
+    """One call site timed three ways: back to back over the rotated copies
+    (one graph per rotation, five samples: median and interquartile range, us
+    per call), and as an isolated launch (a one-call graph on copy 0, replayed
+    right after a full rotation has evicted that copy from L2; events around
+    it; median of seven)."""
+    gk = _GraphRunner(capture(lambda: [fn(c) for c in range(wl.copies)], stream))
+    time_steps(gk, 2, stream)
+    samples = sorted(time_steps(gk, reps, stream) * 1e3 / (reps * wl.copies) for _ in range(5))
+    g1 = capture(lambda: fn(0), stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    iso = []
+    with torch.cuda.stream(stream):
+        for _ in range(7):
+            gk.replay(1)
+            e0.record(stream)
+            g1.replay()
+            e1.record(stream)
+            e1.synchronize()
+            iso.append(e0.elapsed_time(e1) * 1e3)
+    return samples[2], samples[3] - samples[1], statistics.median(iso)
+
+
 def packed(shapes, dtype, device):
     """One flat device buffer and views of it with the given shapes (16-byte
     aligned offsets), so a step's inputs or outputs move in one copy."""
@@ -1330,11 +1354,9 @@ def main(argv=None):
     tot_b, tot_ms, launches = 0, 0.0, 0
     reps = max(3, min(20, 2000 // max(1, wl.copies)))
     for label, nbytes, fn in wl.kernel_calls():
-        gk = _GraphRunner(capture(lambda fn=fn: [fn(c) for c in range(wl.copies)], stream))
-        time_steps(gk, 2, stream)
-        t = time_steps(gk, reps, stream)
-        us = t * 1e3 / (reps * wl.copies)
-        per_call[label] = {"us": round(us, 3), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1)}
+        us, iqr, iso = time_call_site(wl, fn, stream, reps)
+        per_call[label] = {"us": round(us, 3), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                           "iqr_us": round(iqr, 3), "isolated_us": round(iso, 3)}
         if hasattr(wl, "roofline_call") and not wl.roofline_call(label):
             continue                               # another kernel than the dominant one
         tot_b += nbytes
@@ -1344,12 +1366,9 @@ def main(argv=None):
     # other ways of computing the same product, timed the same way, outside
     # the roofline figure
     for label, nbytes, fn in (wl.extra_calls() if hasattr(wl, "extra_calls") else []):
-        gk = _GraphRunner(capture(lambda fn=fn: [fn(c) for c in range(wl.copies)], stream))
-        time_steps(gk, 2, stream)
-        t = time_steps(gk, reps, stream)
-        us = t * 1e3 / (reps * wl.copies)
+        us, iqr, iso = time_call_site(wl, fn, stream, reps)
         per_call[label] = {"us": round(us, 3), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
-                           "extra": True}
+                           "iqr_us": round(iqr, 3), "isolated_us": round(iso, 3), "extra": True}
     peak, peak_kind = measured_peaks()
     traffic = traffic_record(cls.kernel if isinstance(cls.kernel, str) else None)
 
