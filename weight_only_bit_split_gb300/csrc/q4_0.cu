@@ -572,6 +572,170 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc_cp_kernel(
   }
 }
 
+// The same stream for 2..4 columns with two rows per warp: half-warp h
+// takes row 2p + h of the warp's row pair p, and a segment is 64 blocks of
+// both rows (2048 bytes of codes, 256 of scales: the ring keeps its size).
+// Lanes l and l + 16 read the same activation block, so each read of the
+// activation planes serves both rows; with four columns those reads, not
+// the weight stream, are the larger part of the shared-memory traffic.
+constexpr int kPairSegBlocks = 64;
+constexpr int kPairSegQs = 2 * kPairSegBlocks * 16;
+constexpr int kPairSegBytes = kPairSegQs + 2 * kPairSegBlocks * 2;
+static_assert(kPairSegBytes == kSegBytes, "the pair kernel uses the same ring");
+
+template <int MC, bool kArgmax>
+__global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
+    const uint8_t* __restrict__ qs, const uint16_t* __restrict__ d4, const uint8_t* __restrict__ xq,
+    int M, float* __restrict__ Y, int N, int K, ArgmaxArgs am) {
+  constexpr int W = McShape<MC>::kWarps;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int nb = K >> 5;
+  const int kh = K >> 1;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int h = lane >> 4, hl = lane & 15;
+  const int total_warps = gridDim.x * W;
+  const int wg = warp * gridDim.x + blockIdx.x;   // row pairs round-robin over the CTAs first
+  const int npairs = (N + 1) >> 1;
+  const int nseg = (nb + kPairSegBlocks - 1) / kPairSegBlocks;
+  const int pairs_w = wg < npairs ? (npairs - 1 - wg) / total_warps + 1 : 0;
+  const int T = pairs_w * nseg;
+  uint8_t* myring = smem + warp * (kRing * kPairSegBytes);
+  int4* x_lo = reinterpret_cast<int4*>(smem + McShape<MC>::kRingBytes);   // [MC][nb]
+  int4* x_hi = x_lo + MC * nb;
+  float2* x_ds = reinterpret_cast<float2*>(x_hi + MC * nb);               // (d, exact sum)
+
+  int pp = wg, pseg = 0;
+  auto issue = [&](int slot) {
+    uint8_t* st = myring + slot * kPairSegBytes;
+    const int b0 = pseg * kPairSegBlocks;
+    const int n = min(kPairSegBlocks, nb - b0);
+    const int r0 = 2 * pp;
+    const bool two = r0 + 1 < N;
+    // codes: 16-byte chunk j of 128 is block b0 + (j & 63) of row r0 + (j >> 6)
+#pragma unroll
+    for (int u = 0; u < 2 * kPairSegBlocks / 32; ++u) {
+      const int j = 32 * u + lane, rr = j >> 6, bl = j & 63;
+      if (bl < n && (rr == 0 || two))
+        cp_async16(st + 16 * j, qs + static_cast<int64_t>(r0 + rr) * kh + (b0 + bl) * 16);
+    }
+    // scales: 16-byte chunk c (8 blocks) of row r0 + rr
+    if (lane < 16) {
+      const int rr = lane >> 3, c = lane & 7;
+      if (8 * c < n && (rr == 0 || two))
+        cp_async16(st + kPairSegQs + 128 * rr + 16 * c,
+                   reinterpret_cast<const uint8_t*>(d4 + static_cast<int64_t>(r0 + rr) * nb + b0) + 16 * c);
+    }
+    if (++pseg == nseg) { pseg = 0; pp += total_warps; }
+  };
+#pragma unroll
+  for (int i = 0; i < kRing - 1; ++i) {
+    if (i < T) issue(i);
+    cp_async_commit();
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+  for (int i = threadIdx.x; i < MC * nb; i += W * 32) {
+    const int m = i / nb, b = i - m * nb;
+    if (m < M) {
+      const XBlock xb = load_xblock(xq + 36 * (static_cast<int64_t>(m) * nb + b));
+      x_lo[i] = xb.lo;
+      x_hi[i] = xb.hi;
+      x_ds[i] = make_float2(xb.d, __int_as_float(xb.s));
+    } else {
+      x_lo[i] = make_int4(0, 0, 0, 0);
+      x_hi[i] = make_int4(0, 0, 0, 0);
+      x_ds[i] = make_float2(0.f, __int_as_float(0));
+    }
+  }
+  __syncthreads();
+
+  int cpair = wg, cseg = 0;
+  float acc[MC];
+#pragma unroll
+  for (int m = 0; m < MC; ++m) acc[m] = 0.f;
+  uint64_t best[MC];
+#pragma unroll
+  for (int m = 0; m < MC; ++m) best[m] = 0ull;
+  for (int t = 0; t < T; ++t) {
+    if (t + kRing - 1 < T) issue((t + kRing - 1) % kRing);
+    cp_async_commit();
+    cp_async_wait<kRing - 1>();
+    __syncwarp();
+    const uint8_t* st = myring + (t % kRing) * kPairSegBytes;
+    const int b0 = cseg * kPairSegBlocks;
+    const int n = min(kPairSegBlocks, nb - b0);
+    // a missing second row of the last pair computes on stale bytes and
+    // writes nothing
+#pragma unroll
+    for (int u = 0; u < kPairSegBlocks / 16; ++u) {
+      const int bl = 16 * u + hl;
+      if (bl < n) {
+        const uint4 q = *reinterpret_cast<const uint4*>(st + h * (kPairSegBlocks * 16) + 16 * bl);
+        const float dw = half_bits_to_float(
+            *reinterpret_cast<const uint16_t*>(st + kPairSegQs + h * (kPairSegBlocks * 2) + 2 * bl));
+        const int b = b0 + bl;
+        const int lo0 = static_cast<int>(q.x & 0x0F0F0F0Fu), lo1 = static_cast<int>(q.y & 0x0F0F0F0Fu);
+        const int lo2 = static_cast<int>(q.z & 0x0F0F0F0Fu), lo3 = static_cast<int>(q.w & 0x0F0F0F0Fu);
+        const int hi0 = static_cast<int>((q.x >> 4) & 0x0F0F0F0Fu), hi1 = static_cast<int>((q.y >> 4) & 0x0F0F0F0Fu);
+        const int hi2 = static_cast<int>((q.z >> 4) & 0x0F0F0F0Fu), hi3 = static_cast<int>((q.w >> 4) & 0x0F0F0F0Fu);
+#pragma unroll
+        for (int m = 0; m < MC; ++m) {
+          const int4 xl = x_lo[m * nb + b], xh = x_hi[m * nb + b];
+          const float2 ds = x_ds[m * nb + b];
+          int sdot = -8 * __float_as_int(ds.y);
+          sdot = __dp4a(lo0, xl.x, sdot); sdot = __dp4a(lo1, xl.y, sdot);
+          sdot = __dp4a(lo2, xl.z, sdot); sdot = __dp4a(lo3, xl.w, sdot);
+          sdot = __dp4a(hi0, xh.x, sdot); sdot = __dp4a(hi1, xh.y, sdot);
+          sdot = __dp4a(hi2, xh.z, sdot); sdot = __dp4a(hi3, xh.w, sdot);
+          acc[m] = fmaf(static_cast<float>(sdot), dw * ds.x, acc[m]);
+        }
+      }
+    }
+    if (cseg == nseg - 1) {
+      const int row = 2 * cpair + h;
+#pragma unroll
+      for (int m = 0; m < MC; ++m) {
+        float sum = acc[m];
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);   // within the half
+        if (m < M && row < N) {
+          if (hl == m) Y[static_cast<int64_t>(m) * N + row] = sum;
+          if (kArgmax) {
+            const uint64_t k = argmax_key(sum, static_cast<uint32_t>(row));
+            best[m] = k > best[m] ? k : best[m];
+          }
+        }
+        acc[m] = 0.f;
+      }
+    }
+    if (++cseg == nseg) { cseg = 0; cpair += total_warps; }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  if (kArgmax) {
+    __shared__ uint64_t s_best[W][MC];
+    __shared__ uint64_t s_cta[MC];
+#pragma unroll
+    for (int m = 0; m < MC; ++m) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, best[m], 16);   // the other row of the pair
+      best[m] = o > best[m] ? o : best[m];
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int m = 0; m < MC; ++m) s_best[warp][m] = best[m];
+    }
+    __syncthreads();
+    if (threadIdx.x < MC) {
+      uint64_t bk = 0;
+      for (int i = 0; i < W; ++i) bk = s_best[i][threadIdx.x] > bk ? s_best[i][threadIdx.x] : bk;
+      s_cta[threadIdx.x] = bk;
+    }
+    __syncthreads();
+    argmax_publish(s_cta, M, am, gridDim.x);
+  }
+}
+
 template <int MC>
 int mc_smem(int K) {
   return McShape<MC>::kRingBytes + MC * (K / 32) * 40;
@@ -582,12 +746,21 @@ cudaError_t run_mc_t(const uint8_t* qs, const void* d, const void* xq, int M, fl
                      int K, const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   constexpr int W = McShape<MC>::kWarps;
   const int smem = mc_smem<MC>(K);
-  auto kern = q4_mc_cp_kernel<MC, kArgmax>;
+  // two rows per warp except for 2 columns on tall matrices (GB300, us per
+  // call back to back, one row / two rows per warp: M = 2 4096^2 4.04 / 3.64,
+  // 14336x4096 8.16 / 8.34; M = 4 4096^2 5.45 / 5.12, 14336x4096 12.47 /
+  // 12.18); WOBS_Q4MC=1 or 2 forces one of them
+  const char* v = std::getenv("WOBS_Q4MC");
+  bool pairs = !(MC == 2 && N >= 8192);
+  if (v && v[0] == '1') pairs = false;
+  if (v && v[0] == '2') pairs = true;
+  auto kern = pairs ? q4_mc2_cp_kernel<MC, kArgmax> : q4_mc_cp_kernel<MC, kArgmax>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int per_sm = max_resident_ctas(reinterpret_cast<const void*>(kern), W * 32, smem);
   int grid = device_sm_count() * (per_sm > 0 ? per_sm : 1);
-  if (grid > N) grid = N;
+  const int units = pairs ? (N + 1) / 2 : N;   // rows or row pairs
+  if (grid > units) grid = units;
   info->grid_x = grid;
   info->block = W * 32;
   info->smem = smem;
