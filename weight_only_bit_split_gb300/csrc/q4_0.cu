@@ -572,16 +572,20 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc_cp_kernel(
   }
 }
 
-// The same stream for 2..4 columns with two rows per warp: half-warp h
-// takes row 2p + h of the warp's row pair p, and a segment is 64 blocks of
-// both rows (2048 bytes of codes, 256 of scales: the ring keeps its size).
-// Lanes l and l + 16 read the same activation block, so each read of the
-// activation planes serves both rows; with four columns those reads, not
-// the weight stream, are the larger part of the shared-memory traffic.
+// The same stream for 2..4 columns with two rows per warp: lane l takes
+// row 2p + (l & 1) of the warp's row pair p and block l >> 1 of each group
+// of 16, and a segment is 64 blocks of both rows.  In the segment each row
+// keeps its codes and its scales contiguous (so every cp.async fills whole
+// lines of shared memory in the global order), the second row's planes 64
+// bytes past a bank period so that the two rows' reads of one block fall
+// in different banks.  Lanes 2j and 2j + 1 read the same activation block
+// in the same quarter-warp: every read of the activation planes is a
+// broadcast serving both rows.
 constexpr int kPairSegBlocks = 64;
-constexpr int kPairSegQs = 2 * kPairSegBlocks * 16;
-constexpr int kPairSegBytes = kPairSegQs + 2 * kPairSegBlocks * 2;
-static_assert(kPairSegBytes == kSegBytes, "the pair kernel uses the same ring");
+constexpr int kPairCodesB = kPairSegBlocks * 16 + 64;               // second row's codes: 1088
+constexpr int kPairScaleA = kPairCodesB + kPairSegBlocks * 16;      // 2112
+constexpr int kPairScaleB = kPairScaleA + kPairSegBlocks * 2 + 64;  // 2304
+constexpr int kPairSegBytes = kPairScaleB + kPairSegBlocks * 2;     // 2432
 
 template <int MC, bool kArgmax>
 __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
@@ -593,7 +597,7 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
   const int kh = K >> 1;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int h = lane >> 4, hl = lane & 15;
+  const int h = lane & 1, hl = lane >> 1;
   const int total_warps = gridDim.x * W;
   const int wg = warp * gridDim.x + blockIdx.x;   // row pairs round-robin over the CTAs first
   const int npairs = (N + 1) >> 1;
@@ -601,9 +605,9 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
   const int pairs_w = wg < npairs ? (npairs - 1 - wg) / total_warps + 1 : 0;
   const int T = pairs_w * nseg;
   uint8_t* myring = smem + warp * (kRing * kPairSegBytes);
-  int4* x_lo = reinterpret_cast<int4*>(smem + McShape<MC>::kRingBytes);   // [MC][nb]
+  int4* x_lo = reinterpret_cast<int4*>(smem + W * kRing * kPairSegBytes);   // [MC][nb]
   int4* x_hi = x_lo + MC * nb;
-  float2* x_ds = reinterpret_cast<float2*>(x_hi + MC * nb);               // (d, exact sum)
+  float2* x_ds = reinterpret_cast<float2*>(x_hi + MC * nb);                 // (d, exact sum)
 
   int pp = wg, pseg = 0;
   auto issue = [&](int slot) {
@@ -617,13 +621,14 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
     for (int u = 0; u < 2 * kPairSegBlocks / 32; ++u) {
       const int j = 32 * u + lane, rr = j >> 6, bl = j & 63;
       if (bl < n && (rr == 0 || two))
-        cp_async16(st + 16 * j, qs + static_cast<int64_t>(r0 + rr) * kh + (b0 + bl) * 16);
+        cp_async16(st + (rr ? kPairCodesB : 0) + 16 * bl,
+                   qs + static_cast<int64_t>(r0 + rr) * kh + (b0 + bl) * 16);
     }
     // scales: 16-byte chunk c (8 blocks) of row r0 + rr
     if (lane < 16) {
       const int rr = lane >> 3, c = lane & 7;
       if (8 * c < n && (rr == 0 || two))
-        cp_async16(st + kPairSegQs + 128 * rr + 16 * c,
+        cp_async16(st + (rr ? kPairScaleB : kPairScaleA) + 16 * c,
                    reinterpret_cast<const uint8_t*>(d4 + static_cast<int64_t>(r0 + rr) * nb + b0) + 16 * c);
     }
     if (++pseg == nseg) { pseg = 0; pp += total_warps; }
@@ -671,9 +676,9 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
     for (int u = 0; u < kPairSegBlocks / 16; ++u) {
       const int bl = 16 * u + hl;
       if (bl < n) {
-        const uint4 q = *reinterpret_cast<const uint4*>(st + h * (kPairSegBlocks * 16) + 16 * bl);
+        const uint4 q = *reinterpret_cast<const uint4*>(st + (h ? kPairCodesB : 0) + 16 * bl);
         const float dw = half_bits_to_float(
-            *reinterpret_cast<const uint16_t*>(st + kPairSegQs + h * (kPairSegBlocks * 2) + 2 * bl));
+            *reinterpret_cast<const uint16_t*>(st + (h ? kPairScaleB : kPairScaleA) + 2 * bl));
         const int b = b0 + bl;
         const int lo0 = static_cast<int>(q.x & 0x0F0F0F0Fu), lo1 = static_cast<int>(q.y & 0x0F0F0F0Fu);
         const int lo2 = static_cast<int>(q.z & 0x0F0F0F0Fu), lo3 = static_cast<int>(q.w & 0x0F0F0F0Fu);
@@ -698,7 +703,7 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
       for (int m = 0; m < MC; ++m) {
         float sum = acc[m];
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);   // within the half
+        for (int o = 16; o > 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);   // lanes of one row
         if (m < M && row < N) {
           if (hl == m) Y[static_cast<int64_t>(m) * N + row] = sum;
           if (kArgmax) {
@@ -718,7 +723,7 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
     __shared__ uint64_t s_cta[MC];
 #pragma unroll
     for (int m = 0; m < MC; ++m) {
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, best[m], 16);   // the other row of the pair
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, best[m], 1);    // the other row of the pair
       best[m] = o > best[m] ? o : best[m];
     }
     if (lane == 0) {
@@ -736,24 +741,32 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
   }
 }
 
+// Two CTAs of the few-column kernel fit on an SM with this much shared memory each.
+constexpr int kMcSmemMax = 110 * 1024;
+
 template <int MC>
 int mc_smem(int K) {
   return McShape<MC>::kRingBytes + MC * (K / 32) * 40;
+}
+template <int MC>
+int mc_pair_smem(int K) {
+  return McShape<MC>::kWarps * kRing * kPairSegBytes + MC * (K / 32) * 40;
 }
 
 template <int MC, bool kArgmax>
 cudaError_t run_mc_t(const uint8_t* qs, const void* d, const void* xq, int M, float* y, int N,
                      int K, const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   constexpr int W = McShape<MC>::kWarps;
-  const int smem = mc_smem<MC>(K);
-  // two rows per warp except for 2 columns on tall matrices (GB300, us per
-  // call back to back, one row / two rows per warp: M = 2 4096^2 4.04 / 3.64,
-  // 14336x4096 8.16 / 8.34; M = 4 4096^2 5.45 / 5.12, 14336x4096 12.47 /
-  // 12.18); WOBS_Q4MC=1 or 2 forces one of them
+  // two rows per warp (GB300, us per call back to back, one row / two rows
+  // per warp: M = 2 4096^2 4.04 / 3.56, 14336x4096 8.16 / 7.51; M = 4
+  // 4096^2 5.45 / 4.82, 14336x4096 12.47 / 10.49) unless its larger ring
+  // would leave one CTA per SM; WOBS_Q4MC=1 or 2 forces one of them
   const char* v = std::getenv("WOBS_Q4MC");
-  bool pairs = !(MC == 2 && N >= 8192);
+  bool pairs = true;
   if (v && v[0] == '1') pairs = false;
   if (v && v[0] == '2') pairs = true;
+  if (mc_pair_smem<MC>(K) > kMcSmemMax) pairs = false;   // keep two CTAs per SM
+  const int smem = pairs ? mc_pair_smem<MC>(K) : mc_smem<MC>(K);
   auto kern = pairs ? q4_mc2_cp_kernel<MC, kArgmax> : q4_mc_cp_kernel<MC, kArgmax>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -776,8 +789,6 @@ cudaError_t run_mc(const uint8_t* qs, const void* d, const void* xq, int M, floa
                 : run_mc_t<MC, false>(qs, d, xq, M, y, N, K, am, st, info);
 }
 
-// Two CTAs of the few-column kernel fit on an SM with this much shared memory each.
-constexpr int kMcSmemMax = 110 * 1024;
 
 // --------------------------------------------------------- M columns
 
