@@ -58,9 +58,9 @@
  *     call off it; WOBS_Q4F32=16 or 32 runs the fused quantise-and-GEMV
  *     kernel with 16 warps and two CTAs per SM or 32 warps and one (the
  *     default picks by shape; testing only).  WOBS_NF4_P=0..3 also applies
- *     to the NF4 tensor-memory kernel for several columns.  WOBS_Q4MC=1 or 2
- *     runs the 2..4-column Q4_0 kernel with one or two weight rows per warp
- *     (the default picks by shape; testing only).
+ *     to the NF4 tensor-memory kernel for several columns.  WOBS_Q4MC=1, 2
+ *     or 4 runs the 2..4-column Q4_0 kernel with that many weight rows per
+ *     warp (the default picks by shape; testing only).
  */
 #ifndef WOBS_H
 #define WOBS_H

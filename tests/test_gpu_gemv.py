@@ -23,15 +23,16 @@ def m1_path(request, monkeypatch):
     return request.param
 
 
-@pytest.fixture(params=["tc", "mma", "mc1"])
+@pytest.fixture(params=["tc", "mma", "mc1", "mc4"])
 def q4_mc_path(request, monkeypatch):
     """Run a multi-column Q4_0 test through the tcgen05 kernel (forced for 5..32
     columns wherever its plan applies) and with it disabled (mma.sync / few-
-    column / CUDA-core kernels); "mc1" also runs the 2..4-column kernel with
-    one weight row per warp instead of the default choice by shape."""
+    column / CUDA-core kernels); "mc1" and "mc4" also run the 2..4-column
+    kernel with one or four weight rows per warp instead of the default
+    choice by shape."""
     monkeypatch.setenv("WOBS_Q4TC", "1" if request.param == "tc" else "0")
-    if request.param == "mc1":
-        monkeypatch.setenv("WOBS_Q4MC", "1")
+    if request.param in ("mc1", "mc4"):
+        monkeypatch.setenv("WOBS_Q4MC", request.param[-1])
     else:
         monkeypatch.delenv("WOBS_Q4MC", raising=False)
     return request.param

@@ -572,22 +572,25 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc_cp_kernel(
   }
 }
 
-// The same stream for 2..4 columns with two rows per warp: lane l takes
-// row 2p + (l & 1) of the warp's row pair p and block l >> 1 of each group
-// of 16, and a segment is 64 blocks of both rows.  In the segment each row
-// keeps its codes and its scales contiguous (so every cp.async fills whole
-// lines of shared memory in the global order), the second row's planes 64
-// bytes past a bank period so that the two rows' reads of one block fall
-// in different banks.  Lanes 2j and 2j + 1 read the same activation block
-// in the same quarter-warp: every read of the activation planes is a
-// broadcast serving both rows.
-constexpr int kPairSegBlocks = 64;
-constexpr int kPairCodesB = kPairSegBlocks * 16 + 64;               // second row's codes: 1088
-constexpr int kPairScaleA = kPairCodesB + kPairSegBlocks * 16;      // 2112
-constexpr int kPairScaleB = kPairScaleA + kPairSegBlocks * 2 + 64;  // 2304
-constexpr int kPairSegBytes = kPairScaleB + kPairSegBlocks * 2;     // 2432
+// The same stream for 2..4 columns with R = 2 or 4 rows per warp: lane l
+// takes row R p + (l mod R) of the warp's row group p and block l / R of
+// each group of 32 / R, and a segment is 128 / R blocks of the R rows.  In
+// the segment each row keeps its codes and its scales contiguous (so every
+// cp.async fills shared memory in global order), row r's planes 128 r / R
+// bytes past a bank period so that the R rows' reads of one block fall in
+// different banks.  The R lanes of one block sit in the same quarter-warp:
+// every read of the activation planes is a broadcast serving R rows.
+template <int R>
+struct RowGroup {
+  static constexpr int kBlocks = 128 / R;                           // blocks per segment
+  static constexpr int kCodePitch = kBlocks * 16 + 128 / R;          // row r's codes at r * pitch
+  static constexpr int kScale0 = (R - 1) * kCodePitch + kBlocks * 16;
+  static constexpr int kScalePitch = ((kBlocks * 2 + 127) / 128) * 128 + 128 / R;
+  static constexpr int kSegBytes = kScale0 + (R - 1) * kScalePitch + kBlocks * 2;   // 2432 / 2688
+  static_assert(kCodePitch % 16 == 0 && kScale0 % 16 == 0 && kScalePitch % 16 == 0, "16-byte copies");
+};
 
-template <int MC, bool kArgmax>
+template <int MC, int R, bool kArgmax>
 __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
     const uint8_t* __restrict__ qs, const uint16_t* __restrict__ d4, const uint8_t* __restrict__ xq,
     int M, float* __restrict__ Y, int N, int K, ArgmaxArgs am) {
@@ -597,38 +600,39 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
   const int kh = K >> 1;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int h = lane & 1, hl = lane >> 1;
+  using G = RowGroup<R>;
+  constexpr int SB = G::kBlocks;
+  const int h = lane % R, hl = lane / R;
   const int total_warps = gridDim.x * W;
-  const int wg = warp * gridDim.x + blockIdx.x;   // row pairs round-robin over the CTAs first
-  const int npairs = (N + 1) >> 1;
-  const int nseg = (nb + kPairSegBlocks - 1) / kPairSegBlocks;
-  const int pairs_w = wg < npairs ? (npairs - 1 - wg) / total_warps + 1 : 0;
-  const int T = pairs_w * nseg;
-  uint8_t* myring = smem + warp * (kRing * kPairSegBytes);
-  int4* x_lo = reinterpret_cast<int4*>(smem + W * kRing * kPairSegBytes);   // [MC][nb]
+  const int wg = warp * gridDim.x + blockIdx.x;   // row groups round-robin over the CTAs first
+  const int ngroups = (N + R - 1) / R;
+  const int nseg = (nb + SB - 1) / SB;
+  const int groups_w = wg < ngroups ? (ngroups - 1 - wg) / total_warps + 1 : 0;
+  const int T = groups_w * nseg;
+  uint8_t* myring = smem + warp * (kRing * G::kSegBytes);
+  int4* x_lo = reinterpret_cast<int4*>(smem + W * kRing * G::kSegBytes);    // [MC][nb]
   int4* x_hi = x_lo + MC * nb;
   float2* x_ds = reinterpret_cast<float2*>(x_hi + MC * nb);                 // (d, exact sum)
 
   int pp = wg, pseg = 0;
   auto issue = [&](int slot) {
-    uint8_t* st = myring + slot * kPairSegBytes;
-    const int b0 = pseg * kPairSegBlocks;
-    const int n = min(kPairSegBlocks, nb - b0);
-    const int r0 = 2 * pp;
-    const bool two = r0 + 1 < N;
-    // codes: 16-byte chunk j of 128 is block b0 + (j & 63) of row r0 + (j >> 6)
+    uint8_t* st = myring + slot * G::kSegBytes;
+    const int b0 = pseg * SB;
+    const int n = min(SB, nb - b0);
+    const int r0 = R * pp;
+    // codes: 16-byte chunk j of 128 is block b0 + (j mod SB) of row r0 + j / SB
 #pragma unroll
-    for (int u = 0; u < 2 * kPairSegBlocks / 32; ++u) {
-      const int j = 32 * u + lane, rr = j >> 6, bl = j & 63;
-      if (bl < n && (rr == 0 || two))
-        cp_async16(st + (rr ? kPairCodesB : 0) + 16 * bl,
+    for (int u = 0; u < 4; ++u) {
+      const int j = 32 * u + lane, rr = j / SB, bl = j % SB;
+      if (bl < n && r0 + rr < N)
+        cp_async16(st + rr * G::kCodePitch + 16 * bl,
                    qs + static_cast<int64_t>(r0 + rr) * kh + (b0 + bl) * 16);
     }
     // scales: 16-byte chunk c (8 blocks) of row r0 + rr
     if (lane < 16) {
-      const int rr = lane >> 3, c = lane & 7;
-      if (8 * c < n && (rr == 0 || two))
-        cp_async16(st + (rr ? kPairScaleB : kPairScaleA) + 16 * c,
+      const int rr = lane / (SB / 8), c = lane % (SB / 8);
+      if (8 * c < n && r0 + rr < N)
+        cp_async16(st + G::kScale0 + rr * G::kScalePitch + 16 * c,
                    reinterpret_cast<const uint8_t*>(d4 + static_cast<int64_t>(r0 + rr) * nb + b0) + 16 * c);
     }
     if (++pseg == nseg) { pseg = 0; pp += total_warps; }
@@ -667,18 +671,18 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
     cp_async_commit();
     cp_async_wait<kRing - 1>();
     __syncwarp();
-    const uint8_t* st = myring + (t % kRing) * kPairSegBytes;
-    const int b0 = cseg * kPairSegBlocks;
-    const int n = min(kPairSegBlocks, nb - b0);
+    const uint8_t* st = myring + (t % kRing) * G::kSegBytes;
+    const int b0 = cseg * SB;
+    const int n = min(SB, nb - b0);
     // a missing second row of the last pair computes on stale bytes and
     // writes nothing
 #pragma unroll
-    for (int u = 0; u < kPairSegBlocks / 16; ++u) {
-      const int bl = 16 * u + hl;
+    for (int u = 0; u < SB * R / 32; ++u) {
+      const int bl = (32 / R) * u + hl;
       if (bl < n) {
-        const uint4 q = *reinterpret_cast<const uint4*>(st + (h ? kPairCodesB : 0) + 16 * bl);
+        const uint4 q = *reinterpret_cast<const uint4*>(st + h * G::kCodePitch + 16 * bl);
         const float dw = half_bits_to_float(
-            *reinterpret_cast<const uint16_t*>(st + (h ? kPairScaleB : kPairScaleA) + 2 * bl));
+            *reinterpret_cast<const uint16_t*>(st + G::kScale0 + h * G::kScalePitch + 2 * bl));
         const int b = b0 + bl;
         const int lo0 = static_cast<int>(q.x & 0x0F0F0F0Fu), lo1 = static_cast<int>(q.y & 0x0F0F0F0Fu);
         const int lo2 = static_cast<int>(q.z & 0x0F0F0F0Fu), lo3 = static_cast<int>(q.w & 0x0F0F0F0Fu);
@@ -698,12 +702,12 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
       }
     }
     if (cseg == nseg - 1) {
-      const int row = 2 * cpair + h;
+      const int row = R * cpair + h;
 #pragma unroll
       for (int m = 0; m < MC; ++m) {
         float sum = acc[m];
 #pragma unroll
-        for (int o = 16; o > 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);   // lanes of one row
+        for (int o = 16; o >= R; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);   // lanes of one row
         if (m < M && row < N) {
           if (hl == m) Y[static_cast<int64_t>(m) * N + row] = sum;
           if (kArgmax) {
@@ -722,10 +726,12 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
     __shared__ uint64_t s_best[W][MC];
     __shared__ uint64_t s_cta[MC];
 #pragma unroll
-    for (int m = 0; m < MC; ++m) {
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, best[m], 1);    // the other row of the pair
-      best[m] = o > best[m] ? o : best[m];
-    }
+    for (int m = 0; m < MC; ++m)
+#pragma unroll
+      for (int o = 1; o < R; o <<= 1) {                               // the other rows of the group
+        const uint64_t k = __shfl_xor_sync(0xffffffffu, best[m], o);
+        best[m] = k > best[m] ? k : best[m];
+      }
     if (lane == 0) {
 #pragma unroll
       for (int m = 0; m < MC; ++m) s_best[warp][m] = best[m];
@@ -748,31 +754,34 @@ template <int MC>
 int mc_smem(int K) {
   return McShape<MC>::kRingBytes + MC * (K / 32) * 40;
 }
-template <int MC>
-int mc_pair_smem(int K) {
-  return McShape<MC>::kWarps * kRing * kPairSegBytes + MC * (K / 32) * 40;
+template <int MC, int R>
+int mc_group_smem(int K) {
+  return McShape<MC>::kWarps * kRing * RowGroup<R>::kSegBytes + MC * (K / 32) * 40;
 }
 
 template <int MC, bool kArgmax>
 cudaError_t run_mc_t(const uint8_t* qs, const void* d, const void* xq, int M, float* y, int N,
                      int K, const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   constexpr int W = McShape<MC>::kWarps;
-  // two rows per warp (GB300, us per call back to back, one row / two rows
-  // per warp: M = 2 4096^2 4.04 / 3.56, 14336x4096 8.16 / 7.51; M = 4
-  // 4096^2 5.45 / 4.82, 14336x4096 12.47 / 10.49) unless its larger ring
-  // would leave one CTA per SM; WOBS_Q4MC=1 or 2 forces one of them
+  // rows per warp (GB300, us per call back to back, 1 / 2 / 4 rows per
+  // warp: M = 2 4096^2 4.04 / 3.64 / 4.93, 14336x4096 8.16 / 7.67 / 8.20;
+  // M = 4 4096^2 5.45 / 4.74 / 5.13, 14336x4096 12.47 / 10.54 / 9.62): four
+  // for 3..4 columns on tall matrices, else two; a group ring that would
+  // leave one CTA per SM falls back to fewer rows.  WOBS_Q4MC=1, 2 or 4
+  // forces the rows per warp.
   const char* v = std::getenv("WOBS_Q4MC");
-  bool pairs = true;
-  if (v && v[0] == '1') pairs = false;
-  if (v && v[0] == '2') pairs = true;
-  if (mc_pair_smem<MC>(K) > kMcSmemMax) pairs = false;   // keep two CTAs per SM
-  const int smem = pairs ? mc_pair_smem<MC>(K) : mc_smem<MC>(K);
-  auto kern = pairs ? q4_mc2_cp_kernel<MC, kArgmax> : q4_mc_cp_kernel<MC, kArgmax>;
+  int R = (MC == 4 && N >= 8192) ? 4 : 2;
+  if (v && (v[0] == '1' || v[0] == '2' || v[0] == '4')) R = v[0] - '0';
+  if (R == 4 && mc_group_smem<MC, 4>(K) > kMcSmemMax) R = 2;
+  if (R == 2 && mc_group_smem<MC, 2>(K) > kMcSmemMax) R = 1;
+  const int smem = R == 4 ? mc_group_smem<MC, 4>(K) : R == 2 ? mc_group_smem<MC, 2>(K) : mc_smem<MC>(K);
+  auto kern = R == 4 ? q4_mc2_cp_kernel<MC, 4, kArgmax>
+            : R == 2 ? q4_mc2_cp_kernel<MC, 2, kArgmax> : q4_mc_cp_kernel<MC, kArgmax>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int per_sm = max_resident_ctas(reinterpret_cast<const void*>(kern), W * 32, smem);
   int grid = device_sm_count() * (per_sm > 0 ? per_sm : 1);
-  const int units = pairs ? (N + 1) / 2 : N;   // rows or row pairs
+  const int units = (N + R - 1) / R;   // rows or row groups
   if (grid > units) grid = units;
   info->grid_x = grid;
   info->block = W * 32;
