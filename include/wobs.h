@@ -60,7 +60,9 @@
  *     default picks by shape; testing only).  WOBS_NF4_P=0..3 also applies
  *     to the NF4 tensor-memory kernel for several columns.  WOBS_Q4MC=1, 2
  *     or 4 runs the 2..4-column Q4_0 kernel with that many weight rows per
- *     warp (the default picks by shape; testing only).
+ *     warp (the default picks by shape; testing only).  WOBS_NF4_MC=tc
+ *     takes NF4 calls with 2..4 columns to the tensor-memory kernel instead
+ *     of the mma.sync kernel (testing only).
  */
 #ifndef WOBS_H
 #define WOBS_H
@@ -349,9 +351,12 @@ WOBS_API int wobs_gemv_q8_0_f32(const int8_t* qs, const void* d, const float* x,
  * X[m][i], fp32 accumulation, bf16 output (round to nearest even).
  * Optional fused argmax per column over the bf16 outputs (as stored).
  * M >= 2 runs on the tensor cores with every weight rounded once to f16
- * (relative error <= 2^-11, inside the GEMV tolerance) where K is a multiple
- * of 256 and the planes and activation rows are 16-byte aligned, else on
- * the CUDA cores in fp32.
+ * (relative error <= 2^-11, inside the GEMV tolerance): for 2..4 columns
+ * the one-column mma.sync kernel, each code decoded once for all columns,
+ * where K is a multiple of 1024 up to 8192, the planes and X 16-byte
+ * aligned and ldx a multiple of 8; otherwise the tcgen05 kernel where K is
+ * a multiple of 256 and the planes and activation rows are 16-byte aligned;
+ * else the CUDA cores in fp32.
  *
  *   qs [N][K/2], absmax fp32 [N][K/64], codebook HOST pointer to 16 floats,
  *   X bf16 [M][ldx] (ldx >= K; ignored for M = 1), Y bf16 [M][N], argmax

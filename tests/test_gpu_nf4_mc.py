@@ -1,13 +1,14 @@
 """NF4 with several activation columns and the dequantise-then-GEMM path on
 the GPU, against the fp64 oracle.
 
-The fused multi-column GEMV (wobs_gemv_nf4 with M > 1: the tcgen05 kernel,
-or the CUDA-core kernel where that does not apply) is compared element by
-element with oracle.gemv_nf4 within the bf16 parity bound, its argmax with
-the oracle's argmax of the returned outputs; ragged row tiles, split K
-ranges, columns past the MMA width, scaled inputs, the fallback kernel,
-identical columns, the full 70B MLP shape on sampled rows and guard regions
-around every output are covered.  The dequantiser is bit-exact with
+The fused multi-column GEMV (wobs_gemv_nf4 with M > 1: the mma.sync kernel
+for up to four columns, the tcgen05 kernel, or the CUDA-core kernel where
+neither applies) is compared element by element with oracle.gemv_nf4 within
+the bf16 parity bound, its argmax with the oracle's argmax of the returned
+outputs; ragged row tiles, split K ranges, columns past the MMA width,
+scaled inputs, columns of very different magnitudes, pitched activation
+rows, the fallback kernel, identical columns, the full 70B MLP shape on
+sampled rows and guard regions around every output are covered.  The dequantiser is bit-exact with
 oracle.dequantize_nf4_bf16, and the dequantise-then-GEMM composition is
 compared with the dense oracle on those bf16 weights.
 """
@@ -42,19 +43,24 @@ def _ref(qs, absmax, cb, xb):
     return oracle.gemv_nf4(qs, absmax, cb, xf), oracle.abs_dot_nf4(qs, absmax, cb, xf)
 
 
-@pytest.fixture(params=["tc", "cp"])
+@pytest.fixture(params=["mma", "tc", "cp"])
 def mc_path(request, monkeypatch):
-    """The tensor-memory kernel (default) and the CUDA-core kernel (forced)."""
+    """The default choice (mma.sync kernel for up to four columns, else the
+    tensor-memory kernel), the tensor-memory kernel forced for every M, and
+    the CUDA-core kernel (forced)."""
+    monkeypatch.delenv("WOBS_NF4", raising=False)
+    monkeypatch.delenv("WOBS_NF4_MC", raising=False)
     if request.param == "cp":
         monkeypatch.setenv("WOBS_NF4", "cp")
-    else:
-        monkeypatch.delenv("WOBS_NF4", raising=False)
+    elif request.param == "tc":
+        monkeypatch.setenv("WOBS_NF4_MC", "tc")
     return request.param
 
 
 @pytest.mark.parametrize("n,k,m", [(300, 1024, 2), (1000, 4096, 5), (129, 256, 16), (2000, 2048, 17),
                                    (640, 8192, 32), (4096, 1024, 32), (77, 512, 3), (1, 768, 9),
-                                   (5003, 2048, 8)])
+                                   (5003, 2048, 8), (1000, 8192, 4), (5003, 4096, 3), (64, 2048, 2),
+                                   (4097, 1024, 4)])
 def test_nf4_columns_match_the_oracle(n, k, m, mc_path):
     cb, qs, absmax = _planes(n, k)
     xb = _x(m, k)
@@ -92,6 +98,35 @@ def test_nf4_columns_offset_rows_take_the_fallback():
     assert_within(y.float().cpu().numpy(), ref, ad, "bf16", "nf4 offset activation rows")
 
 
+@pytest.mark.parametrize("m", [2, 3, 4])
+def test_nf4_columns_pitched_rows(m, mc_path):
+    """Activation rows 16-byte aligned with a pitch above K."""
+    n, k = 900, 4096
+    cb, qs, absmax = _planes(n, k, copy=2)
+    xb = _x(m, k, copy=2)
+    big = torch.zeros(m, k + 64, dtype=torch.bfloat16)
+    big[:, :k] = xb
+    xv = big.to(dev())[:, :k]
+    ref, ad = _ref(qs, absmax, cb, xb)
+    y, am = wobs.wobs_gemv_nf4(to_dev(qs), to_dev(absmax), cb, xv, want_argmax=True)
+    yf = y.float().cpu().numpy()
+    assert_within(yf, ref, ad, "bf16", f"nf4 {m} pitched columns ({mc_path})")
+    assert np.array_equal(am.cpu().numpy(), oracle.argmax_rows(yf))
+
+
+@pytest.mark.parametrize("muls", [(2.0 ** 40, 2.0 ** -40), (1.0, 2.0 ** -60, 2.0 ** 30),
+                                  (2.0 ** -30, 1.0, 2.0 ** 50, 3.0e-3)])
+def test_nf4_columns_far_apart_magnitudes(muls, mc_path):
+    """Columns whose magnitudes differ by many powers of two: each column's
+    own scaling must keep every column within its bound."""
+    n, k, m = 700, 8192, len(muls)
+    cb, qs, absmax = _planes(n, k, copy=9)
+    xb = torch.cat([_x(1, k, copy=10 + i, mul=mul) for i, mul in enumerate(muls)])
+    ref, ad = _ref(qs, absmax, cb, xb)
+    y, _ = wobs.wobs_gemv_nf4(to_dev(qs), to_dev(absmax), cb, xb.to(dev()))
+    assert_within(y.float().cpu().numpy(), ref, ad, "bf16", f"nf4 column magnitudes {muls} ({mc_path})")
+
+
 @pytest.mark.parametrize("xmul,cbmul", [(2.0 ** 40, 1.0), (2.0 ** -40, 1.0), (1.0, 1000.0),
                                         (3.0e-3, 2.0 ** -30)])
 def test_nf4_columns_scaled_inputs(xmul, cbmul):
@@ -106,8 +141,9 @@ def test_nf4_columns_scaled_inputs(xmul, cbmul):
     assert_within(y.float().cpu().numpy(), ref, ad, "bf16", f"nf4 columns x*{xmul} cb*{cbmul}")
 
 
-def test_nf4_identical_columns_give_identical_outputs(mc_path):
-    n, k, m = 1000, 2048, 24
+@pytest.mark.parametrize("m", [4, 24])
+def test_nf4_identical_columns_give_identical_outputs(m, mc_path):
+    n, k = 1000, 2048
     cb, qs, absmax = _planes(n, k, copy=4)
     xb = _x(1, k, copy=4).repeat(m, 1)
     y, am = wobs.wobs_gemv_nf4(to_dev(qs), to_dev(absmax), cb, xb.to(dev()), want_argmax=True)
@@ -126,7 +162,7 @@ def test_nf4_columns_deterministic():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("m", [2, 8, 32])
+@pytest.mark.parametrize("m", [2, 4, 8, 32])
 def test_nf4_28672x8192_columns_full_sampled(m):
     n, k = 28672, 8192
     cb = normal_float_levels().numpy()
@@ -146,7 +182,9 @@ def test_nf4_28672x8192_columns_full_sampled(m):
 
 
 @pytest.mark.parametrize("n,k,m,path", [(1000, 4096, 32, "tc"), (333, 1024, 5, "tc"),
-                                        (5003, 8192, 17, "tc"), (700, 1088, 6, "cp")])
+                                        (5003, 8192, 17, "tc"), (700, 1088, 6, "cp"),
+                                        (2049, 8192, 2, "mma"), (333, 1024, 3, "mma"),
+                                        (1000, 4096, 4, "mma")])
 def test_nf4_columns_stay_in_bounds(n, k, m, path, monkeypatch):
     if path == "cp":
         monkeypatch.setenv("WOBS_NF4", "cp")
@@ -172,13 +210,17 @@ def test_nf4_columns_stay_in_bounds(n, k, m, path, monkeypatch):
 def test_nf4_columns_dispatch(monkeypatch, capfd):
     monkeypatch.setenv("WOBS_DEBUG", "1")
     monkeypatch.delenv("WOBS_NF4", raising=False)
-    for k, m in ((8192, 32), (4096, 2), (320, 4)):
+    monkeypatch.delenv("WOBS_NF4_MC", raising=False)
+    for k, m in ((8192, 32), (4096, 2), (8192, 4), (2048, 5), (320, 4), (512, 2)):
         cb, qs, absmax = _planes(256, k)
         wobs.wobs_gemv_nf4(to_dev(qs), to_dev(absmax), cb, _x(m, k).to(dev()))
+    monkeypatch.setenv("WOBS_NF4_MC", "tc")
+    cb, qs, absmax = _planes(256, 4096)
+    wobs.wobs_gemv_nf4(to_dev(qs), to_dev(absmax), cb, _x(3, 4096).to(dev()))
     torch.cuda.synchronize()
     err = capfd.readouterr().err
     kernels = [ln.split("kernel=")[1].split()[0] for ln in err.splitlines() if ln.startswith("wobs: op=")]
-    assert kernels == ["nf4_tc", "nf4_tc", "nf4_mn"], kernels
+    assert kernels == ["nf4_tc", "nf4_mma", "nf4_mma", "nf4_tc", "nf4_mn", "nf4_tc", "nf4_tc"], kernels
 
 
 # ------------------------------------------------------- dequantise -> GEMM

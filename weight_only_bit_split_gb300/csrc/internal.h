@@ -167,11 +167,12 @@ constexpr int kErrSelfTestWait = 3;   // the failure-path self test's wait gave 
 bool m1_ldg_forced();
 // WOBS_NF4=cp: NF4 GEMVs take the CUDA-core staged kernel, not the tensor-core one
 bool nf4_cp_forced();
-// NF4 M = 1 on the tensor cores; cudaErrorNotSupported when the shape, the
-// alignment or the codebook rules it out (the caller then takes another kernel)
+// NF4 for 1..4 activation columns (x [M][ldx] bf16, y [M][N]) on mma.sync;
+// cudaErrorNotSupported when the shape, the alignment or the codebook rules
+// it out (the caller then takes another kernel)
 cudaError_t launch_nf4_mma(const uint8_t* qs, const float* absmax, const Codebook16& cb,
-                           const void* x, void* y, int N, int K, const ArgmaxArgs& am,
-                           cudaStream_t st, Launch* info);
+                           const void* x, int64_t ldx, int M, void* y, int N, int K,
+                           const ArgmaxArgs& am, cudaStream_t st, Launch* info);
 
 // ---- shared launch-shape helpers (api.cu) ----
 int device_sm_count();                       // current device, cached

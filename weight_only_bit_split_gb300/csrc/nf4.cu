@@ -22,6 +22,9 @@
 //   * at the end of a batch a 31-shuffle reduce-scatter leaves row r's warp
 //     partial in lane r; warps combine through shared memory in a fixed
 //     order, so the result does not depend on timing.
+#include <cstdlib>
+#include <cstring>
+
 #include "common.cuh"
 
 namespace wobs {
@@ -497,6 +500,16 @@ cudaError_t launch_gemv_nf4_mc(const uint8_t* qs, const float* absmax, const Cod
                                const void* X, int64_t ldx, int M, void* Y, int N, int K,
                                const SplitArgs& sk, const ArgmaxArgs& am, cudaStream_t st,
                                Launch* info) {
+  // up to four columns: the one-column tensor-core kernel serves them all
+  // (its B operand has eight columns; the decode is shared), unless
+  // WOBS_NF4_MC=tc asks for the tensor-memory kernel
+  const char* mcv = std::getenv("WOBS_NF4_MC");
+  const bool tc_forced = mcv && std::strcmp(mcv, "tc") == 0;
+  if (M <= 4 && !nf4_cp_forced() && !tc_forced && !m1_ldg_forced()) {
+    cudaError_t e = launch_nf4_mma(qs, absmax, cb, X, ldx, M, Y, N, K, am, st, info);
+    if (e != cudaErrorNotSupported) return e;
+    cudaGetLastError();
+  }
   if (!nf4_cp_forced()) {
     cudaError_t e = launch_nf4_tc(qs, absmax, cb, X, ldx, M, Y, N, K, sk, am, st, info);
     if (e != cudaErrorNotSupported) return e;
@@ -517,7 +530,7 @@ cudaError_t launch_gemv_nf4(const uint8_t* qs, const float* absmax, const Codebo
   // scaled codebook, 16-byte aligned planes); WOBS_NF4=cp selects the
   // CUDA-core staged variant instead
   if (!m1_ldg_forced() && !nf4_cp_forced()) {
-    cudaError_t e = launch_nf4_mma(qs, absmax, cb, x, y, N, K, am, st, info);
+    cudaError_t e = launch_nf4_mma(qs, absmax, cb, x, K, 1, y, N, K, am, st, info);
     if (e != cudaErrorNotSupported) return e;
     cudaGetLastError();
   }

@@ -1,5 +1,5 @@
-// NF4 blockwise 4-bit decode GEMV, M = 1, with the products on the tensor
-// cores.
+// NF4 blockwise 4-bit decode GEMV for one to four activation columns, with
+// the products on the tensor cores.
 //
 // bitsandbytes issue #1842 ("70B 4-bit LLM decode bottlenecked by HIP kernel
 // (kgemm_4bit_inference_naive) efficiency"): the fused 4-bit inference GEMV
@@ -38,7 +38,14 @@
 //     no bank twice;
 //   * the table lives at shared-window address 0x20000, so the lookup
 //     address of a byte is one byte permute of the code word and a constant
-//     (0x20000 | lane * 4), with no add.
+//     (0x20000 | lane * 4), with no add;
+//   * two to four columns share every decoded code: the MMA's B operand
+//     has eight columns, lane (g, t) supplies column g % M, and the sums of
+//     columns 2t and 2t + 1 come back in lane (g, t).  The extra columns'
+//     activations need shared memory beside the table, so the ring has
+//     three stages for two columns and two for four.  One column keeps its
+//     own kernel: the column form instantiated for one column ran 2 us
+//     slower on the 70B matrix (28.9 against 26.9 us).
 #include <cmath>
 #include <cstdlib>
 
@@ -57,8 +64,8 @@ constexpr uint32_t kTabAddr = 0x20000;       // shared-window address of the tab
 constexpr int kTabBytes = 256 * 256;         // entry e: 64 words at e * 256, lane l reads word l;
                                              // bytes 128..255 of entry c hold activation block c
 constexpr int kMaxStages = 4;
-constexpr int kMiscBytes = 512;              // barriers, counters, codebook, argmax keys
-constexpr int kRedBytes = kMaxStages * kKG * kRB * 4;
+constexpr int kMiscBytes = 512;              // barriers, counters, codebook, scales, argmax keys
+constexpr int kRedBytes = kMaxStages * kKG * kRB * 4;   // one-column partials
 // A stage: 64 rows x 1024 codes (four 128-byte x 64-row code boxes in the
 // 128-byte swizzle, 8 KB each) and their 16 absmax per row (4 KB).
 constexpr int kKS = 1024;                    // codes per row per stage
@@ -145,18 +152,21 @@ __device__ __forceinline__ void pow2_scale(float m, float& scale, float& inv) {
 }
 
 // Shared-memory layout, from the dynamic base `base` (same in every CTA):
-// [base, +512) misc, [+512, +512 + kRedBytes) warp partials, then 1024-byte
-// aligned stage slots up to the table at 0x20000, the table [0x20000,
-// 0x30000), then more stage slots up to the end of the allocation.
+// [base, +lead) barriers, counters and extra activation columns, [+lead,
+// +lead + red) warp partials, then 1024-byte aligned stage slots up to the
+// table at 0x20000, the table [0x20000, 0x30000), then more stage slots up
+// to the end of the allocation.
 struct Layout {
   uint32_t base, red, a0, b0;
   int na, S;
 };
-__device__ __forceinline__ Layout make_layout(uint32_t base, uint32_t bytes) {
+__device__ __forceinline__ Layout make_layout(uint32_t base, uint32_t bytes,
+                                              uint32_t lead = kMiscBytes,
+                                              uint32_t red_bytes = kRedBytes) {
   Layout L;
   L.base = base;
-  L.red = base + kMiscBytes;
-  L.a0 = (L.red + kRedBytes + 1023u) & ~1023u;
+  L.red = base + lead;
+  L.a0 = (L.red + red_bytes + 1023u) & ~1023u;
   L.b0 = kTabAddr + kTabBytes;
   const uint32_t end = base + bytes;
   L.na = L.a0 <= kTabAddr ? static_cast<int>((kTabAddr - L.a0) / kStage) : -1;
@@ -449,6 +459,359 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_kernel(const __grid_const
   }
 }
 
+// The same GEMV for MC activation columns (2 or 4; M <= MC of them exist),
+// same warps, stages and decode: the B operand of
+// m16n8k16 has eight columns, so lane (g, t) supplies activation column g %
+// M and the decoded codes, the shared-memory lookups and the MMAs serve
+// every column at once; lane (g, t) then holds the sums of columns 2t and 2t
+// + 1.  Column 0 sits in the table's gaps; columns 1.. M - 1 in their own
+// region after the barriers ([column - 1][block][64 f16]).  Each column has
+// its own power-of-two scale.
+template <int P, bool kArgmax, int MC>
+__global__ void __launch_bounds__(kThreads, 1) nf4_mma_mc_kernel(const __grid_constant__ CUtensorMap tq,
+                                                             const __grid_constant__ CUtensorMap ta,
+                                                             Codebook16 cb, float cb_scale,
+                                                             float cb_inv,
+                                                             const __nv_bfloat16* __restrict__ x,
+                                                             int64_t ldx, int M,
+                                                             __nv_bfloat16* __restrict__ y, int N,
+                                                             int K, uint32_t smem_bytes,
+                                                             int max_stages, ArgmaxArgs am,
+                                                             int* err) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t base = smem_addr(smem);
+  const int nbk = K / 64;
+  // extra activation columns right after the barriers, then the partials
+  // [S][8 K groups][64 rows][MC] sized for the deepest ring that fits
+  const uint32_t xcol = base + kMiscBytes;
+  static_assert(MC == 2 || MC == 4, "two or four columns");
+  const uint32_t xbytes = static_cast<uint32_t>(M - 1) * nbk * 128u;
+  Layout L{};
+  for (int s_try = kMaxStages; s_try >= 2; --s_try) {
+    L = make_layout(base, smem_bytes, kMiscBytes + xbytes,
+                    static_cast<uint32_t>(s_try) * kKG * kRB * 4 * MC);
+    if (L.S >= s_try) {
+      L.S = s_try;
+      break;
+    }
+    L.S = 0;
+  }
+  auto gen = [&](uint32_t a) { return smem + (a - base); };
+  uint64_t* full = reinterpret_cast<uint64_t*>(gen(base));              // [4]
+  uint64_t* empty = full + kMaxStages;                                   // [4]
+  uint64_t* keys = reinterpret_cast<uint64_t*>(gen(base + 64));          // [MC]
+  unsigned* nissue = reinterpret_cast<unsigned*>(gen(base + 128));       // [4]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gen(base + 160));
+  uint16_t* cbh = reinterpret_cast<uint16_t*>(gen(base + 192));          // [16]
+  float* wmax = reinterpret_cast<float*>(gen(base + 224));               // [16 warps][MC], to base + 480
+  float* red = reinterpret_cast<float*>(gen(L.red));                     // [S][8][64][MC]
+  const int S = L.S < max_stages ? L.S : max_stages;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int spb = K / kKS;                  // stages per row block
+  const int nblk = (N + kRB - 1) / kRB;
+  const int T = static_cast<int>(blockIdx.x) < nblk
+                    ? (nblk - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                    : 0;
+  const int total = T * spb;                // stages this CTA streams
+  if (S < 2) {                              // no room for two stages: refuse, touch nothing
+    if (tid == 0 && err) atomicExch(err, kErrGemvWait);
+    return;
+  }
+
+  // stage j (row block j / spb, K part j % spb) -> slot j % S; lane 0 of the
+  // producer warp calls it
+  auto issue = [&](int j) {
+    const int s = j % S;
+    const uint32_t st = slot_addr(L, s);
+    const int row0 = (static_cast<int>(blockIdx.x) + (j / spb) * static_cast<int>(gridDim.x)) * kRB;
+    const int k0 = (j % spb) * (kKS / 2);   // byte column of the codes
+    nissue[s] += 1u;
+    mbar_expect_tx(full + s, kStageTx);
+#pragma unroll
+    for (int bx = 0; bx < 4; ++bx) tma_load_2d(st + bx * 8192, &tq, k0 + bx * 128, row0, full + s);
+    tma_load_2d(st + 4 * 8192, &ta, (j % spb) * (kKS / 64), row0, full + s);
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, kCW);
+    }
+    mbar_fence_init();
+    *abort_flag = 0;
+  }
+  if (tid < kMaxStages) nissue[tid] = 0u;
+  if (tid < 16) {
+    float v = cb.v[0];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) v = tid == i ? cb.v[i] : v;
+    cbh[tid] = __half_as_ushort(__float2half_rn(v * cb_scale));
+  }
+  __syncthreads();
+  if (tid == kCW * 32)
+    for (int j = 0; j < S && j < total; ++j) issue(j);
+  pdl_launch_dependents();
+
+  Planes pl;
+  if (warp < kCW) {
+    // the codebook as the shared table (every entry's 32 lane words) and as
+    // byte planes
+    for (int i = tid; i < 256 * 32; i += kCW * 32) {
+      const int e = i >> 5, l = i & 31;
+      sts32(kTabAddr + e * 256 + l * 4,
+            static_cast<uint32_t>(cbh[e >> 4]) | (static_cast<uint32_t>(cbh[e & 15]) << 16));
+    }
+    auto lob = [&](int i) { return static_cast<uint32_t>(cbh[i] & 0xFFu); };
+    auto hib = [&](int i) { return static_cast<uint32_t>(cbh[i] >> 8); };
+    pl.la0 = lob(0) | lob(1) << 8 | lob(2) << 16 | lob(3) << 24;
+    pl.la1 = lob(4) | lob(5) << 8 | lob(6) << 16 | lob(7) << 24;
+    pl.lb0 = lob(8) | lob(9) << 8 | lob(10) << 16 | lob(11) << 24;
+    pl.lb1 = lob(12) | lob(13) << 8 | lob(14) << 16 | lob(15) << 24;
+    pl.ha0 = hib(0) | hib(1) << 8 | hib(2) << 16 | hib(3) << 24;
+    pl.ha1 = hib(4) | hib(5) << 8 | hib(6) << 16 | hib(7) << 24;
+    pl.hb0 = hib(8) | hib(9) << 8 | hib(10) << 16 | hib(11) << 24;
+    pl.hb1 = hib(12) | hib(13) << 8 | hib(14) << 16 | hib(15) << 24;
+  }
+  pdl_wait();
+  // activations -> f16: block c of column 0 at kTabAddr + c * 256 + 128, of
+  // column m >= 1 at xcol + ((m - 1) * nbk + c) * 128 (elements in order),
+  // each column scaled by one power of two that puts its max |x| in [2^14,
+  // 2^15): the maxima first (warp w takes blocks w, w + 16, ...), then the
+  // conversion
+  auto xaddr = [&](int m, int c) -> uint32_t {
+    return m == 0 ? kTabAddr + c * 256 + 128 : xcol + ((m - 1) * nbk + c) * 128;
+  };
+  if (warp < kCW) {
+    float mx[MC];
+#pragma unroll
+    for (int m = 0; m < MC; ++m) mx[m] = 0.f;
+    for (int c = warp; c < nbk; c += kCW) {
+#pragma unroll
+      for (int m = 0; m < MC; ++m)
+        if (m < M) {
+          const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(x + m * ldx + c * 64) + lane);
+          mx[m] = fmaxf(mx[m], fmaxf(fabsf(__uint_as_float(v << 16)), fabsf(__uint_as_float(v & 0xFFFF0000u))));
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MC; ++m) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx[m] = fmaxf(mx[m], __shfl_xor_sync(0xffffffffu, mx[m], o));
+      if (lane == 0) wmax[warp * MC + m] = mx[m];
+    }
+  }
+  __syncthreads();
+  float xs[MC], xinv[MC];
+#pragma unroll
+  for (int m = 0; m < MC; ++m) {
+    float mx = 0.f;
+#pragma unroll
+    for (int w2 = 0; w2 < kCW; ++w2) mx = fmaxf(mx, wmax[w2 * MC + m]);
+    pow2_scale(mx, xs[m], xinv[m]);
+  }
+  if (warp < kCW) {
+    for (int c = warp; c < nbk; c += kCW) {
+#pragma unroll
+      for (int m = 0; m < MC; ++m)
+        if (m < M) {
+          const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(x + m * ldx + c * 64) + lane);
+          const __half2 h2 = __floats2half2_rn(__uint_as_float(v << 16) * xs[m],
+                                               __uint_as_float(v & 0xFFFF0000u) * xs[m]);
+          sts32(xaddr(m, c) + 4 * lane, *reinterpret_cast<const uint32_t*>(&h2));
+        }
+    }
+  }
+  __syncthreads();                          // table and activation blocks complete
+
+  uint64_t best[MC];
+#pragma unroll
+  for (int m = 0; m < MC; ++m) best[m] = 0;
+  bool ok = true;
+  if (warp < kCW) {
+    // ------------------------------------------------------------ compute
+    const int rh = warp & 1, q = warp >> 1;
+    const uint32_t tl = kTabAddr | (static_cast<uint32_t>(lane) << 2);
+    // this lane's activation column (B column g) and its block stride
+    const int xm = g % M;
+    const uint32_t xb = xaddr(xm, 0) + 32 * t, xst = xm == 0 ? 256u : 128u;
+    // output scales of the two columns this lane's sums belong to
+    // (lanes t = 0, 1 carry columns 0..3; the others' sums are not used)
+    float om0 = xinv[0] * cb_inv, om1 = xinv[1] * cb_inv;
+    if constexpr (MC == 4) {
+      const float e0 = xinv[0] * cb_inv, e1 = xinv[1] * cb_inv;
+      const float e2 = xinv[2] * cb_inv, e3 = xinv[3] * cb_inv;
+      om0 = (t & 1) ? e2 : e0;
+      om1 = (t & 1) ? e3 : e1;
+    }
+    // rows of MMA row g in row tile u: 32 rh + 16 u + 2g, and + 1 for MMA
+    // row g + 8.  This lane's 8 code bytes of block b of a row: logical
+    // 16-byte chunk 4 (q & 1) + 2b + t / 2 of box q / 2, stored at chunk ^
+    // (row & 7); the odd row's chunk differs by one in bit 0.
+    const int r0 = 32 * rh + 2 * g;
+    const uint32_t swz = (2 * g) & 7;
+    uint32_t co[2][2];                      // [block][row parity] byte offsets in the stage
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const uint32_t c = 4 * (q & 1) + 2 * b + (t >> 1);
+      co[b][0] = (q >> 1) * 8192 + r0 * 128 + ((c ^ swz) << 4) + 8 * (t & 1);
+      co[b][1] = (q >> 1) * 8192 + (r0 + 1) * 128 + ((c ^ swz ^ 1u) << 4) + 8 * (t & 1);
+    }
+    // absmax box: 64-byte rows in the 64-byte swizzle (16-byte chunk index ^=
+    // (row >> 1) & 3); this lane's pair of K group q is chunk q / 2, half q & 1
+    const uint32_t abs_off = 4 * 8192 + r0 * 64 + ((((q >> 1) ^ g) & 3) << 4) + 8 * (q & 1);
+    constexpr int NH = 2;                   // output columns per lane
+    float acc[2][2][NH];                    // [row tile][row parity][column]
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int p2 = 0; p2 < 2; ++p2)
+#pragma unroll
+        for (int h = 0; h < NH; ++h) acc[u][p2][h] = 0.f;
+    int s = 0, ks = 0;
+    uint32_t ph = 0;
+    uint32_t st = slot_addr(L, 0);
+    for (int j = 0; j < total; ++j) {
+      if (*abort_flag) break;
+      if (!mbar_wait(full + s, ph)) {
+        ok = false;
+        *abort_flag = 1;
+        break;
+      }
+      st = launder(st);
+      float amx[2][2][2];                   // [row tile][row parity][block]
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int p2 = 0; p2 < 2; ++p2) {
+          const uint2 a = lds64(st + abs_off + (16 * u + p2) * 64);
+          amx[u][p2][0] = __uint_as_float(a.x);
+          amx[u][p2][1] = __uint_as_float(a.y);
+        }
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t xa = xb + (ks * 16 + 2 * q + b) * xst;
+        const uint4 xv0 = lds128(xa), xv1 = lds128(xa + 16);
+        const uint32_t xf[8] = {xv0.x, xv0.y, xv0.z, xv0.w, xv1.x, xv1.y, xv1.z, xv1.w};
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint2 wg = lds64(st + co[b][0] + u * 16 * 128);
+          const uint2 wh = lds64(st + co[b][1] + u * 16 * 128);
+          const uint32_t words[4] = {wg.x, wg.y, wh.x, wh.y};
+          uint32_t r[4][4];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            // P of every 8 code words (two blocks) through the register planes
+            if (4 * b + qq >= 8 - P) decode_planes(words[qq], pl, r[qq]);
+            else decode_table(words[qq], tl, r[qq]);
+          }
+          float d[4];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            // MMA m: bytes 2m, 2m + 1 of the lane's 8 bytes of both rows
+            const int wq = m >> 1, jj = 2 * (m & 1);
+            const uint32_t a[4] = {r[wq][jj], r[2 + wq][jj], r[wq][jj + 1], r[2 + wq][jj + 1]};
+            if (m == 0) mma16816_z(d, a, xf[0], xf[1]);
+            else mma16816(d, a, xf[2 * m], xf[2 * m + 1]);
+          }
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            acc[u][0][h] = fmaf(amx[u][0][b], d[h], acc[u][0][h]);
+            acc[u][1][h] = fmaf(amx[u][1][b], d[2 + h], acc[u][1][h]);
+          }
+        }
+      }
+      if (ks == spb - 1) {
+        // row block complete for this warp: its row partials, then a fresh start
+        if (2 * t < MC) {
+          float* rs = red + ((s * kKG + q) * kRB + r0) * MC + 2 * t;
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int p2 = 0; p2 < 2; ++p2) {
+              rs[(16 * u + p2) * MC] = acc[u][p2][0] * om0;
+              rs[(16 * u + p2) * MC + 1] = acc[u][p2][NH - 1] * om1;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int p2 = 0; p2 < 2; ++p2)
+#pragma unroll
+            for (int h = 0; h < NH; ++h) acc[u][p2][h] = 0.f;
+      }
+      __syncwarp();
+      if (lane == 0)
+        mbar_arrive_after(empty + s, acc[0][0][0], acc[0][1][0], acc[1][0][0], acc[1][1][NH - 1]);
+      if (++ks == spb) ks = 0;
+      if (++s == S) { s = 0; ph ^= 1u; }
+      st = slot_addr(L, s);
+    }
+  } else {
+    // ----------------------------------------------------------- produce
+    int s = 0;
+    uint32_t ph = 0;
+    for (int j = 0; j < total; ++j) {
+      if (*abort_flag) break;
+      if (!mbar_wait(empty + s, ph)) {
+        ok = false;
+        *abort_flag = 1;
+        break;
+      }
+      if (j % spb == spb - 1) {
+        // every compute warp has left its partials of this row block in slot s:
+        // rows lane and lane + 32, K groups added in order
+        const int row0 = (static_cast<int>(blockIdx.x) + (j / spb) * static_cast<int>(gridDim.x)) * kRB;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int rr = lane + 32 * hh, row = row0 + rr;
+          if (row < N) {
+#pragma unroll
+            for (int m = 0; m < MC; ++m) {
+              if (m < M) {
+                const float* rs = red + (s * kKG * kRB + rr) * MC + m;
+                float v = rs[0];
+#pragma unroll
+                for (int q2 = 1; q2 < kKG; ++q2) v += rs[q2 * kRB * MC];
+                const __nv_bfloat16 o = __float2bfloat16_rn(v);
+                y[static_cast<int64_t>(m) * N + row] = o;
+                if (kArgmax) {
+                  const uint64_t k = argmax_key(__bfloat162float(o), static_cast<uint32_t>(row));
+                  best[m] = k > best[m] ? k : best[m];
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+      }
+      if (j + S < total && lane == 0) issue(j + S);
+      __syncwarp();
+      if (++s == S) { s = 0; ph ^= 1u; }
+    }
+  }
+  if (!ok && lane == 0 && err) atomicExch(err, kErrGemvWait);
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    // let every issued copy land before the CTA's shared memory is released
+    for (int s2 = 0; s2 < S; ++s2)
+      if (nissue[s2] > 0u) mbar_wait(full + s2, (nissue[s2] - 1u) & 1u);
+  }
+  if (kArgmax) {
+    // only the producer warp folds outputs into the keys
+    if (warp == kCW) {
+#pragma unroll
+      for (int m = 0; m < MC; ++m) {
+        const uint64_t k = warp_max_u64(best[m]);
+        if (lane == 0) keys[m] = k;
+      }
+    }
+    __syncthreads();
+    argmax_publish(keys, M, am, gridDim.x);
+  }
+}
+
 // 2-D tensor map over a row-major [rows][cols] matrix (row pitch `ld`
 // bytes), no fill beyond the edges other than zeros.
 bool make_map(CUtensorMap* map, CUtensorMapDataType type, int esize, const void* ptr, int64_t cols,
@@ -465,11 +828,14 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType type, int esize, const void*
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int P, bool kArgmax>
+template <int P, bool kArgmax, int MC>
 cudaError_t run_p(const uint8_t* qs, const float* absmax, const Codebook16& cb, float cb_scale,
-                  float cb_inv, const void* x, void* y, int N, int K, const ArgmaxArgs& am,
-                  cudaStream_t st, Launch* info) {
-  auto kern = nf4_mma_kernel<P, kArgmax>;
+                  float cb_inv, const void* x, int64_t ldx, int M, void* y, int N, int K,
+                  const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
+  auto kern = [] {
+    if constexpr (MC == 1) return nf4_mma_kernel<P, kArgmax>;
+    else return nf4_mma_mc_kernel<P, kArgmax, MC>;
+  }();
   // all the opt-in shared memory the static part leaves, set up once (-1 if
   // the attribute calls fail)
   static const int smem = [&] {
@@ -505,24 +871,40 @@ cudaError_t run_p(const uint8_t* qs, const float* absmax, const Codebook16& cb, 
   // caps it, for measurements)
   const char* sv = std::getenv("WOBS_NF4_STAGES");
   const int max_stages = sv ? std::atoi(sv) : kMaxStages;
-  return launch_k(kern, dim3(grid), dim3(kThreads), smem, st, true, tq, ta, cb, cb_scale, cb_inv,
-                  static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, K,
-                  static_cast<uint32_t>(smem), max_stages < 2 ? 2 : max_stages, am,
-                  error_word_ptr());
+  const int ms = max_stages < 2 ? 2 : max_stages;
+  if constexpr (MC == 1)
+    return launch_k(kern, dim3(grid), dim3(kThreads), smem, st, true, tq, ta, cb, cb_scale, cb_inv,
+                    static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), N, K,
+                    static_cast<uint32_t>(smem), ms, am, error_word_ptr());
+  else
+    return launch_k(kern, dim3(grid), dim3(kThreads), smem, st, true, tq, ta, cb, cb_scale, cb_inv,
+                    static_cast<const __nv_bfloat16*>(x), ldx, M, static_cast<__nv_bfloat16*>(y), N,
+                    K, static_cast<uint32_t>(smem), ms, am, error_word_ptr());
 }
 
-template <bool kArgmax>
+template <bool kArgmax, int MC>
 cudaError_t run(const uint8_t* qs, const float* absmax, const Codebook16& cb, float cb_scale,
-                float cb_inv, const void* x, void* y, int N, int K, const ArgmaxArgs& am,
-                cudaStream_t st, Launch* info) {
+                float cb_inv, const void* x, int64_t ldx, int M, void* y, int N, int K,
+                const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   // code words per 8 decoded through the register planes instead of the
   // shared table (WOBS_NF4_P = 0..3 overrides the default)
   const char* v = std::getenv("WOBS_NF4_P");
   const int p = v ? std::atoi(v) : 1;
-  if (p == 0) return run_p<0, kArgmax>(qs, absmax, cb, cb_scale, cb_inv, x, y, N, K, am, st, info);
-  if (p == 2) return run_p<2, kArgmax>(qs, absmax, cb, cb_scale, cb_inv, x, y, N, K, am, st, info);
-  if (p == 3) return run_p<3, kArgmax>(qs, absmax, cb, cb_scale, cb_inv, x, y, N, K, am, st, info);
-  return run_p<1, kArgmax>(qs, absmax, cb, cb_scale, cb_inv, x, y, N, K, am, st, info);
+  if (p == 0)
+    return run_p<0, kArgmax, MC>(qs, absmax, cb, cb_scale, cb_inv, x, ldx, M, y, N, K, am, st, info);
+  if (p == 2)
+    return run_p<2, kArgmax, MC>(qs, absmax, cb, cb_scale, cb_inv, x, ldx, M, y, N, K, am, st, info);
+  if (p == 3)
+    return run_p<3, kArgmax, MC>(qs, absmax, cb, cb_scale, cb_inv, x, ldx, M, y, N, K, am, st, info);
+  return run_p<1, kArgmax, MC>(qs, absmax, cb, cb_scale, cb_inv, x, ldx, M, y, N, K, am, st, info);
+}
+
+template <int MC>
+cudaError_t run_mc(const uint8_t* qs, const float* absmax, const Codebook16& cb, float cb_scale,
+                   float cb_inv, const void* x, int64_t ldx, int M, void* y, int N, int K,
+                   const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
+  return am.out ? run<true, MC>(qs, absmax, cb, cb_scale, cb_inv, x, ldx, M, y, N, K, am, st, info)
+                : run<false, MC>(qs, absmax, cb, cb_scale, cb_inv, x, ldx, M, y, N, K, am, st, info);
 }
 
 }  // namespace
@@ -549,18 +931,20 @@ bool nf4_codebook_scale(const Codebook16& cb, float* scale, float* inv) {
 }
 
 cudaError_t launch_nf4_mma(const uint8_t* qs, const float* absmax, const Codebook16& cb,
-                           const void* x, void* y, int N, int K, const ArgmaxArgs& am,
-                           cudaStream_t st, Launch* info) {
+                           const void* x, int64_t ldx, int M, void* y, int N, int K,
+                           const ArgmaxArgs& am, cudaStream_t st, Launch* info) {
   float sc, inv;
   if (!nf4_codebook_scale(cb, &sc, &inv)) return cudaErrorNotSupported;
   if (reinterpret_cast<uintptr_t>(qs) % 16 || reinterpret_cast<uintptr_t>(absmax) % 16 ||
       reinterpret_cast<uintptr_t>(x) % 16)
     return cudaErrorNotSupported;
   // stages of 1024 codes per row; at most 128 blocks of 64, the activation
-  // blocks the table's gaps hold
-  if (K % kKS != 0 || K > 8192) return cudaErrorNotSupported;
-  return am.out ? run<true>(qs, absmax, cb, sc, inv, x, y, N, K, am, st, info)
-                : run<false>(qs, absmax, cb, sc, inv, x, y, N, K, am, st, info);
+  // blocks the table's gaps hold; up to four columns, rows 16-byte aligned
+  if (K % kKS != 0 || K > 8192 || M < 1 || M > 4) return cudaErrorNotSupported;
+  if (M > 1 && (ldx % 8 != 0)) return cudaErrorNotSupported;
+  if (M == 1) return run_mc<1>(qs, absmax, cb, sc, inv, x, K, 1, y, N, K, am, st, info);
+  if (M == 2) return run_mc<2>(qs, absmax, cb, sc, inv, x, ldx, M, y, N, K, am, st, info);
+  return run_mc<4>(qs, absmax, cb, sc, inv, x, ldx, M, y, N, K, am, st, info);
 }
 
 }  // namespace wobs

@@ -466,7 +466,11 @@ Q4Plan q4_plan(int M, int N, int K, int forced) {
     p.splits = (nb + kpb - 1) / kpb;
     return p;
   }
-  const int want = 4 * device_sm_count();
+  // (row group, K range) units to aim for: 4 per SM, 8 per SM for up to 8
+  // columns (two CTAs of 8 warps per SM; GB300, 8 columns on 4096^2: 8 K
+  // ranges 6.63 us against 4 ranges 7.13; 14336 x 4096 keeps 4 ranges,
+  // 13.5 us against 14.9 with 8)
+  const int want = (p.nt == 1 ? 8 : 4) * device_sm_count();
   for (int kpb = kQKB; kpb >= kQSB; kpb /= 2) {
     p.kpb = kpb;
     p.splits = (nb + kpb - 1) / kpb;
