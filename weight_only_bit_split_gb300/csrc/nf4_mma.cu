@@ -41,9 +41,9 @@
 //     (0x20000 | lane * 4), with no add;
 //   * two to four columns share every decoded code: the MMA's B operand
 //     has eight columns, lane (g, t) supplies column g % M, and the sums of
-//     columns 2t and 2t + 1 come back in lane (g, t).  The extra columns'
-//     activations need shared memory beside the table, so the ring has
-//     three stages for two columns and two for four.  One column keeps its
+//     columns 2t and 2t + 1 come back in lane (g, t).  Column 1 fits in the
+//     table's unused gaps; columns 2 and 3 need shared memory beside it, so
+//     the ring has four stages for two columns and three for four.  One column keeps its
 //     own kernel: the column form instantiated for one column ran 2 us
 //     slower on the 70B matrix (28.9 against 26.9 us).
 #include <cmath>
@@ -464,9 +464,14 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_kernel(const __grid_const
 // m16n8k16 has eight columns, so lane (g, t) supplies activation column g %
 // M and the decoded codes, the shared-memory lookups and the MMAs serve
 // every column at once; lane (g, t) then holds the sums of columns 2t and 2t
-// + 1.  Column 0 sits in the table's gaps; columns 1.. M - 1 in their own
-// region after the barriers ([column - 1][block][64 f16]).  Each column has
-// its own power-of-two scale.
+// + 1.  Columns 0 and 1 sit in the table's gaps (entries 0..127 and
+// 128..255; K <= 8192 is at most 128 blocks), columns 2.. M - 1 in their
+// own region after the barriers ([column - 2][block][64 f16]); column 1's
+// 16-byte pieces are stored rotated by one place.  Each column has its own
+// power-of-two scale.  The K-group partials need one buffer
+// when a row block spans more stages than the ring holds (no warp can then
+// reach the next row block's end before the copy warp has read them), else
+// one per slot.
 template <int P, bool kArgmax, int MC>
 __global__ void __launch_bounds__(kThreads, 1) nf4_mma_mc_kernel(const __grid_constant__ CUtensorMap tq,
                                                              const __grid_constant__ CUtensorMap ta,
@@ -481,15 +486,18 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_mc_kernel(const __grid_co
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t base = smem_addr(smem);
   const int nbk = K / 64;
-  // extra activation columns right after the barriers, then the partials
-  // [S][8 K groups][64 rows][MC] sized for the deepest ring that fits
+  // activation columns 2.. right after the barriers, then the partials
+  // [nred][8 K groups][64 rows][MC], for the deepest ring that fits
   const uint32_t xcol = base + kMiscBytes;
   static_assert(MC == 2 || MC == 4, "two or four columns");
-  const uint32_t xbytes = static_cast<uint32_t>(M - 1) * nbk * 128u;
+  const int spb0 = K / kKS;
+  const uint32_t xbytes = M > 2 ? static_cast<uint32_t>(M - 2) * nbk * 128u : 0u;
   Layout L{};
+  int nred = 1;
   for (int s_try = kMaxStages; s_try >= 2; --s_try) {
+    nred = spb0 > s_try ? 1 : s_try;
     L = make_layout(base, smem_bytes, kMiscBytes + xbytes,
-                    static_cast<uint32_t>(s_try) * kKG * kRB * 4 * MC);
+                    static_cast<uint32_t>(nred) * kKG * kRB * 4 * MC);
     if (L.S >= s_try) {
       L.S = s_try;
       break;
@@ -576,12 +584,13 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_mc_kernel(const __grid_co
   }
   pdl_wait();
   // activations -> f16: block c of column 0 at kTabAddr + c * 256 + 128, of
-  // column m >= 1 at xcol + ((m - 1) * nbk + c) * 128 (elements in order),
+  // column 1 at kTabAddr + (128 + c) * 256 + 128, of column m >= 2 at xcol +
+  // ((m - 2) * nbk + c) * 128 (elements in order),
   // each column scaled by one power of two that puts its max |x| in [2^14,
   // 2^15): the maxima first (warp w takes blocks w, w + 16, ...), then the
   // conversion
   auto xaddr = [&](int m, int c) -> uint32_t {
-    return m == 0 ? kTabAddr + c * 256 + 128 : xcol + ((m - 1) * nbk + c) * 128;
+    return m < 2 ? kTabAddr + (128 * m + c) * 256 + 128 : xcol + ((m - 2) * nbk + c) * 128;
   };
   if (warp < kCW) {
     float mx[MC];
@@ -619,7 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_mc_kernel(const __grid_co
           const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(x + m * ldx + c * 64) + lane);
           const __half2 h2 = __floats2half2_rn(__uint_as_float(v << 16) * xs[m],
                                                __uint_as_float(v & 0xFFFF0000u) * xs[m]);
-          sts32(xaddr(m, c) + 4 * lane, *reinterpret_cast<const uint32_t*>(&h2));
+          // column 1's 16-byte pieces rotated by one: its lanes then read
+          // other banks than column 0's in the same load
+          const uint32_t o = m == 1 ? ((((lane >> 2) + 1) & 7) << 4) | ((4 * lane) & 15) : 4 * lane;
+          sts32(xaddr(m, c) + o, *reinterpret_cast<const uint32_t*>(&h2));
         }
     }
   }
@@ -635,7 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_mc_kernel(const __grid_co
     const uint32_t tl = kTabAddr | (static_cast<uint32_t>(lane) << 2);
     // this lane's activation column (B column g) and its block stride
     const int xm = g % M;
-    const uint32_t xb = xaddr(xm, 0) + 32 * t, xst = xm == 0 ? 256u : 128u;
+    const uint32_t xb = xaddr(xm, 0), xst = xm < 2 ? 256u : 128u;
+    const uint32_t xo0 = xm == 1 ? ((2 * t + 1) & 7) << 4 : 32 * t;
+    const uint32_t xo1 = xm == 1 ? ((2 * t + 2) & 7) << 4 : 32 * t + 16;
     // output scales of the two columns this lane's sums belong to
     // (lanes t = 0, 1 carry columns 0..3; the others' sums are not used)
     float om0 = xinv[0] * cb_inv, om1 = xinv[1] * cb_inv;
@@ -692,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_mc_kernel(const __grid_co
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
         const uint32_t xa = xb + (ks * 16 + 2 * q + b) * xst;
-        const uint4 xv0 = lds128(xa), xv1 = lds128(xa + 16);
+        const uint4 xv0 = lds128(xa + xo0), xv1 = lds128(xa + xo1);
         const uint32_t xf[8] = {xv0.x, xv0.y, xv0.z, xv0.w, xv1.x, xv1.y, xv1.z, xv1.w};
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -725,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_mc_kernel(const __grid_co
       if (ks == spb - 1) {
         // row block complete for this warp: its row partials, then a fresh start
         if (2 * t < MC) {
-          float* rs = red + ((s * kKG + q) * kRB + r0) * MC + 2 * t;
+          float* rs = red + (((nred == 1 ? 0 : s) * kKG + q) * kRB + r0) * MC + 2 * t;
 #pragma unroll
           for (int u = 0; u < 2; ++u)
 #pragma unroll
@@ -770,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) nf4_mma_mc_kernel(const __grid_co
 #pragma unroll
             for (int m = 0; m < MC; ++m) {
               if (m < M) {
-                const float* rs = red + (s * kKG * kRB + rr) * MC + m;
+                const float* rs = red + ((nred == 1 ? 0 : s) * kKG * kRB + rr) * MC + m;
                 float v = rs[0];
 #pragma unroll
                 for (int q2 = 1; q2 < kKG; ++q2) v += rs[q2 * kRB * MC];
