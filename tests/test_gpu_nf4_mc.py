@@ -60,7 +60,8 @@ def mc_path(request, monkeypatch):
 @pytest.mark.parametrize("n,k,m", [(300, 1024, 2), (1000, 4096, 5), (129, 256, 16), (2000, 2048, 17),
                                    (640, 8192, 32), (4096, 1024, 32), (77, 512, 3), (1, 768, 9),
                                    (5003, 2048, 8), (1000, 8192, 4), (5003, 4096, 3), (64, 2048, 2),
-                                   (4097, 1024, 4)])
+                                   (4097, 1024, 4), (3000, 8192, 8), (777, 8192, 5), (130, 1024, 7),
+                                   (9000, 8192, 6)])
 def test_nf4_columns_match_the_oracle(n, k, m, mc_path):
     cb, qs, absmax = _planes(n, k)
     xb = _x(m, k)
@@ -115,7 +116,8 @@ def test_nf4_columns_pitched_rows(m, mc_path):
 
 
 @pytest.mark.parametrize("muls", [(2.0 ** 40, 2.0 ** -40), (1.0, 2.0 ** -60, 2.0 ** 30),
-                                  (2.0 ** -30, 1.0, 2.0 ** 50, 3.0e-3)])
+                                  (2.0 ** -30, 1.0, 2.0 ** 50, 3.0e-3),
+                                  (1.0, 2.0 ** 40, 2.0 ** -40, 7.0, 2.0 ** -20, 2.0 ** 20, 0.1, 3.0e5)])
 def test_nf4_columns_far_apart_magnitudes(muls, mc_path):
     """Columns whose magnitudes differ by many powers of two: each column's
     own scaling must keep every column within its bound."""
@@ -141,7 +143,7 @@ def test_nf4_columns_scaled_inputs(xmul, cbmul):
     assert_within(y.float().cpu().numpy(), ref, ad, "bf16", f"nf4 columns x*{xmul} cb*{cbmul}")
 
 
-@pytest.mark.parametrize("m", [4, 24])
+@pytest.mark.parametrize("m", [4, 8, 24])
 def test_nf4_identical_columns_give_identical_outputs(m, mc_path):
     n, k = 1000, 2048
     cb, qs, absmax = _planes(n, k, copy=4)
@@ -152,8 +154,9 @@ def test_nf4_identical_columns_give_identical_outputs(m, mc_path):
     assert np.all(am.cpu().numpy() == am.cpu().numpy()[0])
 
 
-def test_nf4_columns_deterministic():
-    n, k, m = 3000, 8192, 32
+@pytest.mark.parametrize("m", [8, 32])
+def test_nf4_columns_deterministic(m):
+    n, k = 3000, 8192
     cb, qs, absmax = _planes(n, k, copy=5)
     xb = _x(m, k, copy=5).to(dev())
     qd, ad = to_dev(qs), to_dev(absmax)
@@ -184,7 +187,8 @@ def test_nf4_28672x8192_columns_full_sampled(m):
 @pytest.mark.parametrize("n,k,m,path", [(1000, 4096, 32, "tc"), (333, 1024, 5, "tc"),
                                         (5003, 8192, 17, "tc"), (700, 1088, 6, "cp"),
                                         (2049, 8192, 2, "mma"), (333, 1024, 3, "mma"),
-                                        (1000, 4096, 4, "mma")])
+                                        (1000, 4096, 4, "mma"), (2049, 8192, 7, "mma"),
+                                        (300, 4096, 8, "mma")])
 def test_nf4_columns_stay_in_bounds(n, k, m, path, monkeypatch):
     if path == "cp":
         monkeypatch.setenv("WOBS_NF4", "cp")
@@ -211,7 +215,8 @@ def test_nf4_columns_dispatch(monkeypatch, capfd):
     monkeypatch.setenv("WOBS_DEBUG", "1")
     monkeypatch.delenv("WOBS_NF4", raising=False)
     monkeypatch.delenv("WOBS_NF4_MC", raising=False)
-    for k, m in ((8192, 32), (4096, 2), (8192, 4), (2048, 5), (320, 4), (512, 2)):
+    for k, m in ((8192, 32), (4096, 2), (8192, 4), (2048, 5), (8192, 8), (8192, 9), (320, 4),
+                 (512, 2)):
         cb, qs, absmax = _planes(256, k)
         wobs.wobs_gemv_nf4(to_dev(qs), to_dev(absmax), cb, _x(m, k).to(dev()))
     monkeypatch.setenv("WOBS_NF4_MC", "tc")
@@ -220,7 +225,8 @@ def test_nf4_columns_dispatch(monkeypatch, capfd):
     torch.cuda.synchronize()
     err = capfd.readouterr().err
     kernels = [ln.split("kernel=")[1].split()[0] for ln in err.splitlines() if ln.startswith("wobs: op=")]
-    assert kernels == ["nf4_tc", "nf4_mma", "nf4_mma", "nf4_tc", "nf4_mn", "nf4_tc", "nf4_tc"], kernels
+    assert kernels == ["nf4_tc", "nf4_mma", "nf4_mma", "nf4_tc", "nf4_tc", "nf4_tc", "nf4_mn",
+                       "nf4_tc", "nf4_tc"], kernels
 
 
 # ------------------------------------------------------- dequantise -> GEMM
