@@ -251,6 +251,26 @@ def test_dequantize_nf4_pitched_output_stays_in_bounds():
                           oracle.dequantize_nf4_bf16(qs, absmax, cb))
 
 
+@pytest.mark.parametrize("pitch_extra", [2, 6, 8])
+def test_dequantize_nf4_any_even_pitch(pitch_extra, monkeypatch, capfd):
+    """Pitches that are not whole 16-byte pieces take the element kernel,
+    those that are take the row kernel; both bit-exact and in bounds."""
+    monkeypatch.setenv("WOBS_DEBUG", "1")
+    n, k = 130, 2048
+    cb, qs, absmax = _planes(n, k, copy=8)
+    g = guarded((n, k + pitch_extra), torch.bfloat16)
+    W = g[4][:, :k]
+    wobs.wobs_dequantize_nf4(to_dev(qs), to_dev(absmax), cb, W=W)
+    torch.cuda.synchronize()
+    check_guards(g, "dequantised W")
+    assert np.array_equal(W.contiguous().view(torch.int16).cpu().numpy().view(np.uint16),
+                          oracle.dequantize_nf4_bf16(qs, absmax, cb))
+    err = capfd.readouterr().err
+    kernels = [ln.split("kernel=")[1].split()[0] for ln in err.splitlines() if ln.startswith("wobs: op=")]
+    aligned = (k + pitch_extra) % 8 == 0 and W.data_ptr() % 16 == 0
+    assert kernels == ["dequantize_nf4_rows" if aligned else "dequantize_nf4"], kernels
+
+
 @pytest.mark.parametrize("n,k,m", [(1000, 4096, 1), (640, 2048, 40), (3000, 1024, 32)])
 def test_nf4_dequant_gemm_path(n, k, m):
     cb, qs, absmax = _planes(n, k, copy=9)
