@@ -429,6 +429,14 @@ bool m1_cp_applies(const void* d, int K) { return m1_cp_shape(d, K) && !m1_ldg_f
 
 // ------------------------------------- 2..8 columns, cp.async staging
 
+// The block dots of the few-column kernels start from kDotBias - 8 s (s the
+// block's Q8_1 code sum): the integer bits of float 1.5 * 2^23 plus the
+// exact dot Sum (q4 - 8) q8, whose magnitude stays below 2^22, are the bits
+// of the float 1.5 * 2^23 + dot, so one float subtraction yields the dot
+// exactly, with no integer-to-float conversion (a quarter-rate unit).
+constexpr int kDotBias = 0x4B400000;
+constexpr float kDotBiasF = 12582912.0f;
+
 // The M = 1 structure (warp per row, lanes along K, per-warp cp.async ring,
 // whole rows so no K split) for a few activation columns: each weight block
 // is unpacked once and dotted with MC columns.  The activation planes
@@ -488,11 +496,11 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc_cp_kernel(
       const XBlock xb = load_xblock(xq + 36 * (static_cast<int64_t>(m) * nb + b));
       x_lo[i] = xb.lo;
       x_hi[i] = xb.hi;
-      x_ds[i] = make_float2(xb.d, __int_as_float(xb.s));
+      x_ds[i] = make_float2(xb.d, __int_as_float(kDotBias - 8 * xb.s));
     } else {
       x_lo[i] = make_int4(0, 0, 0, 0);
       x_hi[i] = make_int4(0, 0, 0, 0);
-      x_ds[i] = make_float2(0.f, __int_as_float(0));
+      x_ds[i] = make_float2(0.f, __int_as_float(kDotBias));
     }
   }
   __syncthreads();
@@ -527,12 +535,12 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc_cp_kernel(
         for (int m = 0; m < MC; ++m) {
           const int4 xl = x_lo[m * nb + b], xh = x_hi[m * nb + b];
           const float2 ds = x_ds[m * nb + b];
-          int sdot = -8 * __float_as_int(ds.y);
+          int sdot = __float_as_int(ds.y);
           sdot = __dp4a(lo0, xl.x, sdot); sdot = __dp4a(lo1, xl.y, sdot);
           sdot = __dp4a(lo2, xl.z, sdot); sdot = __dp4a(lo3, xl.w, sdot);
           sdot = __dp4a(hi0, xh.x, sdot); sdot = __dp4a(hi1, xh.y, sdot);
           sdot = __dp4a(hi2, xh.z, sdot); sdot = __dp4a(hi3, xh.w, sdot);
-          acc[m] = fmaf(static_cast<float>(sdot), dw * ds.x, acc[m]);
+          acc[m] = fmaf(__int_as_float(sdot) - kDotBiasF, dw * ds.x, acc[m]);
         }
       }
     }
@@ -650,11 +658,11 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
       const XBlock xb = load_xblock(xq + 36 * (static_cast<int64_t>(m) * nb + b));
       x_lo[i] = xb.lo;
       x_hi[i] = xb.hi;
-      x_ds[i] = make_float2(xb.d, __int_as_float(xb.s));
+      x_ds[i] = make_float2(xb.d, __int_as_float(kDotBias - 8 * xb.s));
     } else {
       x_lo[i] = make_int4(0, 0, 0, 0);
       x_hi[i] = make_int4(0, 0, 0, 0);
-      x_ds[i] = make_float2(0.f, __int_as_float(0));
+      x_ds[i] = make_float2(0.f, __int_as_float(kDotBias));
     }
   }
   __syncthreads();
@@ -692,12 +700,12 @@ __global__ void __launch_bounds__(McShape<MC>::kThreads) q4_mc2_cp_kernel(
         for (int m = 0; m < MC; ++m) {
           const int4 xl = x_lo[m * nb + b], xh = x_hi[m * nb + b];
           const float2 ds = x_ds[m * nb + b];
-          int sdot = -8 * __float_as_int(ds.y);
+          int sdot = __float_as_int(ds.y);
           sdot = __dp4a(lo0, xl.x, sdot); sdot = __dp4a(lo1, xl.y, sdot);
           sdot = __dp4a(lo2, xl.z, sdot); sdot = __dp4a(lo3, xl.w, sdot);
           sdot = __dp4a(hi0, xh.x, sdot); sdot = __dp4a(hi1, xh.y, sdot);
           sdot = __dp4a(hi2, xh.z, sdot); sdot = __dp4a(hi3, xh.w, sdot);
-          acc[m] = fmaf(static_cast<float>(sdot), dw * ds.x, acc[m]);
+          acc[m] = fmaf(__int_as_float(sdot) - kDotBiasF, dw * ds.x, acc[m]);
         }
       }
     }
