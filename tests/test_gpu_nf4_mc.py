@@ -61,7 +61,7 @@ def mc_path(request, monkeypatch):
                                    (640, 8192, 32), (4096, 1024, 32), (77, 512, 3), (1, 768, 9),
                                    (5003, 2048, 8), (1000, 8192, 4), (5003, 4096, 3), (64, 2048, 2),
                                    (4097, 1024, 4), (3000, 8192, 8), (777, 8192, 5), (130, 1024, 7),
-                                   (9000, 8192, 6)])
+                                   (9000, 8192, 6), (1, 1024, 2), (65, 2048, 3), (63, 8192, 4)])
 def test_nf4_columns_match_the_oracle(n, k, m, mc_path):
     cb, qs, absmax = _planes(n, k)
     xb = _x(m, k)
