@@ -43,8 +43,17 @@ __device__ __forceinline__ float half_bits_to_float(uint16_t h) {
 }
 
 // Exact 32-element dot: sum over the 16 low-nibble and 16 high-nibble codes.
-__device__ __forceinline__ int q4_dot_u(uint4 q, int4 lo, int4 hi) {
-  int s = 0;
+// Block dots may start from kDotBias - 8 s (s the block's Q8_1 code sum):
+// the integer bits of float 1.5 * 2^23 plus the exact dot Sum (q4 - 8) q8,
+// whose magnitude stays below 2^22, are the bits of the float 1.5 * 2^23 +
+// dot, so one float subtraction yields the dot exactly, with no
+// integer-to-float conversion (a quarter-rate unit).
+constexpr int kDotBias = 0x4B400000;
+constexpr float kDotBiasF = 12582912.0f;
+
+// Sum of q4 * q8 over one block (codes 0..15, no offset), added to s0.
+__device__ __forceinline__ int q4_dot_u(uint4 q, int4 lo, int4 hi, int s0 = 0) {
+  int s = s0;
   s = __dp4a(static_cast<int>(q.x & 0x0F0F0F0Fu), lo.x, s);
   s = __dp4a(static_cast<int>(q.y & 0x0F0F0F0Fu), lo.y, s);
   s = __dp4a(static_cast<int>(q.z & 0x0F0F0F0Fu), lo.z, s);
@@ -259,7 +268,7 @@ __device__ __forceinline__ void q8_1_planes_tpb(const float* __restrict__ X, int
     }
     if (j == 0) {
       x_d[b] = __half2float(__float2half_rn(h.d));
-      x_s[b] = h.sum;
+      x_s[b] = kDotBias - 8 * h.sum;
     }
     // each 36-byte Q8_1 block written by one CTA
     if (xq_out != nullptr && b % static_cast<int>(gridDim.x) == static_cast<int>(blockIdx.x))
@@ -336,7 +345,7 @@ __global__ void __launch_bounds__(W * 32) q4_m1_cp_kernel(const uint8_t* __restr
       x_lo[b] = xb.lo;
       x_hi[b] = xb.hi;
       x_d[b] = xb.d;
-      x_s[b] = xb.s;
+      x_s[b] = kDotBias - 8 * xb.s;
     }
   }
   __syncthreads();
@@ -360,10 +369,10 @@ __global__ void __launch_bounds__(W * 32) q4_m1_cp_kernel(const uint8_t* __restr
         const uint4 q = *reinterpret_cast<const uint4*>(st + 16 * bl);
         const uint16_t dh = *reinterpret_cast<const uint16_t*>(st + kSegQs + 2 * bl);
         const int b = b0 + bl;
-        const int dot = q4_dot_u(q, x_lo[b], x_hi[b]) - 8 * x_s[b];
+        const float dot = __int_as_float(q4_dot_u(q, x_lo[b], x_hi[b], x_s[b])) - kDotBiasF;
         const float sc = half_bits_to_float(dh) * x_d[b];
-        if (u & 1) acc1 = fmaf(static_cast<float>(dot), sc, acc1);
-        else acc0 = fmaf(static_cast<float>(dot), sc, acc0);
+        if (u & 1) acc1 = fmaf(dot, sc, acc1);
+        else acc0 = fmaf(dot, sc, acc0);
       }
     }
     if (cseg == nseg - 1) {
@@ -428,14 +437,6 @@ bool m1_cp_shape(const void* d, int K) {
 bool m1_cp_applies(const void* d, int K) { return m1_cp_shape(d, K) && !m1_ldg_forced(); }
 
 // ------------------------------------- 2..8 columns, cp.async staging
-
-// The block dots of the few-column kernels start from kDotBias - 8 s (s the
-// block's Q8_1 code sum): the integer bits of float 1.5 * 2^23 plus the
-// exact dot Sum (q4 - 8) q8, whose magnitude stays below 2^22, are the bits
-// of the float 1.5 * 2^23 + dot, so one float subtraction yields the dot
-// exactly, with no integer-to-float conversion (a quarter-rate unit).
-constexpr int kDotBias = 0x4B400000;
-constexpr float kDotBiasF = 12582912.0f;
 
 // The M = 1 structure (warp per row, lanes along K, per-warp cp.async ring,
 // whole rows so no K split) for a few activation columns: each weight block
