@@ -62,7 +62,9 @@
  *     or 4 runs the 2..4-column Q4_0 kernel with that many weight rows per
  *     warp (the default picks by shape; testing only).  WOBS_NF4_MC=tc
  *     takes NF4 calls with 2..4 columns to the tensor-memory kernel instead
- *     of the mma.sync kernel (testing only).
+ *     of the mma.sync kernel (testing only).  WOBS_PDL=0 launches every
+ *     kernel without programmatic dependent launch (each then starts after
+ *     its predecessor has finished; for measurements).
  */
 #ifndef WOBS_H
 #define WOBS_H

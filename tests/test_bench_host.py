@@ -46,3 +46,15 @@ def test_sweeps_report_their_dominant_kernel_only():
     assert nf4.kernel == "nf4_tc"
     assert not any(nf4.roofline_call(f"M{m}") for m in nf4.Ms if m <= 4)
     assert all(nf4.roofline_call(f"M{m}") for m in nf4.Ms if m > 4)
+
+
+def test_every_environment_knob_is_documented():
+    """Each WOBS_* variable the library reads is described in the header."""
+    import re
+    csrc = os.path.join(ROOT, "weight_only_bit_split_gb300", "csrc")
+    names = set()
+    for f in os.listdir(csrc):
+        if f.endswith((".cu", ".cuh", ".h")):
+            names |= set(re.findall(r'getenv\("(WOBS_[A-Z0-9_]+)"\)', open(os.path.join(csrc, f)).read()))
+    header = open(os.path.join(ROOT, "include", "wobs.h")).read()
+    assert names and all(n in header for n in names), sorted(n for n in names if n not in header)
